@@ -1,0 +1,69 @@
+"""The oracle pins must reject a broken oracle (CPU only).
+
+Each case below plants one plausible mistake in a private copy of the oracle
+source (a wrong mean divisor, eps in the wrong place, a swapped sign, a wrong
+partner index, swapped q/k weights, a double rounding, ...), compiles it with
+gcc, and runs the pin suite against it.  The suite must fail for every
+mutant; a mutant that survives means the pins have a blind spot.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "rn_oracle.c")
+
+MUTANTS = {
+    "mean_divisor_n_minus_1": ("double ms = ss / (double)N;", "double ms = ss / (double)(N - 1);"),
+    "eps_on_sum": ("double ms = ss / (double)N;\n        double rs = 1.0 / sqrt(ms + deps);",
+                   "double ms = ss / (double)N;\n        double rs = 1.0 / sqrt((ss + deps) / (double)N);"),
+    "eps_outside_sqrt": ("double rs = 1.0 / sqrt(ms + deps);", "double rs = 1.0 / (sqrt(ms) + deps);"),
+    "no_weight": ("yr[j] = rn_oracle_double_to_bf16(v * rs * g);", "yr[j] = rn_oracle_double_to_bf16(v * rs + 0.0 * g);"),
+    "round_via_float": ("double n = nearbyint(v / q);", "double n = nearbyint((double)(float)v / q);"),
+    "ties_away": ("double n = nearbyint(v / q);", "double n = round(v / q);"),
+    "rope_sign_first": ("o[i] = n[i] * c - n[i + half] * s;", "o[i] = n[i] * c + n[i + half] * s;"),
+    "rope_sign_second": ("o[i + half] = n[i + half] * c + n[i] * s;", "o[i + half] = n[i + half] * c - n[i] * s;"),
+    "rope_partner_d_half": ("o[i] = n[i] * c - n[i + half] * s;", "o[i] = n[i] * c - n[i + D / 2] * s;"),
+    "rope_cos_sin_swapped": ("double c = (double)cs[i];\n                double s = (double)cs[half + i];",
+                             "double s = (double)cs[i];\n                double c = (double)cs[half + i];"),
+    "qk_weights_swapped": ("const uint16_t *w = (h < Hq) ? wq : wk;", "const uint16_t *w = (h < Hq) ? wk : wq;"),
+    "qk_mean_over_rotary": ("double rs = 1.0 / sqrt(ss / (double)D + deps);",
+                            "double rs = 1.0 / sqrt(ss / (double)rotary_dim + deps);"),
+    "qk_tail_dropped": ("for (int j = rotary_dim; j < D; ++j) o[j] = n[j];",
+                        "for (int j = rotary_dim; j < D; ++j) o[j] = 0.0;"),
+    "qk_touches_v": ("for (int h = 0; h < Hq + Hkv; ++h) {", "for (int h = 0; h < Hq + 2 * Hkv; ++h) {"),
+    "table_freq_over_d": ("double f = pow(theta, -2.0 * (double)i / (double)rotary_dim);",
+                          "double f = pow(theta, -1.0 * (double)i / (double)rotary_dim);"),
+    "table_sin_first": ("row[i] = (float)cos(a);\n            row[half + i] = (float)sin(a);",
+                        "row[i] = (float)sin(a);\n            row[half + i] = (float)cos(a);"),
+    "layernorm_unbiased": ("double rs = 1.0 / sqrt(m2 / (double)N + (double)eps);",
+                           "double rs = 1.0 / sqrt(m2 / (double)(N - 1) + (double)eps);"),
+    "layernorm_bias_dropped": ("if (b) v += rn_oracle_bf16_to_double(b[j]);", "(void)b;"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, mutant_dir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    c_path = mutant_dir / f"{name}.c"
+    so_path = mutant_dir / f"{name}.so"
+    c_path.write_text(mutated)
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so_path), str(c_path), "-lm"], check=True)
+    env = dict(os.environ, RN_ORACLE_LIB=str(so_path))
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode != 0, f"mutant {name} survived the pins:\n{res.stdout[-2000:]}"
