@@ -1,0 +1,530 @@
+#!/usr/bin/env python3
+"""Throughput of the bf16 row-normalization hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over resident synthetic inputs:
+  * RMSNorm over the sweep M in {4096, 8192, 16384, 32768} x N in {4096, 8192,
+    16384} (x ~ N(0,1) with 1% of rows scaled x100, w = 1 + 0.1 N(0,1),
+    eps 1e-6): 12 launches;
+  * fused Q/K RMSNorm + neox RoPE on packed QKV [16384, 48*128] (32 query and
+    8 key/value heads of 128, theta 1e6, positions uniform in [0, 131072)),
+    once with rotary_dim 128 and once with 64: 2 launches.
+The metric is achieved HBM bandwidth over the ideal bytes (each input read
+once, each output written once), in GB/s, whole job.  Device-side timing
+uses CUDA events on the launching stream; `e2e` repeats the step through the
+same C entry points with the inputs copied in from pinned host memory and
+the outputs copied back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --impl reference the CPU oracle (the plain fp64 implementation the tests
+use as the yardstick) is timed on the host cores on a bounded sample of the
+same workload.  Under torchrun with N > 1 every rank runs the same per-GPU
+workload (weak scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 peak for bf16 RMSNorm / QK-norm+RoPE"
+SPEC_GBS = 7928.0
+
+RMS_SHAPES = [(M, N) for M in (4096, 8192, 16384, 32768) for N in (4096, 8192, 16384)]
+RMS_EPS = 1e-6
+QK_T = 16384
+QK_ROT = (128, 64)
+HQ, HKV, D = 32, 8, 128
+MAX_POS = 131072
+THETA = 1e6
+QK_EPS = 1e-6
+WORKLOAD = ("rmsnorm sweep M{4096,8192,16384,32768}xN{4096,8192,16384} (1% outlier rows) + "
+            "qk_norm_rope T=16384 Hq=32 Hkv=8 D=128 rotary {128,64}")
+
+
+def rms_bytes(M: int, N: int) -> int:
+    """Ideal bytes: read x once, read w once, write y once."""
+    return 4 * M * N + 2 * N
+
+
+def qk_bytes(T: int, r: int) -> int:
+    """Ideal bytes: read+write every Q/K head (V untouched), one fp32 cos/sin
+    row and one int64 position per token, both weights once."""
+    return T * (2 * (HQ + HKV) * D * 2 + r * 4 + 8) + 2 * D * 2
+
+
+def step_bytes() -> int:
+    return sum(rms_bytes(M, N) for M, N in RMS_SHAPES) + sum(qk_bytes(QK_T, r) for r in QK_ROT)
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except (OSError, ValueError):
+        return {}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] is None or r["power"] > 200.0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"),
+                              ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in busy),
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+def traffic_per_launch(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/), or None
+    when no capture matches or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = os.path.join(ROOT, "row_normalization_gb300", "csrc",
+                       "rmsnorm.cu" if kernel.startswith("rms") else "qk_norm_rope.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        with open(path) as fh:
+            for line in fh:
+                if line.startswith("#") or "|" not in line:
+                    continue
+                k, wl, nbytes, sha = [p.strip() for p in line.split("|")[:4]]
+                if k == kernel and wl == workload and sha == digest:
+                    return int(float(nbytes))
+    except OSError:
+        return None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+RMS_KERNELS = {1: "rms_warp_rows_kernel", 2: "rms_cta_rows_kernel", 3: "rms_persistent_bulk_kernel"}
+
+
+def build_inputs(torch, binding, inputs, device):
+    """All inputs of one step, resident on the device."""
+    rms = []
+    for i, (M, N) in enumerate(RMS_SHAPES):
+        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=100 * i)
+        y = torch.empty_like(x)
+        rms.append({"M": M, "N": N, "x": x, "w": w, "y": y})
+    qk = []
+    for j, r in enumerate(QK_ROT):
+        qkv, wq, wk, pos = inputs.qkv_inputs(QK_T, HQ, HKV, D, positions="uniform",
+                                             max_pos=MAX_POS, device=device, seed=1000 + j)
+        table = binding.rope_cos_sin_table(THETA, MAX_POS, r, device=device)
+        qk.append({"r": r, "qkv": qkv, "wq": wq, "wk": wk, "pos": pos, "table": table})
+    return rms, qk
+
+
+def launch_step(binding, rms, qk, events=None):
+    """Enqueue one step; optionally record an event before every launch."""
+    k = 0
+    for c in rms:
+        if events is not None:
+            events[k].record()
+        k += 1
+        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"])
+    for c in qk:
+        if events is not None:
+            events[k].record()
+        k += 1
+        binding.qk_norm_rope_fwd(c["qkv"], c["wq"], c["wk"], c["table"], c["pos"], HQ, HKV, D,
+                                 c["r"], QK_EPS)
+    return k
+
+
+def run_ours(args) -> int:
+    import torch
+
+    from row_normalization_gb300 import binding, inputs
+    from row_normalization_gb300.build import build
+
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = dist_mod
+    if rank == 0:
+        build()
+    if dist:
+        dist.barrier()
+    binding.load()
+    device = torch.device("cuda", local)
+
+    rms, qk = build_inputs(torch, binding, inputs, device)
+    n_launch = len(rms) + len(qk)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        launch_step(binding, rms, qk)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for s in range(K):
+        launch_step(binding, rms, qk, ev[s])
+        ev[s][n_launch].record()
+    end.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    total_ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    per_launch_ms = [statistics.fmean(ev[s][k].elapsed_time(ev[s][k + 1]) for s in range(K))
+                     for k in range(n_launch)]
+
+    bytes_step = step_bytes()
+    value = world * bytes_step * K / (total_ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    per_shape = []
+    for k, c in enumerate(rms):
+        sched = binding.rmsnorm_select_schedule(c["M"], c["N"])
+        b = rms_bytes(c["M"], c["N"])
+        per_shape.append({"op": "rmsnorm", "M": c["M"], "N": c["N"],
+                          "kernel": RMS_KERNELS.get(sched, str(sched)),
+                          "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
+                          "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
+    for j, c in enumerate(qk):
+        k = len(rms) + j
+        b = qk_bytes(QK_T, c["r"])
+        per_shape.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
+                          "kernel": "qk_norm_rope_kernel",
+                          "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
+                          "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
+    for p in per_shape:
+        p["frac_of_measured"] = round(p["gbs"] / hbm_peak, 4)
+    dom = max(per_shape, key=lambda p: p["us"])
+    dom_wl = (f"rmsnorm M={dom['M']} N={dom['N']}" if dom["op"] == "rmsnorm"
+              else f"qk_norm_rope T={dom['T']} r={dom['rotary_dim']}")
+    achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                "traffic": traffic_per_launch(dom["kernel"], dom_wl),
+                "kernel": dom["kernel"], "launch": dom_wl,
+                "algorithmic_bytes_per_launch": dom["bytes"]}
+
+    e2e = run_e2e(torch, binding, rms, qk, args, dist, device) if args.e2e_steps > 0 else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=args.cpu_seconds)
+
+    rms_ms = sum(per_launch_ms[:len(rms)])
+    qk_ms = sum(per_launch_ms[len(rms):])
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch generators; see DESIGN.md input recipe)",
+        "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step,
+                   "launches_per_step": n_launch, "parallelism": f"replicas x{world}",
+                   "l2": ("inputs larger than L2: each buffer is touched once per step and a "
+                          f"step moves {bytes_step / 1e9:.2f} GB, >50x the 126 MiB L2")},
+        "frac_of_measured_copy": round(value / world / hbm_peak, 4),
+        "frac_of_spec_7928": round(value / world / SPEC_GBS, 4),
+        "per_op": {"rmsnorm_sweep_gbs": round(sum(rms_bytes(M, N) for M, N in RMS_SHAPES)
+                                              / (rms_ms * 1e-3) / 1e9, 1),
+                   "qk_norm_rope_gbs": round(sum(qk_bytes(QK_T, r) for r in QK_ROT)
+                                             / (qk_ms * 1e-3) / 1e9, 1)},
+        "per_shape": per_shape,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": n_launch * K,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(torch, binding, rms, qk, args, dist, device):
+    """The same step with host buffers: H2D of each input from pinned memory,
+    the C-ABI call, D2H of each output, all inside the timed region."""
+    world = dist.get_world_size() if dist else 1
+    host = []
+    for c in rms:
+        host.append((c["x"].cpu().pin_memory(), torch.empty_like(c["y"], device="cpu").pin_memory()))
+    qhost = []
+    for c in qk:
+        qhost.append((c["qkv"].cpu().pin_memory(), c["pos"].cpu().pin_memory(),
+                      torch.empty_like(c["qkv"], device="cpu").pin_memory()))
+    h2d = sum(h[0].numel() * 2 for h in host) + sum(q[0].numel() * 2 + q[1].numel() * 8
+                                                    for q in qhost)
+    d2h = sum(h[1].numel() * 2 for h in host) + sum(q[2].numel() * 2 for q in qhost)
+
+    def one_step():
+        for c, (xh, yh) in zip(rms, host):
+            c["x"].copy_(xh, non_blocking=True)
+            binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"])
+            yh.copy_(c["y"], non_blocking=True)
+        for c, (qh, ph, oh) in zip(qk, qhost):
+            c["qkv"].copy_(qh, non_blocking=True)
+            c["pos"].copy_(ph, non_blocking=True)
+            binding.qk_norm_rope_fwd(c["qkv"], c["wq"], c["wk"], c["table"], c["pos"], HQ, HKV,
+                                     D, c["r"], QK_EPS)
+            oh.copy_(c["qkv"], non_blocking=True)
+
+    for _ in range(2):
+        one_step()
+    torch.cuda.synchronize()
+    E = args.e2e_steps
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    s.record()
+    for _ in range(E):
+        one_step()
+    e.record()
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    ms = s.elapsed_time(e)
+    if dist:
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    val = world * step_bytes() * E / (ms * 1e-3) / 1e9
+    return {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": round(ms / E, 3),
+            "host_wall_ms_per_step": round(wall_ms / E, 3),
+            "note": "inputs x/qkv/positions in from pinned host memory and outputs y/qkv back "
+                    "every step; weights and the cos/sin table stay resident"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _cpu_sample(frac_den: int):
+    """A bounded sample of the workload on the host: the first ceil(M/frac_den)
+    rows of every RMSNorm shape and the first ceil(T/frac_den) tokens of each
+    QK case, with inputs drawn by the same generators (host device)."""
+    import numpy as np
+
+    import oracle
+    from row_normalization_gb300.inputs import bf16_bits, qkv_inputs, rmsnorm_inputs
+    rms = []
+    for i, (M, N) in enumerate(RMS_SHAPES):
+        m = max(1, math.ceil(M / frac_den))
+        x, w = rmsnorm_inputs(m, N, outlier_frac=0.01, device="cpu", seed=100 * i)
+        rms.append((bf16_bits(x), bf16_bits(w)))
+    qk = []
+    for j, r in enumerate(QK_ROT):
+        t = max(1, math.ceil(QK_T / frac_den))
+        qkv, wq, wk, pos = qkv_inputs(t, HQ, HKV, D, positions="uniform", max_pos=MAX_POS,
+                                      device="cpu", seed=1000 + j)
+        qk.append((bf16_bits(qkv), bf16_bits(wq), bf16_bits(wk), pos.numpy(), r))
+    tables = {r: oracle.rope_cos_sin(THETA, MAX_POS, r) for r in QK_ROT}
+    nbytes = sum(rms_bytes(x.shape[0], x.shape[1]) for x, _ in rms) + \
+        sum(qk_bytes(q[0].shape[0], q[4]) for q in qk)
+    return rms, qk, tables, nbytes, np
+
+
+def _cpu_pass(pool, threads, rms, qk, tables):
+    import numpy as np
+
+    import oracle
+    futs = []
+    for x, w in rms:
+        for part in np.array_split(np.arange(x.shape[0]), min(threads, x.shape[0])):
+            if part.size:
+                futs.append(pool.submit(oracle.rmsnorm, x[part[0]:part[-1] + 1], w, RMS_EPS))
+    for qkv, wq, wk, pos, r in qk:
+        for part in np.array_split(np.arange(qkv.shape[0]), min(threads, qkv.shape[0])):
+            if part.size:
+                a, b = part[0], part[-1] + 1
+                futs.append(pool.submit(oracle.qk_norm_rope, qkv[a:b], wq, wk, tables[r],
+                                        pos[a:b], HQ, HKV, D, r, QK_EPS))
+    for f in futs:
+        f.result()
+
+
+def cpu_baseline(budget_s: float = 10.0, frac_den: int = 256) -> dict:
+    """Times the oracle, unchanged, on the host cores: rows and tokens are split
+    over one thread per core (the C oracle releases the GIL), and whole passes
+    over the sample repeat until about `budget_s` seconds have run."""
+    threads = len(os.sched_getaffinity(0))
+    rms, qk, tables, nbytes, _ = _cpu_sample(frac_den)
+    passes = 0
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        while True:
+            _cpu_pass(pool, threads, rms, qk, tables)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    return {"value": round(nbytes * passes / el / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"first 1/{frac_den} of the rows of every RMSNorm shape and of the "
+                       f"tokens of each QK case ({nbytes / 1e6:.1f} MB ideal traffic per pass), "
+                       f"{passes} passes in {el:.1f} s, fp64 C oracle on {threads} threads")}
+
+
+def run_reference(args) -> int:
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    threads = len(os.sched_getaffinity(0))
+    # size each step so the whole run stays near a minute and a half
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    frac_den = 256
+    rms, qk, tables, nbytes, _ = _cpu_sample(frac_den)
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        _cpu_pass(pool, threads, rms, qk, tables)
+        one = time.perf_counter() - t0
+        scale = max(1, int(round(one / budget)))
+        if scale > 1:
+            frac_den *= scale
+            rms, qk, tables, nbytes, _ = _cpu_sample(frac_den)
+        for _ in range(args.warmup):
+            _cpu_pass(pool, threads, rms, qk, tables)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            _cpu_pass(pool, threads, rms, qk, tables)
+        el = time.perf_counter() - t0
+    value = nbytes * args.steps / el / 1e9
+    sample = (f"each step: first 1/{frac_den} of the rows of every RMSNorm shape and of the "
+              f"tokens of each QK case ({nbytes / 1e6:.2f} MB ideal traffic)")
+    line = {"metric": METRIC, "impl": "reference", "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "ours" and args.warmup < 3:
+        args.warmup = 3  # never time without at least three warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * row_norm.h -- C ABI of the GB300 (sm_103a) bf16 row-normalization library.
+ *
+ * Operations
+ *   rmsnorm_fwd       y = x * 1/sqrt(mean(x^2) + eps) * w, row by row.
+ *                     "[Inductor] Codegen Gluon", section 3.1 (MVP: RMSNorm
+ *                     with TMA-cached reused input): x feeds both the x*x
+ *                     reduction and the x * rstd * weight pass, and is read
+ *                     from HBM once.
+ *   qk_norm_rope_fwd  per-head RMSNorm of the query and key heads of a packed
+ *                     QKV tensor, followed by neox rotary embedding, in place.
+ *                     "[pretuned] Optimize fused_qk_norm_rope on B200",
+ *                     section "Summary": load each head's rotary halves once,
+ *                     reduce over the whole head in registers, apply the Q/K
+ *                     weight and the rotation, store each half once; partial
+ *                     rotary still normalises the non-rotary tail.
+ *   rope_cos_sin_table  builds the cos/sin table the rotary step reads.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 tensors are passed as pointers to their raw 16-bit patterns
+ *     (rn_bf16); fp32 and int64 tensors as float* and int64_t*.
+ *   - Every tensor pointer is a DEVICE pointer (cudaMalloc'd or managed) on
+ *     the current CUDA device, 16-byte aligned, densely packed row-major.
+ *   - The caller owns every buffer.  The library allocates no device memory,
+ *     never synchronises, and enqueues its kernels on `stream` (NULL = the
+ *     legacy default stream).  Results are ready when the stream reaches
+ *     that point.
+ *   - Every function returns RN_OK (0) or a negative RN_ERR_* code.  Argument
+ *     errors are detected on the host before anything is launched; nothing is
+ *     written in that case.  RN_ERR_LAUNCH reports a failed launch.
+ *   - Zero rows (M == 0 or T == 0) is a no-op that returns RN_OK.
+ *   - Arithmetic: bf16 inputs are widened to fp32 at the point of use, all
+ *     sums and products run in fp32, and each output is rounded once to
+ *     bf16 (round to nearest even).
+ */
+#ifndef ROW_NORM_H
+#define ROW_NORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Raw bf16 bit pattern (sign, 8-bit exponent, 7-bit mantissa). */
+typedef uint16_t rn_bf16;
+
+/* ABI-identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st *rn_stream_t;
+
+enum {
+    RN_OK = 0,
+    RN_ERR_NULL = -1,     /* a required pointer is NULL                        */
+    RN_ERR_ALIGN = -2,    /* a tensor pointer is not 16-byte aligned           */
+    RN_ERR_SHAPE = -3,    /* a size is negative, unsupported or inconsistent   */
+    RN_ERR_LAUNCH = -4,   /* the CUDA launch failed (cudaGetLastError)         */
+    RN_ERR_DEVICE = -5,   /* no usable CUDA device / device query failed       */
+    RN_ERR_ARG = -6       /* another invalid argument (unknown option value)   */
+};
+
+/* Bits of the per-device status word that kernels raise instead of trapping. */
+enum {
+    RN_STATUS_WAIT_TIMEOUT = 1u,  /* a pipeline wait ran out; that launch's
+                                     output is incomplete                     */
+    RN_STATUS_BAD_POSITION = 2u   /* qk_norm_rope_fwd_checked met a position
+                                     outside [0, max_pos)                     */
+};
+
+/* Static description of a code.  Never NULL. */
+const char *rn_error_string(int code);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int rn_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* y[r, :] = bf16( x[r, :] * 1/sqrt(sum_j x[r, j]^2 / N + eps) * w[:] )
+ *
+ *   x    [M, N] bf16, row-major, read once.
+ *   w    [N] bf16.
+ *   eps  added to the mean of squares inside the square root.
+ *   y    [M, N] bf16, written once.  Must not overlap x or w.
+ *   Requirements: M >= 0; 8 <= N <= 65536 and N % 8 == 0 (rows start on
+ *   16-byte boundaries); x, w, y 16-byte aligned.
+ * The schedule (warp per row, CTA per row, or a persistent CTA per SM that
+ * streams rows through a shared-memory ring with bulk async copies) is
+ * chosen from (M, N) and the SM count.  Errors: RN_ERR_NULL, RN_ERR_ALIGN,
+ * RN_ERR_SHAPE, RN_ERR_DEVICE, RN_ERR_LAUNCH. */
+int rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M,
+                int64_t N, rn_bf16 *y, rn_stream_t stream);
+
+/* Schedules that rmsnorm_fwd_sched can force (for tests and measurement). */
+enum {
+    RN_SCHED_AUTO = 0,
+    RN_SCHED_WARP_ROW = 1,    /* one warp per row, row in registers (N <= 2048)  */
+    RN_SCHED_CTA_ROW = 2,     /* one CTA per row, row in registers               */
+    RN_SCHED_PERSIST_BULK = 3 /* persistent CTAs, bulk-copy shared-memory ring
+                                 (N a power of two, 1024 <= N <= 32768)          */
+};
+
+/* rmsnorm_fwd with an explicit schedule.  `schedule` is one of RN_SCHED_*;
+ * a schedule that cannot serve (M, N) returns RN_ERR_SHAPE.
+ * `wait_timeout_ns` bounds every pipeline wait of the persistent schedule
+ * (0 = the default of 2 s); when one runs out, the kernel raises
+ * RN_STATUS_WAIT_TIMEOUT in the status word, drains its own copies and
+ * returns.  `debug_flags` is 0 in normal use.  Tests and tuning set:
+ *   bit 0      the persistent schedule never issues its copies, so its
+ *              waits run out (exercises the timeout path);
+ *   bits 4-7   persistent schedule: CTAs per SM (0 = 1);
+ *   bits 8-12  persistent schedule: ring stages, capped by shared memory
+ *              (0 = as many as fit, at most 16). */
+int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps,
+                      int64_t M, int64_t N, rn_bf16 *y, int schedule,
+                      uint64_t wait_timeout_ns, int debug_flags,
+                      rn_stream_t stream);
+
+/* The schedule (RN_SCHED_*) that rmsnorm_fwd launches for (M, N) on the
+ * current device; RN_ERR_SHAPE / RN_ERR_DEVICE as rmsnorm_fwd would return.
+ * Host-only query: launches nothing. */
+int rmsnorm_select_schedule(int64_t M, int64_t N);
+
+/* ------------------------------------------------------------------------ */
+/* Fused Q/K RMSNorm + neox RoPE                                              */
+/* ------------------------------------------------------------------------ */
+
+/* In place on qkv [T, (Hq + 2*Hkv) * D] bf16: token t holds Hq query heads,
+ * then Hkv key heads, then Hkv value heads, D contiguous elements each.
+ * For every query head (weight wq) and key head (weight wk):
+ *   n_j = x_j * 1/sqrt(sum_k x_k^2 / D + eps) * w_j      (all D elements)
+ *   for i < r/2 (r = rotary_dim), c = cos_sin[pos, i], s = cos_sin[pos, r/2 + i]:
+ *     o_i = n_i*c - n_{i+r/2}*s,   o_{i+r/2} = n_{i+r/2}*c + n_i*s
+ *   o_j = n_j for r <= j < D
+ * and o is stored back, rounded once to bf16.  Value heads are neither read
+ * nor written.
+ *
+ *   wq, wk     [D] bf16.
+ *   cos_sin    [max_pos, r] fp32, row p = [cos(p f_0..) | sin(p f_0..)]
+ *              (see rope_cos_sin_table).
+ *   positions  [T] int64; every entry must lie in [0, max_pos) of the table
+ *              the caller passes: this entry point does not check them (a
+ *              position outside the table reads outside cos_sin).  Use
+ *              qk_norm_rope_fwd_checked for untrusted positions.
+ *   Requirements: T >= 0, Hq >= 0, Hkv >= 0; D in {64, 128, 256};
+ *   rotary_dim in {D, D/2, D/4}; all pointers 16-byte aligned.
+ * The schedule (1, 2 or 4 heads per warp; persistent grid for large T) is
+ * chosen from T.  Errors: RN_ERR_NULL, RN_ERR_ALIGN, RN_ERR_SHAPE,
+ * RN_ERR_DEVICE, RN_ERR_LAUNCH. */
+int qk_norm_rope_fwd(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
+                     const float *cos_sin, const int64_t *positions, int64_t T,
+                     int Hq, int Hkv, int D, int rotary_dim, float eps,
+                     rn_stream_t stream);
+
+/* As qk_norm_rope_fwd, but every position is checked against max_pos: the
+ * heads of a token whose position lies outside [0, max_pos) are left
+ * untouched and RN_STATUS_BAD_POSITION is OR-ed into *d_err_flag (a device
+ * int the caller owns and clears).  max_pos >= 1. */
+int qk_norm_rope_fwd_checked(rn_bf16 *qkv, const rn_bf16 *wq,
+                             const rn_bf16 *wk, const float *cos_sin,
+                             const int64_t *positions, int64_t T, int Hq,
+                             int Hkv, int D, int rotary_dim, float eps,
+                             int64_t max_pos, int *d_err_flag,
+                             rn_stream_t stream);
+
+/* Heads per warp that qk_norm_rope_fwd_sched can force. */
+enum {
+    RN_QK_AUTO = 0,
+    RN_QK_HEAD_PER_WARP = 1,   /* 32 lanes per head                      */
+    RN_QK_TWO_HEADS = 2,       /* 16 lanes per head                      */
+    RN_QK_FOUR_HEADS = 4,      /* 8 lanes per head                       */
+    RN_QK_PERSISTENT = 8       /* 8 lanes per head, persistent grid       */
+};
+
+/* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*). */
+int qk_norm_rope_fwd_sched(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
+                           const float *cos_sin, const int64_t *positions,
+                           int64_t T, int Hq, int Hkv, int D, int rotary_dim,
+                           float eps, int schedule, rn_stream_t stream);
+
+/* The schedule (RN_QK_*) that qk_norm_rope_fwd launches for T tokens
+ * (RN_ERR_SHAPE if T < 0).  Host-only query: launches nothing. */
+int qk_norm_rope_select_schedule(int64_t T);
+
+/* cos_sin[p, i] = cos(p * f_i), cos_sin[p, r/2 + i] = sin(p * f_i),
+ * f_i = theta^(-2i/r), for p < max_pos, i < r/2 (r = rotary_dim, even, > 0).
+ * Computed on the device in fp64 and rounded once to fp32; written to the
+ * caller's DEVICE buffer cos_sin [max_pos, r] fp32.  theta > 0. */
+int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim,
+                       float *cos_sin, rn_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status word                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Reads (and, if clear != 0, resets) the current device's status word: an
+ * OR of RN_STATUS_* bits raised by kernels since the last reset.
+ * Synchronous: waits for the device to finish its queued work. */
+int rn_device_status(unsigned int *out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROW_NORM_H */

@@ -1,0 +1,243 @@
+"""Thin Python binding over the C ABI of ``librownorm.so`` (include/row_norm.h).
+
+Argument marshalling only: every function checks the tensors' dtype, device
+and layout, passes raw pointers, sizes and the current CUDA stream to the
+C entry point of the same name, and raises on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback.  If the
+library is not built, the first call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+_lock = threading.Lock()
+_lib = None
+
+RN_OK = 0
+RN_ERR_NULL = -1
+RN_ERR_ALIGN = -2
+RN_ERR_SHAPE = -3
+RN_ERR_LAUNCH = -4
+RN_ERR_DEVICE = -5
+RN_ERR_ARG = -6
+
+RN_STATUS_WAIT_TIMEOUT = 1
+RN_STATUS_BAD_POSITION = 2
+
+RN_SCHED_AUTO = 0
+RN_SCHED_WARP_ROW = 1
+RN_SCHED_CTA_ROW = 2
+RN_SCHED_PERSIST_BULK = 3
+
+RN_QK_AUTO = 0
+RN_QK_HEAD_PER_WARP = 1
+RN_QK_TWO_HEADS = 2
+RN_QK_FOUR_HEADS = 4
+RN_QK_PERSISTENT = 8
+
+
+class RowNormError(RuntimeError):
+    def __init__(self, name: str, code: int):
+        super().__init__(f"{name}: {error_string(code)} (status {code})")
+        self.code = code
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (once).  Raises RuntimeError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the CUDA library first "
+                "(row_normalization_gb300.build.build())")
+        L = ctypes.CDLL(path)
+        vp, i64, i32, f32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_double)
+        u64 = ctypes.c_uint64
+        L.rn_error_string.argtypes = [i32]
+        L.rn_error_string.restype = ctypes.c_char_p
+        L.rn_version.argtypes = []
+        L.rn_version.restype = i32
+        L.rmsnorm_fwd.argtypes = [vp, vp, f32, i64, i64, vp, vp]
+        L.rmsnorm_fwd.restype = i32
+        L.rmsnorm_fwd_sched.argtypes = [vp, vp, f32, i64, i64, vp, i32, u64, i32, vp]
+        L.rmsnorm_fwd_sched.restype = i32
+        L.qk_norm_rope_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, vp]
+        L.qk_norm_rope_fwd.restype = i32
+        L.qk_norm_rope_fwd_sched.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
+                                             i32, vp]
+        L.qk_norm_rope_fwd_sched.restype = i32
+        L.qk_norm_rope_fwd_checked.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
+                                               i64, vp, vp]
+        L.qk_norm_rope_fwd_checked.restype = i32
+        L.rope_cos_sin_table.argtypes = [f64, i64, i32, vp, vp]
+        L.rope_cos_sin_table.restype = i32
+        L.rmsnorm_select_schedule.argtypes = [i64, i64]
+        L.rmsnorm_select_schedule.restype = i32
+        L.qk_norm_rope_select_schedule.argtypes = [i64]
+        L.qk_norm_rope_select_schedule.restype = i32
+        L.rn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+        L.rn_device_status.restype = i32
+        _lib = L
+        return L
+
+
+def error_string(code: int) -> str:
+    return load().rn_error_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load().rn_version())
+
+
+def _check(rc: int, name: str) -> None:
+    if rc != RN_OK:
+        raise RowNormError(name, rc)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+
+def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | None = None,
+                *, schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0,
+                debug_flags: int = 0, stream=None) -> torch.Tensor:
+    """y = x * rsqrt(mean(x^2, -1) + eps) * w for bf16 x [M, N]; returns y."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1]:
+        raise ValueError("x must be [M, N] and w [N]")
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", torch.bfloat16)
+        if y.shape != x.shape:
+            raise ValueError("y must have x's shape")
+    M, N = x.shape
+    L = load()
+    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+        rc = L.rmsnorm_fwd(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(), _stream(stream))
+    else:
+        rc = L.rmsnorm_fwd_sched(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
+                                 schedule, wait_timeout_ns, debug_flags, _stream(stream))
+    _check(rc, "rmsnorm_fwd")
+    return y
+
+
+def _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim):
+    _need(qkv, "qkv", torch.bfloat16)
+    _need(wq, "wq", torch.bfloat16)
+    _need(wk, "wk", torch.bfloat16)
+    _need(cos_sin, "cos_sin", torch.float32)
+    _need(positions, "positions", torch.int64)
+    T = qkv.shape[0]
+    if qkv.numel() != T * (Hq + 2 * Hkv) * D:
+        raise ValueError("qkv must be [T, (Hq + 2*Hkv) * D]")
+    if wq.numel() != D or wk.numel() != D:
+        raise ValueError("wq and wk must have D elements")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != rotary_dim:
+        raise ValueError("cos_sin must be [max_pos, rotary_dim]")
+    if positions.numel() != T:
+        raise ValueError("positions must have T elements")
+    return T
+
+
+def qk_norm_rope_fwd(qkv: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
+                     cos_sin: torch.Tensor, positions: torch.Tensor, Hq: int, Hkv: int, D: int,
+                     rotary_dim: int, eps: float, *, schedule: int = RN_QK_AUTO,
+                     stream=None) -> torch.Tensor:
+    """In place: per-head RMSNorm of Q and K heads, then neox RoPE.  Returns qkv."""
+    T = _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim)
+    L = load()
+    if schedule == RN_QK_AUTO:
+        rc = L.qk_norm_rope_fwd(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(), cos_sin.data_ptr(),
+                                positions.data_ptr(), T, Hq, Hkv, D, rotary_dim, eps,
+                                _stream(stream))
+    else:
+        rc = L.qk_norm_rope_fwd_sched(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                      cos_sin.data_ptr(), positions.data_ptr(), T, Hq, Hkv, D,
+                                      rotary_dim, eps, schedule, _stream(stream))
+    _check(rc, "qk_norm_rope_fwd")
+    return qkv
+
+
+def qk_norm_rope_fwd_checked(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim, eps,
+                             err_flag: torch.Tensor, *, max_pos: int | None = None,
+                             stream=None) -> torch.Tensor:
+    """As qk_norm_rope_fwd; tokens with a position outside [0, max_pos) are left
+    untouched and RN_STATUS_BAD_POSITION is OR-ed into err_flag (int32 CUDA [1])."""
+    T = _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim)
+    _need(err_flag, "err_flag", torch.int32)
+    if max_pos is None:
+        max_pos = cos_sin.shape[0]
+    rc = load().qk_norm_rope_fwd_checked(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                         cos_sin.data_ptr(), positions.data_ptr(), T, Hq, Hkv, D,
+                                         rotary_dim, eps, int(max_pos), err_flag.data_ptr(),
+                                         _stream(stream))
+    _check(rc, "qk_norm_rope_fwd_checked")
+    return qkv
+
+
+def rope_cos_sin_table(theta: float, max_pos: int, rotary_dim: int,
+                       out: torch.Tensor | None = None, *, device=None,
+                       stream=None) -> torch.Tensor:
+    """fp32 [max_pos, rotary_dim] table: cos half then sin half of p * theta^(-2i/r)."""
+    if out is None:
+        out = torch.empty(max_pos, rotary_dim, dtype=torch.float32,
+                          device=device if device is not None else "cuda")
+    _need(out, "out", torch.float32)
+    if out.shape != (max_pos, rotary_dim):
+        raise ValueError("out must be [max_pos, rotary_dim]")
+    rc = load().rope_cos_sin_table(float(theta), int(max_pos), int(rotary_dim), out.data_ptr(),
+                                   _stream(stream))
+    _check(rc, "rope_cos_sin_table")
+    return out
+
+
+def rmsnorm_select_schedule(M: int, N: int) -> int:
+    """The RN_SCHED_* schedule rmsnorm_fwd picks for (M, N) on the current device."""
+    rc = int(load().rmsnorm_select_schedule(int(M), int(N)))
+    if rc < 0:
+        raise RowNormError("rmsnorm_select_schedule", rc)
+    return rc
+
+
+def qk_norm_rope_select_schedule(T: int) -> int:
+    """The RN_QK_* schedule qk_norm_rope_fwd picks for T tokens."""
+    rc = int(load().qk_norm_rope_select_schedule(int(T)))
+    if rc < 0:
+        raise RowNormError("qk_norm_rope_select_schedule", rc)
+    return rc
+
+
+def device_status(clear: bool = True) -> int:
+    """OR of RN_STATUS_* bits raised on the current device (synchronises)."""
+    v = ctypes.c_uint(0)
+    _check(load().rn_device_status(ctypes.byref(v), 1 if clear else 0), "rn_device_status")
+    return int(v.value)

@@ -1,0 +1,536 @@
+// rmsnorm.cu -- bf16 RMSNorm forward for sm_103a, and the library's status word.
+//
+// y[r, :] = bf16( x[r, :] * 1/sqrt(sum_j x[r, j]^2 / N + eps) * w[:] )
+//
+// "[Inductor] Codegen Gluon", section 3.1: x feeds both the x*x reduction and
+// the x * rstd * weight pass.  Every schedule here reads each element of x
+// from HBM exactly once, keeps it (bf16) in registers or shared memory
+// between the two passes, widens to fp32 at the point of use, and writes each
+// output once with a single bf16 rounding.
+//
+// Schedules:
+//   warp_rows        one warp per row, the row in registers (N <= 2048).
+//   cta_rows         one CTA per row, the row in registers, one CTA-wide
+//                    reduction through shared memory (any N up to 65536).
+//   persistent_bulk  one CTA per SM.  A producer warp streams R-row units of
+//                    x into an S-stage shared-memory ring with 1D bulk
+//                    copies (cp.async.bulk, completion on a per-stage
+//                    mbarrier); consumer warps pull each unit into registers
+//                    once, release the stage, reduce, and store y.  The
+//                    weight stays in registers for the CTA's whole life.
+#include "rn_common.cuh"
+#include "rn_host.h"
+
+namespace rn {
+
+static __device__ unsigned int g_status = 0u;
+
+__device__ __forceinline__ void raise_status(unsigned int bits) { atomicOr(&g_status, bits); }
+
+// Sum of squares of the 8 bf16 in a 16-byte vector, in fp32 (pairwise).
+__device__ __forceinline__ float sumsq8(uint4 v) {
+    float a = bf_lo(v.x) * bf_lo(v.x);
+    a = fmaf(bf_hi(v.x), bf_hi(v.x), a);
+    float b = bf_lo(v.y) * bf_lo(v.y);
+    b = fmaf(bf_hi(v.y), bf_hi(v.y), b);
+    float c = bf_lo(v.z) * bf_lo(v.z);
+    c = fmaf(bf_hi(v.z), bf_hi(v.z), c);
+    float d = bf_lo(v.w) * bf_lo(v.w);
+    d = fmaf(bf_hi(v.w), bf_hi(v.w), d);
+    return (a + b) + (c + d);
+}
+
+// y = bf16((x * rstd) * w) for 8 packed elements.
+__device__ __forceinline__ uint4 scale8(uint4 xv, uint4 wv, float rstd) {
+    uint4 o;
+    o.x = pack_bf2(bf_lo(xv.x) * rstd * bf_lo(wv.x), bf_hi(xv.x) * rstd * bf_hi(wv.x));
+    o.y = pack_bf2(bf_lo(xv.y) * rstd * bf_lo(wv.y), bf_hi(xv.y) * rstd * bf_hi(wv.y));
+    o.z = pack_bf2(bf_lo(xv.z) * rstd * bf_lo(wv.z), bf_hi(xv.z) * rstd * bf_hi(wv.z));
+    o.w = pack_bf2(bf_lo(xv.w) * rstd * bf_lo(wv.w), bf_hi(xv.w) * rstd * bf_hi(wv.w));
+    return o;
+}
+
+__device__ __forceinline__ float row_rstd(float ss, int N, float eps) {
+    return __frsqrt_rn(ss / static_cast<float>(N) + eps);
+}
+
+// ---------------------------------------------------------------------------
+// warp_rows: one warp per row; lane l holds 16-byte chunks l, l+32, ...
+// ---------------------------------------------------------------------------
+template <int VPT>
+__global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *__restrict__ x,
+                                                            const uint16_t *__restrict__ w,
+                                                            float eps, int64_t M, int N,
+                                                            uint16_t *__restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int cpr = N >> 3;
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); row < M;
+         row += static_cast<int64_t>(gridDim.x) * wpb) {
+        const uint16_t *xr = x + row * N;
+        uint4 v[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int c = lane + 32 * i;
+            v[i] = (c < cpr) ? ld_stream16(xr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
+        ss = warp_sum(ss);
+        const float rstd = row_rstd(ss, N, eps);
+        uint16_t *yr = y + row * N;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int c = lane + 32 * i;
+            if (c < cpr) st16(yr + 8 * c, scale8(v[i], ld_ro16(w + 8 * c), rstd));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// cta_rows: one CTA per row; thread t holds chunks t, t+nt, ...
+// ---------------------------------------------------------------------------
+template <int VPT, int MAXT>
+__global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *__restrict__ x,
+                                                            const uint16_t *__restrict__ w,
+                                                            float eps, int64_t M, int N,
+                                                            uint16_t *__restrict__ y) {
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int nw = nt >> 5;
+    const int cpr = N >> 3;
+    int par = 0;
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x, par ^= 1) {
+        const uint16_t *xr = x + row * N;
+        uint4 v[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int c = tid + nt * i;
+            v[i] = (c < cpr) ? ld_stream16(xr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) red[par][tid >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        for (int k = 0; k < nw; ++k) tot += red[par][k];
+        const float rstd = row_rstd(tot, N, eps);
+        uint16_t *yr = y + row * N;
+        if constexpr (MAXT < 1024) {
+            // issue every weight load before the first store
+            uint4 wv[VPT];
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = tid + nt * i;
+                if (c < cpr) wv[i] = ld_ro16(w + 8 * c);
+            }
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = tid + nt * i;
+                if (c < cpr) st16(yr + 8 * c, scale8(v[i], wv[i], rstd));
+            }
+        } else {
+            // 64 registers a thread at 1024 threads: stream the weights
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = tid + nt * i;
+                if (c < cpr) st16(yr + 8 * c, scale8(v[i], ld_ro16(w + 8 * c), rstd));
+            }
+        }
+        // red[par] is rewritten two rows later, after the next barrier: safe.
+    }
+}
+
+// ---------------------------------------------------------------------------
+// persistent_bulk
+// ---------------------------------------------------------------------------
+struct BulkArgs {
+    const uint16_t *x;
+    const uint16_t *w;
+    uint16_t *y;
+    int64_t M;
+    int N;
+    float eps;
+    int stages;
+    int debug;
+    uint64_t timeout_ns;
+};
+
+// Shared memory: [stages x R rows of x][full mbarriers][empty mbarriers]
+//                [partial sums 2 x R x 32 floats][flags: 4 ints]
+__host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N) {
+    return static_cast<size_t>(stages) * R * N * 2 + static_cast<size_t>(stages) * 16 +
+           static_cast<size_t>(2) * R * 32 * 4 + 16;
+}
+
+// NT consumer threads (N / 8 / VPR of them) plus one producer warp.
+template <int VPR, int R, int NT>
+__global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const BulkArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = a.stages;
+    const int N = a.N;
+    const uint32_t row_bytes = static_cast<uint32_t>(N) * 2u;
+    const uint32_t stage_bytes = row_bytes * R;
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage_bytes);
+    uint64_t *empty = full + S;
+    float *red = reinterpret_cast<float *>(empty + S);
+    // flags[0], flags[1]: "consumers give up" for even / odd units (decided
+    // before a named barrier, read after it); flags[2]: "someone gave up",
+    // polled inside waits so nobody waits out a full timeout needlessly.
+    volatile int *flags = reinterpret_cast<volatile int *>(red + 2 * R * 32);
+
+    constexpr int NW = NT / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NW);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        flags[2] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Contiguous, balanced row range of this CTA (at most one row of skew).
+    const int64_t G = gridDim.x;
+    const int64_t r_begin = (a.M * static_cast<int64_t>(blockIdx.x)) / G;
+    const int64_t r_end = (a.M * (static_cast<int64_t>(blockIdx.x) + 1)) / G;
+
+    if (warp == NW) {
+        // ---- producer ----
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int64_t k = 0;
+            for (int64_t r0 = r_begin; r0 < r_end; r0 += R, ++k) {
+                const int s = static_cast<int>(k % S);
+                if (k >= S) {
+                    const uint32_t par = static_cast<uint32_t>((k / S - 1) & 1);
+                    if (!mbar_wait_bounded(&empty[s], par, a.timeout_ns, &flags[2])) {
+                        flags[2] = 1;
+                        raise_status(RN_STATUS_WAIT_TIMEOUT);
+                        break;
+                    }
+                }
+                const int64_t left = r_end - r0;
+                const uint32_t rows = static_cast<uint32_t>(left < R ? left : R);
+                const uint32_t bytes = rows * row_bytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                if (!(a.debug & 1))
+                    bulk_copy_g2s(ring + static_cast<size_t>(s) * stage_bytes, a.x + r0 * N, bytes,
+                                  &full[s], pol);
+            }
+            // Drain: every copy issued into this CTA's ring lands before the
+            // CTA may exit.  The last use of each stage is among the last S.
+            const int64_t issued = k;
+            const uint64_t t0 = globaltimer_ns();
+            for (int64_t kk = (issued > S ? issued - S : 0); kk < issued; ++kk) {
+                const uint64_t spent = globaltimer_ns() - t0;
+                const uint64_t budget = spent < a.timeout_ns ? a.timeout_ns - spent : 0;
+                if (!mbar_wait_bounded(&full[kk % S], static_cast<uint32_t>((kk / S) & 1), budget,
+                                       nullptr)) {
+                    raise_status(RN_STATUS_WAIT_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---- consumers ----
+    const int tid = threadIdx.x;
+    uint4 wv[VPR];
+#pragma unroll
+    for (int j = 0; j < VPR; ++j) wv[j] = ld_ro16(a.w + 8 * (tid + j * NT));
+
+    int64_t k = 0;
+    for (int64_t r0 = r_begin; r0 < r_end; r0 += R, ++k) {
+        // Keep the weights packed (bf16) across rows: without this the
+        // compiler hoists their fp32 widening out of the loop and doubles
+        // the register footprint.
+#pragma unroll
+        for (int j = 0; j < VPR; ++j)
+            asm volatile("" : "+r"(wv[j].x), "+r"(wv[j].y), "+r"(wv[j].z), "+r"(wv[j].w));
+        const int s = static_cast<int>(k % S);
+        const uint32_t par = static_cast<uint32_t>((k / S) & 1);
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], par, a.timeout_ns, &flags[2]));
+        const uint8_t *st = ring + static_cast<size_t>(s) * stage_bytes;
+        uint4 xv[R][VPR];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+#pragma unroll
+            for (int j = 0; j < VPR; ++j)
+                xv[rr][j] = ok ? ld_shared16(st + rr * row_bytes + 16u * (tid + j * NT))
+                               : make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        if (lane == 0) {
+            if (ok) {
+                mbar_arrive(&empty[s]);
+            } else {
+                flags[k & 1] = 1;
+                flags[2] = 1;
+                raise_status(RN_STATUS_WAIT_TIMEOUT);
+            }
+        }
+        float ss[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < VPR; ++j) acc += sumsq8(xv[rr][j]);
+            ss[rr] = warp_sum(acc);
+        }
+        // Same for x: hold it packed across the barrier, widen again after.
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+#pragma unroll
+            for (int j = 0; j < VPR; ++j)
+                asm volatile("" : "+r"(xv[rr][j].x), "+r"(xv[rr][j].y), "+r"(xv[rr][j].z),
+                             "+r"(xv[rr][j].w));
+        float *rb = red + (k & 1) * R * 32;
+        if (lane == 0) {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) rb[rr * 32 + warp] = ss[rr];
+        }
+        named_bar_sync(1, NT);
+        if (flags[k & 1]) break;  // same decision in every consumer warp
+        const int64_t left = r_end - r0;
+        const int rows = static_cast<int>(left < R ? left : R);
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            if (rr < rows) {
+                float tot = 0.f;
+                for (int q = 0; q < NW; ++q) tot += rb[rr * 32 + q];
+                const float rstd = row_rstd(tot, N, a.eps);
+                uint16_t *yr = a.y + (r0 + rr) * N;
+#pragma unroll
+                for (int j = 0; j < VPR; ++j)
+                    st16(yr + 8 * (tid + j * NT), scale8(xv[rr][j], wv[j], rstd));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+static int launch_warp_rows(const uint16_t *x, const uint16_t *w, float eps, int64_t M, int N,
+                            uint16_t *y, cudaStream_t st, const DeviceInfo &dev) {
+    const int cpr = N >> 3;
+    const int wpb = 8;
+    const int64_t want = (M + wpb - 1) / wpb;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 64;
+    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+    if (cpr <= 32)
+        rms_warp_rows_kernel<1><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+    else if (cpr <= 64)
+        rms_warp_rows_kernel<2><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+    else if (cpr <= 128)
+        rms_warp_rows_kernel<4><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+    else if (cpr <= 256)
+        rms_warp_rows_kernel<8><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+    else
+        return RN_ERR_SHAPE;
+    return launch_status();
+}
+
+static int launch_cta_rows(const uint16_t *x, const uint16_t *w, float eps, int64_t M, int N,
+                           uint16_t *y, cudaStream_t st, const DeviceInfo &dev) {
+    const int cpr = N >> 3;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 2048;
+    const unsigned grid = static_cast<unsigned>(M < cap ? M : cap);
+    // Threads: enough 16-byte chunks per thread to keep several loads in
+    // flight, at most 1024 threads.
+    auto nthreads = [&](int vpt) {
+        int t = (cpr + vpt - 1) / vpt;
+        return ((t + 31) / 32) * 32;
+    };
+    if (cpr <= 512) {
+        rms_cta_rows_kernel<1, 512><<<grid, nthreads(1), 0, st>>>(x, w, eps, M, N, y);
+    } else if (cpr <= 1024) {
+        rms_cta_rows_kernel<2, 512><<<grid, nthreads(2), 0, st>>>(x, w, eps, M, N, y);
+    } else if (cpr <= 2048) {
+        rms_cta_rows_kernel<4, 512><<<grid, nthreads(4), 0, st>>>(x, w, eps, M, N, y);
+    } else if (cpr <= 4096) {
+        rms_cta_rows_kernel<8, 512><<<grid, nthreads(8), 0, st>>>(x, w, eps, M, N, y);
+    } else if (cpr <= 8192) {
+        rms_cta_rows_kernel<8, 1024><<<grid, nthreads(8), 0, st>>>(x, w, eps, M, N, y);
+    } else {
+        return RN_ERR_SHAPE;
+    }
+    return launch_status();
+}
+
+// Chooses (consumer threads, chunks per thread per row, rows per stage) for
+// the persistent schedule; false when N does not fit it.
+static bool bulk_geometry(int N, int *nt, int *vpr, int *R) {
+    // One instantiation per row width: NT consumer threads x VPR chunks of 8
+    // elements cover a row exactly, and R rows make a stage of 8 chunks per
+    // consumer thread.
+    switch (N) {
+        case 1024: *nt = 128; *vpr = 1; break;
+        case 2048: *nt = 256; *vpr = 1; break;
+        case 4096: *nt = 256; *vpr = 2; break;
+        case 8192: *nt = 256; *vpr = 4; break;
+        case 16384: *nt = 256; *vpr = 8; break;
+        case 32768: *nt = 512; *vpr = 8; break;
+        default: return false;
+    }
+    *R = 8 / *vpr;
+    return true;
+}
+
+template <int VPR, int R, int NT>
+static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_cap,
+                            cudaStream_t st) {
+    static std::atomic<int> attr_done[kMaxDevices];
+    const int dev = current_device_index();
+    if (dev < 0 || dev >= kMaxDevices) return RN_ERR_DEVICE;
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<VPR, R, NT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_cap) != cudaSuccess) {
+            cudaGetLastError();
+            return RN_ERR_DEVICE;
+        }
+        attr_done[dev].store(1, std::memory_order_release);
+    }
+    rms_persistent_bulk_kernel<VPR, R, NT><<<grid, NT + 32, smem, st>>>(a);
+    return launch_status();
+}
+
+static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float eps, int64_t M,
+                                  int N, uint16_t *y, cudaStream_t st, const DeviceInfo &dev,
+                                  uint64_t timeout_ns, int debug_flags) {
+    int nt, vpr, R;
+    if (!bulk_geometry(N, &nt, &vpr, &R)) return RN_ERR_SHAPE;
+    const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
+    int stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, R, N)) /
+                                  (static_cast<size_t>(R) * N * 2 + 16));
+    if (stages > 16) stages = 16;
+    const int forced_stages = (debug_flags >> 8) & 0x1F;
+    if (forced_stages > 0 && forced_stages < stages) stages = forced_stages;
+    if (stages < 2) return RN_ERR_SHAPE;
+    int ctas_per_sm = (debug_flags >> 4) & 0xF;
+    if (ctas_per_sm <= 0) ctas_per_sm = 1;
+    if (ctas_per_sm > 1) {
+        // split the ring between the co-resident CTAs
+        stages = stages / ctas_per_sm;
+        if (stages < 2) return RN_ERR_SHAPE;
+    }
+    const size_t smem = bulk_smem_bytes(stages, R, N);
+    int64_t grid = static_cast<int64_t>(dev.sm_count) * ctas_per_sm;
+    if (grid > M) grid = M;
+    BulkArgs a{x, w, y, M, N, eps, stages, debug_flags & 1,
+               timeout_ns ? timeout_ns : 2000000000ull};
+    const int g = static_cast<int>(grid);
+    if (nt == 128 && vpr == 1) return launch_bulk_inst<1, 8, 128>(a, g, smem, smem_cap, st);
+    if (nt == 256 && vpr == 1) return launch_bulk_inst<1, 8, 256>(a, g, smem, smem_cap, st);
+    if (nt == 256 && vpr == 2) return launch_bulk_inst<2, 4, 256>(a, g, smem, smem_cap, st);
+    if (nt == 256 && vpr == 4) return launch_bulk_inst<4, 2, 256>(a, g, smem, smem_cap, st);
+    if (nt == 256 && vpr == 8) return launch_bulk_inst<8, 1, 256>(a, g, smem, smem_cap, st);
+    if (nt == 512 && vpr == 8) return launch_bulk_inst<8, 1, 512>(a, g, smem, smem_cap, st);
+    return RN_ERR_SHAPE;
+}
+
+static int auto_schedule(int64_t M, int N, const DeviceInfo &dev) {
+    int nt, vpr, R;
+    if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
+    if (bulk_geometry(N, &nt, &vpr, &R) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
+    if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
+    return RN_SCHED_CTA_ROW;
+}
+
+static int rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N,
+                            rn_bf16 *y, int schedule, uint64_t timeout_ns, int debug_flags,
+                            rn_stream_t stream) {
+    if (M < 0 || N < 8 || N > 65536 || (N % 8) != 0) return RN_ERR_SHAPE;
+    if (M == 0) return RN_OK;
+    if (!x || !w || !y) return RN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return RN_ERR_ALIGN;
+    if (schedule < RN_SCHED_AUTO || schedule > RN_SCHED_PERSIST_BULK) return RN_ERR_ARG;
+    const DeviceInfo *dev = current_device_info();
+    if (!dev) return RN_ERR_DEVICE;
+    const int n = static_cast<int>(N);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(M, n, *dev);
+    switch (schedule) {
+        case RN_SCHED_WARP_ROW: return launch_warp_rows(x, w, eps, M, n, y, st, *dev);
+        case RN_SCHED_CTA_ROW: return launch_cta_rows(x, w, eps, M, n, y, st, *dev);
+        case RN_SCHED_PERSIST_BULK:
+            return launch_persistent_bulk(x, w, eps, M, n, y, st, *dev, timeout_ns, debug_flags);
+    }
+    return RN_ERR_ARG;
+}
+
+}  // namespace rn
+
+extern "C" {
+
+int rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N, rn_bf16 *y,
+                rn_stream_t stream) {
+    return rn::rmsnorm_dispatch(x, w, eps, M, N, y, RN_SCHED_AUTO, 0, 0, stream);
+}
+
+int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N,
+                      rn_bf16 *y, int schedule, uint64_t wait_timeout_ns, int debug_flags,
+                      rn_stream_t stream) {
+    return rn::rmsnorm_dispatch(x, w, eps, M, N, y, schedule, wait_timeout_ns, debug_flags,
+                                stream);
+}
+
+int rmsnorm_select_schedule(int64_t M, int64_t N) {
+    if (M < 0 || N < 8 || N > 65536 || (N % 8) != 0) return RN_ERR_SHAPE;
+    const rn::DeviceInfo *dev = rn::current_device_info();
+    if (!dev) return RN_ERR_DEVICE;
+    return rn::auto_schedule(M, static_cast<int>(N), *dev);
+}
+
+int rn_device_status(unsigned int *out, int clear) {
+    if (!out) return RN_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return RN_ERR_DEVICE;
+    }
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, rn::g_status, sizeof v) != cudaSuccess) {
+        cudaGetLastError();
+        return RN_ERR_DEVICE;
+    }
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(rn::g_status, &zero, sizeof zero) != cudaSuccess) {
+            cudaGetLastError();
+            return RN_ERR_DEVICE;
+        }
+    }
+    *out = v;
+    return RN_OK;
+}
+
+const char *rn_error_string(int code) {
+    switch (code) {
+        case RN_OK: return "ok";
+        case RN_ERR_NULL: return "a required pointer is NULL";
+        case RN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+        case RN_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case RN_ERR_LAUNCH: return "CUDA kernel launch failed";
+        case RN_ERR_DEVICE: return "no usable CUDA device";
+        case RN_ERR_ARG: return "invalid argument";
+    }
+    return "unknown status code";
+}
+
+int rn_version(void) { return 100; }
+
+}  // extern "C"

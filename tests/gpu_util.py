@@ -1,0 +1,40 @@
+"""Shared fixtures for the GPU parity tests."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from row_normalization_gb300 import binding
+from row_normalization_gb300.build import build
+from row_normalization_gb300.inputs import bf16_bits
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build()
+    binding.load()
+
+
+@functools.lru_cache(maxsize=8)
+def oracle_table(theta: float, max_pos: int, rotary_dim: int) -> np.ndarray:
+    return oracle.rope_cos_sin(theta, max_pos, rotary_dim)
+
+
+def padded_empty(shape, dtype, pad: int, fill_bits: int):
+    """A CUDA tensor of `shape` carved from a larger buffer whose `pad`
+    elements on each side are set to a canary bit pattern."""
+    n = int(np.prod(shape))
+    buf = torch.empty(n + 2 * pad, dtype=torch.int16, device="cuda")
+    buf.fill_(np.int16(np.uint16(fill_bits).view(np.int16)))
+    view = buf[pad:pad + n].view(dtype).view(*shape)
+    return buf, view
+
+
+def canary_intact(buf: torch.Tensor, pad: int, fill_bits: int) -> bool:
+    b = bf16_bits(buf.view(torch.bfloat16))
+    return bool(np.all(b[:pad] == fill_bits) and np.all(b[-pad:] == fill_bits))

@@ -1,0 +1,130 @@
+"""The C-ABI library loads and exports every symbol row_norm.h declares, and
+its host-side argument checks answer before anything touches a device
+(CPU only: no compute call is made here)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from row_normalization_gb300 import binding
+from row_normalization_gb300.build import ROOT, build
+
+HEADER = os.path.join(ROOT, "include", "row_norm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("rmsnorm_fwd", "qk_norm_rope_fwd", "qk_norm_rope_fwd_checked",
+                     "rope_cos_sin_table", "rn_error_string", "rn_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in row_norm.h but not exported"
+
+
+def test_error_strings_and_version(lib):
+    assert binding.error_string(0) == "ok"
+    for code in range(-6, 0):
+        s = binding.error_string(code)
+        assert s and s != "unknown status code"
+    assert binding.error_string(-99) == "unknown status code"
+    assert binding.version() >= 100
+
+
+# Fake but well-formed pointer values: the checks below must reject the call
+# before any of them is dereferenced or handed to the driver.
+P = 0x10000
+MISALIGNED = 0x10008
+
+
+@pytest.mark.parametrize("M,N,expect", [
+    (4, 7, binding.RN_ERR_SHAPE),       # N % 8 != 0
+    (4, 0, binding.RN_ERR_SHAPE),
+    (4, 65544, binding.RN_ERR_SHAPE),   # N > 65536
+    (-1, 64, binding.RN_ERR_SHAPE),
+    (0, 64, binding.RN_OK),             # empty: no-op
+])
+def test_rmsnorm_shape_checks(lib, M, N, expect):
+    assert lib.rmsnorm_fwd(P, P, 1e-6, M, N, P, None) == expect
+
+
+def test_rmsnorm_null_and_alignment_checks(lib):
+    assert lib.rmsnorm_fwd(None, P, 1e-6, 4, 64, P, None) == binding.RN_ERR_NULL
+    assert lib.rmsnorm_fwd(P, None, 1e-6, 4, 64, P, None) == binding.RN_ERR_NULL
+    assert lib.rmsnorm_fwd(P, P, 1e-6, 4, 64, None, None) == binding.RN_ERR_NULL
+    assert lib.rmsnorm_fwd(MISALIGNED, P, 1e-6, 4, 64, P, None) == binding.RN_ERR_ALIGN
+    assert lib.rmsnorm_fwd(P, P, 1e-6, 4, 64, MISALIGNED, None) == binding.RN_ERR_ALIGN
+    assert lib.rmsnorm_fwd_sched(P, P, 1e-6, 4, 64, P, 9, 0, 0, None) == binding.RN_ERR_ARG
+
+
+@pytest.mark.parametrize("T,Hq,Hkv,D,r,expect", [
+    (4, 32, 8, 96, 96, binding.RN_ERR_SHAPE),     # D unsupported
+    (4, 32, 8, 128, 127, binding.RN_ERR_SHAPE),   # odd rotary_dim
+    (4, 32, 8, 128, 256, binding.RN_ERR_SHAPE),   # rotary_dim > D
+    (4, 32, 8, 128, 48, binding.RN_ERR_SHAPE),    # rotary_dim not D, D/2 or D/4
+    (-1, 32, 8, 128, 128, binding.RN_ERR_SHAPE),
+    (4, -1, 8, 128, 128, binding.RN_ERR_SHAPE),
+    (0, 32, 8, 128, 128, binding.RN_OK),          # no tokens
+    (4, 0, 0, 128, 128, binding.RN_OK),           # no Q/K heads
+    (1 << 26, 32, 8, 128, 128, binding.RN_ERR_SHAPE),  # T*(Hq+Hkv) >= 2^31
+])
+def test_qk_shape_checks(lib, T, Hq, Hkv, D, r, expect):
+    assert lib.qk_norm_rope_fwd(P, P, P, P, P, T, Hq, Hkv, D, r, 1e-6, None) == expect
+
+
+def test_qk_null_alignment_and_checked_args(lib):
+    assert lib.qk_norm_rope_fwd(P, P, None, P, P, 4, 2, 1, 128, 128, 1e-6, None) == binding.RN_ERR_NULL
+    assert lib.qk_norm_rope_fwd(P, P, P, P, MISALIGNED, 4, 2, 1, 128, 128, 1e-6, None) == binding.RN_ERR_ALIGN
+    assert lib.qk_norm_rope_fwd_checked(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 0, P, None) == binding.RN_ERR_SHAPE
+    assert lib.qk_norm_rope_fwd_checked(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 16, None, None) == binding.RN_ERR_NULL
+    assert lib.qk_norm_rope_fwd_sched(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 3, None) == binding.RN_ERR_ARG
+
+
+def test_table_checks(lib):
+    assert lib.rope_cos_sin_table(1e6, 16, 7, P, None) == binding.RN_ERR_SHAPE
+    assert lib.rope_cos_sin_table(-1.0, 16, 8, P, None) == binding.RN_ERR_SHAPE
+    assert lib.rope_cos_sin_table(1e6, 0, 8, P, None) == binding.RN_OK
+    assert lib.rope_cos_sin_table(1e6, 16, 8, None, None) == binding.RN_ERR_NULL
+    assert lib.rope_cos_sin_table(1e6, 16, 8, MISALIGNED, None) == binding.RN_ERR_ALIGN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_no_device_is_reported_not_crashed(lib):
+    # Well-formed arguments on a host without a GPU: the library must answer
+    # RN_ERR_DEVICE instead of launching.
+    assert lib.rmsnorm_fwd(P, P, 1e-6, 4, 64, P, None) == binding.RN_ERR_DEVICE
+    v = ctypes.c_uint(0)
+    assert lib.rn_device_status(ctypes.byref(v), 0) == binding.RN_ERR_DEVICE
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    import row_normalization_gb300.binding as b
+    saved = b._lib
+    try:
+        b._lib = None
+        with pytest.raises(RuntimeError, match="build the CUDA library"):
+            b.load(str(tmp_path / "missing.so"))
+    finally:
+        b._lib = saved
+        importlib.invalidate_caches()

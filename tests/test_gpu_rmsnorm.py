@@ -1,0 +1,181 @@
+"""GPU parity: rmsnorm_fwd (CUDA, through the C ABI) against the fp64 oracle.
+
+RMSNorm: "[Inductor] Codegen Gluon", section 3.1.  Sizes: small shapes that
+span several tiles with ragged tails for every schedule (full comparison),
+then the measured workloads at full size in the launch configuration the
+bench times (sampled rows against the oracle, every row against a property
+check).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from row_normalization_gb300 import binding
+from row_normalization_gb300.inputs import bf16_bits, rmsnorm_inputs
+from tests.exact import ulp_distance_bf16
+from tests.gpu_util import canary_intact, padded_empty, require_gpu
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+SCHEDULES = [binding.RN_SCHED_AUTO, binding.RN_SCHED_WARP_ROW, binding.RN_SCHED_CTA_ROW,
+             binding.RN_SCHED_PERSIST_BULK]
+
+
+def eligible(schedule: int, N: int) -> bool:
+    if schedule == binding.RN_SCHED_WARP_ROW:
+        return N <= 2048
+    if schedule == binding.RN_SCHED_PERSIST_BULK:
+        return N in (1024, 2048, 4096, 8192, 16384, 32768)
+    return True
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+SMALL_SHAPES = [(1, 8), (3, 8), (7, 64), (5, 1000), (33, 2048), (3, 4104), (130, 1024),
+                (300, 4096), (17, 8192), (9, 16384), (5, 32768), (2, 65536), (1000, 512),
+                (157, 3072), (611, 2048)]
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("M,N", SMALL_SHAPES)
+def test_small_shapes_every_schedule(M, N, schedule):
+    x, w = rmsnorm_inputs(M, N, outlier_frac=0.05 if M >= 20 else 0.0, seed=M * 7 + N)
+    want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6)
+    xd, wd = x.cuda(), w.cuda()
+    pad = 64
+    buf, y = padded_empty((M, N), torch.bfloat16, pad, 0x7FC1)
+    if not eligible(schedule, N):
+        with pytest.raises(binding.RowNormError) as ei:
+            binding.rmsnorm_fwd(xd, wd, 1e-6, y, schedule=schedule)
+        assert ei.value.code == binding.RN_ERR_SHAPE
+        return
+    binding.rmsnorm_fwd(xd, wd, 1e-6, y, schedule=schedule)
+    torch.cuda.synchronize()
+    assert_parity(bf16_bits(y), want, f"M={M} N={N} sched={schedule}")
+    assert canary_intact(buf, pad, 0x7FC1), "write outside y"
+    assert np.array_equal(bf16_bits(xd), bf16_bits(x)), "x modified"
+
+
+def test_persistent_ring_wraps_many_times_with_ragged_split():
+    # Many more units than stages, M not a multiple of the grid or of R.
+    for N, M, stages in [(1024, 5003, 2), (4096, 2311, 3), (16384, 997, 2)]:
+        x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=N + M)
+        want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6)
+        y = binding.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6, schedule=binding.RN_SCHED_PERSIST_BULK,
+                                debug_flags=stages << 8)
+        assert_parity(bf16_bits(y), want, f"ring N={N} M={M} S={stages}")
+
+
+def test_two_ctas_per_sm_variant():
+    x, w = rmsnorm_inputs(1201, 4096, seed=5)
+    want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6)
+    y = binding.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6, schedule=binding.RN_SCHED_PERSIST_BULK,
+                            debug_flags=2 << 4)
+    assert_parity(bf16_bits(y), want, "2 CTAs/SM")
+
+
+def test_special_rows():
+    N = 4096
+    x = torch.zeros(6, N, dtype=torch.bfloat16)
+    x[1] = 3.0                       # constant row
+    x[2, 17] = -7.5                  # one-hot row
+    x[3] = torch.randn(N) * 1e-3     # tiny values: eps dominates
+    x[4] = torch.randn(N) * 1e3
+    x[5, ::2] = 1.0
+    w = torch.ones(N, dtype=torch.bfloat16)
+    for eps in (1e-6, 1e-5, 0.0 + 1e-30):
+        want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), eps)
+        for sched in SCHEDULES[1:]:
+            if not eligible(sched, N):
+                continue
+            y = binding.rmsnorm_fwd(x.cuda(), w.cuda(), eps, schedule=sched)
+            got = bf16_bits(y)
+            assert_parity(got, want, f"special eps={eps} sched={sched}")
+            assert np.all(got[0] == 0)  # zero row stays zero
+
+
+def test_empty_and_errors():
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    assert binding.rmsnorm_fwd(x, w, 1e-6).shape == (0, 64)
+    with pytest.raises(binding.RowNormError):
+        xx = torch.ones(4, 12, dtype=torch.bfloat16, device="cuda")
+        binding.rmsnorm_fwd(xx, torch.ones(12, dtype=torch.bfloat16, device="cuda"), 1e-6)
+    with pytest.raises(binding.RowNormError) as ei:
+        binding.rmsnorm_fwd(torch.ones(2, 7, dtype=torch.bfloat16, device="cuda"),
+                            torch.ones(7, dtype=torch.bfloat16, device="cuda"), 1e-6)
+    assert ei.value.code == binding.RN_ERR_SHAPE
+
+
+def test_wait_timeout_reports_status_and_context_survives():
+    # The persistent schedule is told never to issue its copies, so its
+    # bounded waits run out (2 ms): the kernel must record the timeout in the
+    # status word and return, leaving the context usable.
+    binding.device_status(clear=True)
+    x, w = rmsnorm_inputs(2, 1024, seed=3)
+    xd, wd = x.cuda(), w.cuda()
+    binding.rmsnorm_fwd(xd, wd, 1e-6, schedule=binding.RN_SCHED_PERSIST_BULK,
+                        wait_timeout_ns=2_000_000, debug_flags=1)
+    st = binding.device_status(clear=True)
+    assert st & binding.RN_STATUS_WAIT_TIMEOUT
+    y = binding.rmsnorm_fwd(xd, wd, 1e-6, schedule=binding.RN_SCHED_PERSIST_BULK)
+    assert_parity(bf16_bits(y), oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6), "after timeout")
+    assert binding.device_status(clear=True) == 0
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, auto schedule (what the bench launches)
+# ---------------------------------------------------------------------------
+
+def _check_full_size(M, N, eps, outlier_frac, seed=0, n_sample=96):
+    x, w = rmsnorm_inputs(M, N, outlier_frac=outlier_frac, device="cuda", seed=seed)
+    y = binding.rmsnorm_fwd(x, w, eps)
+    torch.cuda.synchronize()
+    # 1) sampled rows against the oracle: first, last, the outlier rows, random rows
+    rng = np.random.default_rng(seed + M + N)
+    rows = {0, M - 1}
+    k = int(round(outlier_frac * M))
+    if k:
+        out_rows = torch.randperm(M, generator=torch.Generator().manual_seed(seed + 2))[:k]
+        rows |= set(out_rows[:64].tolist())
+    rows |= set(rng.choice(M, size=min(n_sample, M), replace=False).tolist())
+    rows = np.array(sorted(rows))
+    idx = torch.from_numpy(rows).cuda()
+    xs = bf16_bits(x.index_select(0, idx))
+    want = oracle.rmsnorm(xs, bf16_bits(w), eps)
+    got = bf16_bits(y.index_select(0, idx))
+    assert_parity(got, want, f"sampled rows M={M} N={N}")
+    # 2) every row: within one bf16 step of an fp32 torch restatement (a
+    #    property that holds at any size; the oracle is the judge above)
+    wf = w.float()
+    for r0 in range(0, M, 4096):
+        xb = x[r0:r0 + 4096].float()
+        ref = (xb * torch.rsqrt(xb.pow(2).mean(-1, keepdim=True) + eps) * wf).to(torch.bfloat16)
+        d = ulp_distance_bf16(bf16_bits(ref), bf16_bits(y[r0:r0 + 4096]))
+        assert d.max() <= 1, f"rows {r0}.. differ from fp32 restatement by {d.max()} steps"
+    del x, y
+
+
+def test_latency_config_full():
+    # 64 x 4096: small enough to compare every element with the oracle
+    x, w = rmsnorm_inputs(64, 4096, device="cuda", seed=0)
+    y = binding.rmsnorm_fwd(x, w, 1e-6)
+    assert_parity(bf16_bits(y), oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6), "64x4096")
+
+
+@pytest.mark.parametrize("M", [4096, 8192, 16384, 32768])
+@pytest.mark.parametrize("N", [4096, 8192, 16384])
+def test_sweep_full_size(M, N):
+    _check_full_size(M, N, 1e-6, 0.01)
+
+
+@pytest.mark.parametrize("M", [1024, 4096, 8192])
+def test_wide_rows_full_size(M):
+    _check_full_size(M, 32768, 1e-5, 0.0)
