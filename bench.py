@@ -69,6 +69,26 @@ def step_bytes() -> int:
     return sum(rms_bytes(M, N) for M, N in RMS_SHAPES) + sum(qk_bytes(QK_T, r) for r in QK_ROT)
 
 
+def restrict_workload(spec: str) -> None:
+    """--only: keep a subset of the step, e.g. "rms:8192x16384,qk:16384:128".
+    Used for profiling one launch; the printed line names the reduced workload."""
+    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD
+    rms, rot = [], []
+    for item in spec.split(","):
+        kind, _, rest = item.partition(":")
+        if kind == "rms":
+            M, N = rest.split("x")
+            rms.append((int(M), int(N)))
+        elif kind == "qk":
+            T, r = rest.split(":")
+            QK_T = int(T)
+            rot.append(int(r))
+        else:
+            raise SystemExit(f"bad --only item {item!r}")
+    RMS_SHAPES, QK_ROT = rms, tuple(rot)
+    WORKLOAD = "subset: " + spec
+
+
 # ---------------------------------------------------------------------------
 # environment helpers
 # ---------------------------------------------------------------------------
@@ -326,9 +346,9 @@ def run_ours(args) -> int:
         "frac_of_measured_copy": round(value / world / hbm_peak, 4),
         "frac_of_spec_7928": round(value / world / SPEC_GBS, 4),
         "per_op": {"rmsnorm_sweep_gbs": round(sum(rms_bytes(M, N) for M, N in RMS_SHAPES)
-                                              / (rms_ms * 1e-3) / 1e9, 1),
+                                              / (rms_ms * 1e-3) / 1e9, 1) if rms_ms else None,
                    "qk_norm_rope_gbs": round(sum(qk_bytes(QK_T, r) for r in QK_ROT)
-                                             / (qk_ms * 1e-3) / 1e9, 1)},
+                                             / (qk_ms * 1e-3) / 1e9, 1) if qk_ms else None},
         "per_shape": per_shape,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -518,7 +538,10 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="profile a subset, e.g. rms:8192x16384")
     args = ap.parse_args()
+    if args.only:
+        restrict_workload(args.only)
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3  # never time without at least three warm-up steps
     if args.impl == "reference":
