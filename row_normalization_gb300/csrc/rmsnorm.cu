@@ -167,6 +167,37 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N) {
            static_cast<size_t>(2) * R * 32 * 4 + 16;
 }
 
+// Which rows the k-th unit of CTA b covers.  Units go round-robin: round q
+// gives CTA b rows [q*G*R + b*R, +R), so at any moment the grid streams one
+// contiguous band of memory.  A last, partial round is re-split evenly (rows
+// per CTA ceil(rem / G)) so no CTA is left with a whole extra unit.
+struct UnitSchedule {
+    int64_t full_rounds;  // rounds in which every CTA gets R rows
+    int64_t rem;          // rows left for the final round
+    int64_t last_r;       // rows per CTA in the final round
+    int64_t G;
+    int R;
+
+    __device__ __forceinline__ UnitSchedule(int64_t M, int64_t G_, int R_) : G(G_), R(R_) {
+        full_rounds = M / (G * R);
+        rem = M - full_rounds * G * R;
+        last_r = (rem + G - 1) / G;
+    }
+    __device__ __forceinline__ int64_t units(int64_t b) const {
+        return full_rounds + ((rem > 0 && b * last_r < rem) ? 1 : 0);
+    }
+    __device__ __forceinline__ void unit(int64_t b, int64_t k, int64_t *r0, int *rows) const {
+        if (k < full_rounds) {
+            *r0 = k * G * R + b * R;
+            *rows = R;
+        } else {
+            *r0 = full_rounds * G * R + b * last_r;
+            const int64_t left = rem - b * last_r;
+            *rows = static_cast<int>(left < last_r ? left : last_r);
+        }
+    }
+};
+
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
 template <int VPR, int R, int NT>
 __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const BulkArgs a) {
@@ -200,17 +231,16 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
     }
     __syncthreads();
 
-    // Contiguous, balanced row range of this CTA (at most one row of skew).
-    const int64_t G = gridDim.x;
-    const int64_t r_begin = (a.M * static_cast<int64_t>(blockIdx.x)) / G;
-    const int64_t r_end = (a.M * (static_cast<int64_t>(blockIdx.x) + 1)) / G;
+    const UnitSchedule sched(a.M, gridDim.x, R);
+    const int64_t bid = blockIdx.x;
+    const int64_t n_units = sched.units(bid);
 
     if (warp == NW) {
         // ---- producer ----
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             int64_t k = 0;
-            for (int64_t r0 = r_begin; r0 < r_end; r0 += R, ++k) {
+            for (; k < n_units; ++k) {
                 const int s = static_cast<int>(k % S);
                 if (k >= S) {
                     const uint32_t par = static_cast<uint32_t>((k / S - 1) & 1);
@@ -220,9 +250,10 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
                         break;
                     }
                 }
-                const int64_t left = r_end - r0;
-                const uint32_t rows = static_cast<uint32_t>(left < R ? left : R);
-                const uint32_t bytes = rows * row_bytes;
+                int64_t r0;
+                int rows;
+                sched.unit(bid, k, &r0, &rows);
+                const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
                 mbar_arrive_expect_tx(&full[s], bytes);
                 if (!(a.debug & 1))
                     bulk_copy_g2s(ring + static_cast<size_t>(s) * stage_bytes, a.x + r0 * N, bytes,
@@ -251,8 +282,10 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 #pragma unroll
     for (int j = 0; j < VPR; ++j) wv[j] = ld_ro16(a.w + 8 * (tid + j * NT));
 
-    int64_t k = 0;
-    for (int64_t r0 = r_begin; r0 < r_end; r0 += R, ++k) {
+    for (int64_t k = 0; k < n_units; ++k) {
+        int64_t r0;
+        int rows;
+        sched.unit(bid, k, &r0, &rows);
         // Keep the weights packed (bf16) across rows: without this the
         // compiler hoists their fp32 widening out of the loop and doubles
         // the register footprint.
@@ -303,8 +336,6 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
         }
         named_bar_sync(1, NT);
         if (flags[k & 1]) break;  // same decision in every consumer warp
-        const int64_t left = r_end - r0;
-        const int rows = static_cast<int>(left < R ? left : R);
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             if (rr < rows) {
@@ -373,20 +404,25 @@ static int launch_cta_rows(const uint16_t *x, const uint16_t *w, float eps, int6
 
 // Chooses (consumer threads, chunks per thread per row, rows per stage) for
 // the persistent schedule; false when N does not fit it.
-static bool bulk_geometry(int N, int *nt, int *vpr, int *R) {
-    // One instantiation per row width: NT consumer threads x VPR chunks of 8
-    // elements cover a row exactly, and R rows make a stage of 8 chunks per
-    // consumer thread.
+// Geometry of the persistent schedule per row width, measured on GB300:
+// NT consumer threads x VPR 16-byte chunks cover one row exactly, R rows make
+// a stage, and two stages in flight per SM (32-64 KiB each) stream best --
+// deeper rings measured slower (more concurrent DRAM streams, no more
+// bandwidth).
+struct BulkGeometry {
+    int nt, vpr, R, stages;
+};
+
+static bool bulk_geometry(int N, BulkGeometry *g) {
     switch (N) {
-        case 1024: *nt = 128; *vpr = 1; break;
-        case 2048: *nt = 256; *vpr = 1; break;
-        case 4096: *nt = 256; *vpr = 2; break;
-        case 8192: *nt = 256; *vpr = 4; break;
-        case 16384: *nt = 256; *vpr = 8; break;
-        case 32768: *nt = 512; *vpr = 8; break;
+        case 1024: *g = {128, 1, 8, 2}; break;
+        case 2048: *g = {256, 1, 8, 2}; break;
+        case 4096: *g = {256, 2, 8, 2}; break;
+        case 8192: *g = {256, 4, 2, 2}; break;
+        case 16384: *g = {512, 4, 1, 2}; break;
+        case 32768: *g = {512, 8, 1, 2}; break;
         default: return false;
     }
-    *R = 8 / *vpr;
     return true;
 }
 
@@ -412,41 +448,40 @@ static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_c
 static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float eps, int64_t M,
                                   int N, uint16_t *y, cudaStream_t st, const DeviceInfo &dev,
                                   uint64_t timeout_ns, int debug_flags) {
-    int nt, vpr, R;
-    if (!bulk_geometry(N, &nt, &vpr, &R)) return RN_ERR_SHAPE;
+    BulkGeometry geo;
+    if (!bulk_geometry(N, &geo)) return RN_ERR_SHAPE;
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
-    int stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, R, N)) /
-                                  (static_cast<size_t>(R) * N * 2 + 16));
-    if (stages > 16) stages = 16;
+    const size_t stage_cost = static_cast<size_t>(geo.R) * N * 2 + 16;
+    int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N)) / stage_cost);
+    if (max_stages > 16) max_stages = 16;
+    int stages = geo.stages;
     const int forced_stages = (debug_flags >> 8) & 0x1F;
-    if (forced_stages > 0 && forced_stages < stages) stages = forced_stages;
-    if (stages < 2) return RN_ERR_SHAPE;
+    if (forced_stages > 0) stages = forced_stages;
     int ctas_per_sm = (debug_flags >> 4) & 0xF;
     if (ctas_per_sm <= 0) ctas_per_sm = 1;
-    if (ctas_per_sm > 1) {
-        // split the ring between the co-resident CTAs
-        stages = stages / ctas_per_sm;
-        if (stages < 2) return RN_ERR_SHAPE;
-    }
-    const size_t smem = bulk_smem_bytes(stages, R, N);
+    if (stages * ctas_per_sm > max_stages) stages = max_stages / ctas_per_sm;
+    if (stages < 2) return RN_ERR_SHAPE;
+    const size_t smem = bulk_smem_bytes(stages, geo.R, N);
     int64_t grid = static_cast<int64_t>(dev.sm_count) * ctas_per_sm;
     if (grid > M) grid = M;
     BulkArgs a{x, w, y, M, N, eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
     const int g = static_cast<int>(grid);
-    if (nt == 128 && vpr == 1) return launch_bulk_inst<1, 8, 128>(a, g, smem, smem_cap, st);
-    if (nt == 256 && vpr == 1) return launch_bulk_inst<1, 8, 256>(a, g, smem, smem_cap, st);
-    if (nt == 256 && vpr == 2) return launch_bulk_inst<2, 4, 256>(a, g, smem, smem_cap, st);
-    if (nt == 256 && vpr == 4) return launch_bulk_inst<4, 2, 256>(a, g, smem, smem_cap, st);
-    if (nt == 256 && vpr == 8) return launch_bulk_inst<8, 1, 256>(a, g, smem, smem_cap, st);
-    if (nt == 512 && vpr == 8) return launch_bulk_inst<8, 1, 512>(a, g, smem, smem_cap, st);
+    switch (N) {
+        case 1024: return launch_bulk_inst<1, 8, 128>(a, g, smem, smem_cap, st);
+        case 2048: return launch_bulk_inst<1, 8, 256>(a, g, smem, smem_cap, st);
+        case 4096: return launch_bulk_inst<2, 8, 256>(a, g, smem, smem_cap, st);
+        case 8192: return launch_bulk_inst<4, 2, 256>(a, g, smem, smem_cap, st);
+        case 16384: return launch_bulk_inst<4, 1, 512>(a, g, smem, smem_cap, st);
+        case 32768: return launch_bulk_inst<8, 1, 512>(a, g, smem, smem_cap, st);
+    }
     return RN_ERR_SHAPE;
 }
 
 static int auto_schedule(int64_t M, int N, const DeviceInfo &dev) {
-    int nt, vpr, R;
+    BulkGeometry geo;
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    if (bulk_geometry(N, &nt, &vpr, &R) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
+    if (bulk_geometry(N, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
     return RN_SCHED_CTA_ROW;
 }

@@ -74,7 +74,8 @@ def test_persistent_ring_wraps_many_times_with_ragged_split():
 
 
 def test_two_ctas_per_sm_variant():
-    x, w = rmsnorm_inputs(1201, 4096, seed=5)
+    # two co-resident persistent CTAs per SM, each with a two-stage ring
+    x, w = rmsnorm_inputs(1201, 8192, seed=5)
     want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6)
     y = binding.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6, schedule=binding.RN_SCHED_PERSIST_BULK,
                             debug_flags=2 << 4)
