@@ -201,6 +201,8 @@ def traffic_per_launch(kernel: str, workload: str):
 # ---------------------------------------------------------------------------
 
 RMS_KERNELS = {1: "rms_warp_rows_kernel", 2: "rms_cta_rows_kernel", 3: "rms_persistent_bulk_kernel"}
+QK_KERNELS = {1: "qk_norm_rope_kernel", 2: "qk_norm_rope_kernel", 4: "qk_norm_rope_kernel",
+              8: "qk_norm_rope_kernel", 16: "qk_persistent_bulk_kernel"}
 
 
 def build_inputs(torch, binding, inputs, device):
@@ -219,6 +221,9 @@ def build_inputs(torch, binding, inputs, device):
     return rms, qk
 
 
+FORCE = {"rms": 0, "qk": 0}  # schedule overrides (--rms-schedule / --qk-schedule)
+
+
 def launch_step(binding, rms, qk, events=None):
     """Enqueue one step; optionally record an event before every launch."""
     k = 0
@@ -226,13 +231,13 @@ def launch_step(binding, rms, qk, events=None):
         if events is not None:
             events[k].record()
         k += 1
-        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"])
+        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
     for c in qk:
         if events is not None:
             events[k].record()
         k += 1
         binding.qk_norm_rope_fwd(c["qkv"], c["wq"], c["wk"], c["table"], c["pos"], HQ, HKV, D,
-                                 c["r"], QK_EPS)
+                                 c["r"], QK_EPS, schedule=FORCE["qk"])
     return k
 
 
@@ -302,7 +307,7 @@ def run_ours(args) -> int:
 
     per_shape = []
     for k, c in enumerate(rms):
-        sched = binding.rmsnorm_select_schedule(c["M"], c["N"])
+        sched = FORCE["rms"] or binding.rmsnorm_select_schedule(c["M"], c["N"])
         b = rms_bytes(c["M"], c["N"])
         per_shape.append({"op": "rmsnorm", "M": c["M"], "N": c["N"],
                           "kernel": RMS_KERNELS.get(sched, str(sched)),
@@ -311,8 +316,9 @@ def run_ours(args) -> int:
     for j, c in enumerate(qk):
         k = len(rms) + j
         b = qk_bytes(QK_T, c["r"])
+        qs = FORCE["qk"] or binding.qk_norm_rope_select_schedule(QK_T)
         per_shape.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
-                          "kernel": "qk_norm_rope_kernel",
+                          "kernel": QK_KERNELS.get(qs, str(qs)),
                           "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
                           "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
     for p in per_shape:
@@ -539,7 +545,10 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="profile a subset, e.g. rms:8192x16384")
+    ap.add_argument("--rms-schedule", type=int, default=0, help="force an RN_SCHED_* value")
+    ap.add_argument("--qk-schedule", type=int, default=0, help="force an RN_QK_* value")
     args = ap.parse_args()
+    FORCE["rms"], FORCE["qk"] = args.rms_schedule, args.qk_schedule
     if args.only:
         restrict_workload(args.only)
     if args.impl == "ours" and args.warmup < 3:

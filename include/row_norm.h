@@ -163,23 +163,32 @@ int qk_norm_rope_fwd_checked(rn_bf16 *qkv, const rn_bf16 *wq,
                              int64_t max_pos, int *d_err_flag,
                              rn_stream_t stream);
 
-/* Heads per warp that qk_norm_rope_fwd_sched can force. */
+/* Schedules that qk_norm_rope_fwd_sched can force. */
 enum {
     RN_QK_AUTO = 0,
     RN_QK_HEAD_PER_WARP = 1,   /* 32 lanes per head                      */
     RN_QK_TWO_HEADS = 2,       /* 16 lanes per head                      */
     RN_QK_FOUR_HEADS = 4,      /* 8 lanes per head                       */
-    RN_QK_PERSISTENT = 8       /* 8 lanes per head, persistent grid       */
+    RN_QK_PERSISTENT = 8,      /* 8 lanes per head, persistent grid       */
+    RN_QK_BULK = 16            /* persistent CTAs stream whole tokens'
+                                  query/key regions and cos/sin rows
+                                  through a bulk-copy shared-memory ring */
 };
 
-/* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*). */
+/* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*).
+ * `wait_timeout_ns` and `debug_flags` (bit 0 only) act on RN_QK_BULK as on
+ * rmsnorm_fwd_sched's persistent schedule; 0 and 0 in normal use. */
 int qk_norm_rope_fwd_sched(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                            const float *cos_sin, const int64_t *positions,
                            int64_t T, int Hq, int Hkv, int D, int rotary_dim,
-                           float eps, int schedule, rn_stream_t stream);
+                           float eps, int schedule, uint64_t wait_timeout_ns,
+                           int debug_flags, rn_stream_t stream);
 
-/* The schedule (RN_QK_*) that qk_norm_rope_fwd launches for T tokens
- * (RN_ERR_SHAPE if T < 0).  Host-only query: launches nothing. */
+/* The schedule (RN_QK_*) that qk_norm_rope_fwd picks for T tokens (RN_ERR_SHAPE
+ * if T < 0).  When it picks RN_QK_BULK for a layout the ring cannot hold
+ * (D = 64 with rotary_dim = 16, or a token wider than the ring's shared
+ * memory) qk_norm_rope_fwd runs RN_QK_PERSISTENT instead.  Host-only query:
+ * launches nothing. */
 int qk_norm_rope_select_schedule(int64_t T);
 
 /* cos_sin[p, i] = cos(p * f_i), cos_sin[p, r/2 + i] = sin(p * f_i),

@@ -40,6 +40,7 @@ RN_QK_HEAD_PER_WARP = 1
 RN_QK_TWO_HEADS = 2
 RN_QK_FOUR_HEADS = 4
 RN_QK_PERSISTENT = 8
+RN_QK_BULK = 16
 
 
 class RowNormError(RuntimeError):
@@ -74,7 +75,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qk_norm_rope_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, vp]
         L.qk_norm_rope_fwd.restype = i32
         L.qk_norm_rope_fwd_sched.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
-                                             i32, vp]
+                                             i32, u64, i32, vp]
         L.qk_norm_rope_fwd_sched.restype = i32
         L.qk_norm_rope_fwd_checked.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
                                                i64, vp, vp]
@@ -171,18 +172,20 @@ def _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim):
 def qk_norm_rope_fwd(qkv: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
                      cos_sin: torch.Tensor, positions: torch.Tensor, Hq: int, Hkv: int, D: int,
                      rotary_dim: int, eps: float, *, schedule: int = RN_QK_AUTO,
+                     wait_timeout_ns: int = 0, debug_flags: int = 0,
                      stream=None) -> torch.Tensor:
     """In place: per-head RMSNorm of Q and K heads, then neox RoPE.  Returns qkv."""
     T = _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim)
     L = load()
-    if schedule == RN_QK_AUTO:
+    if schedule == RN_QK_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
         rc = L.qk_norm_rope_fwd(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(), cos_sin.data_ptr(),
                                 positions.data_ptr(), T, Hq, Hkv, D, rotary_dim, eps,
                                 _stream(stream))
     else:
         rc = L.qk_norm_rope_fwd_sched(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(),
                                       cos_sin.data_ptr(), positions.data_ptr(), T, Hq, Hkv, D,
-                                      rotary_dim, eps, schedule, _stream(stream))
+                                      rotary_dim, eps, schedule, wait_timeout_ns, debug_flags,
+                                      _stream(stream))
     _check(rc, "qk_norm_rope_fwd")
     return qkv
 

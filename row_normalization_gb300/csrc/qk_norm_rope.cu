@@ -20,6 +20,12 @@
 
 namespace rn {
 
+// This translation unit's status word (RN_STATUS_* bits); rn_device_status()
+// ORs it with the other units' words.
+static __device__ unsigned int g_qk_status = 0u;
+
+__device__ __forceinline__ void raise_qk_status(unsigned int bits) { atomicOr(&g_qk_status, bits); }
+
 // ---- vector helpers -----------------------------------------------------------
 
 // CNT consecutive bf16 -> fp32.  The pointer is aligned to the widest of
@@ -104,6 +110,27 @@ __device__ __forceinline__ void load_f32(const float *p, float (&o)[CNT]) {
     } else {
 #pragma unroll
         for (int k = 0; k < CNT; ++k) o[k] = __ldg(p + k);
+    }
+}
+
+// CNT consecutive fp32 from shared memory (plain loads; __ldg is global-only).
+template <int CNT>
+__device__ __forceinline__ void load_f32_smem(const float *p, float (&o)[CNT]) {
+    if constexpr (CNT % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < CNT / 4; ++k) {
+            const float4 v = *reinterpret_cast<const float4 *>(p + 4 * k);
+            o[4 * k + 0] = v.x; o[4 * k + 1] = v.y; o[4 * k + 2] = v.z; o[4 * k + 3] = v.w;
+        }
+    } else if constexpr (CNT % 2 == 0) {
+#pragma unroll
+        for (int k = 0; k < CNT / 2; ++k) {
+            const float2 v = *reinterpret_cast<const float2 *>(p + 2 * k);
+            o[2 * k + 0] = v.x; o[2 * k + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CNT; ++k) o[k] = p[k];
     }
 }
 
@@ -209,6 +236,318 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
     }
 }
 
+// ---- persistent schedule: tokens streamed through a bulk-copy ring -------------
+//
+// One CTA per SM: 16 consumer warps (8 for 256-wide heads) and 1 producer warp.  A unit is `tps`
+// consecutive tokens; for each, the producer copies the token's contiguous
+// query+key region (H heads x D bf16; the value heads are skipped) and the
+// cos/sin row its position selects into a stage of a shared-memory ring with
+// 1D bulk copies, all completing on the stage's mbarrier.  Producer lane i
+// owns token i of the unit and loads its position one unit ahead.
+//
+// Consumer warps take four heads at a time from the stage (8 lanes per head:
+// the lane layout of qk_norm_rope_kernel) and keep wq and wk in registers as
+// packed bf16.  The arithmetic runs on fp32 pairs (Blackwell's packed
+// FFMA2/FMUL2), the results are stored in place with 16-byte writes, and each
+// warp releases the stage once it has read its heads.  Which warp takes which
+// quad of heads rotates from stage to stage, so no warp is always the one with
+// the extra quad.  No CTA-wide barrier after set-up.
+
+struct QkBulkArgs {
+    QkArgs q;
+    int tps;          // tokens per stage (<= 32: one producer lane per token)
+    int stages;
+    int debug;        // bit 0: never issue the copies (exercises the timeout path)
+    uint64_t inv_h;   // ceil(2^32 / H): token slot of stage head hh = (hh * inv_h) >> 32
+                      // (exact for hh, H < 2^16; 2^32 itself when H == 1)
+    uint64_t timeout_ns;
+};
+
+__host__ __device__ constexpr size_t qk_bulk_smem_bytes(int stages, int tps, int tok_bytes,
+                                                        int cs_bytes) {
+    return static_cast<size_t>(stages) * tps * (tok_bytes + cs_bytes) +  // ring
+           static_cast<size_t>(stages) * 16 +                            // full + empty
+           static_cast<size_t>(stages) * tps * 4 +                       // token valid flags
+           16;                                                           // abort flag
+}
+
+__device__ __forceinline__ void bulk_copy_g2s_plain(void *dst_smem, const void *src_gmem,
+                                                    uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float2 bf2f(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
+
+// CNT (even) consecutive bf16 as CNT/2 packed words; same alignment rules as load_bf.
+template <int CNT>
+__device__ __forceinline__ void load_words(const uint16_t *p, uint32_t (&o)[CNT / 2]) {
+    static_assert(CNT % 2 == 0, "even counts only");
+    if constexpr ((CNT * 2) % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < CNT / 8; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(p + 8 * k);
+            o[4 * k + 0] = v.x; o[4 * k + 1] = v.y; o[4 * k + 2] = v.z; o[4 * k + 3] = v.w;
+        }
+    } else if constexpr ((CNT * 2) % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < CNT / 4; ++k) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(p + 4 * k);
+            o[2 * k + 0] = v.x; o[2 * k + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CNT / 2; ++k) o[k] = *reinterpret_cast<const uint32_t *>(p + 2 * k);
+    }
+}
+
+template <int CNT>
+__device__ __forceinline__ void store_words(uint16_t *p, const uint32_t (&v)[CNT / 2]) {
+    if constexpr ((CNT * 2) % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < CNT / 8; ++k)
+            *reinterpret_cast<uint4 *>(p + 8 * k) =
+                make_uint4(v[4 * k + 0], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    } else if constexpr ((CNT * 2) % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < CNT / 4; ++k)
+            *reinterpret_cast<uint2 *>(p + 4 * k) = make_uint2(v[2 * k + 0], v[2 * k + 1]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < CNT / 2; ++k) *reinterpret_cast<uint32_t *>(p + 2 * k) = v[k];
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_f2(float2 v) { return pack_bf2(v.x, v.y); }
+
+// Consumer threads: 16 warps, or 8 for 256-wide heads (twice the per-lane state).
+template <int D>
+constexpr int qk_bulk_consumers() { return D >= 256 ? 256 : 512; }
+
+template <int D, int R>
+__global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
+    qk_persistent_bulk_kernel(const QkBulkArgs args) {
+    constexpr int LPH = 8;
+    constexpr int HPW = 32 / LPH;
+    constexpr int NT = qk_bulk_consumers<D>();
+    constexpr int NW = NT / 32;
+    constexpr int H2 = R / 2;
+    constexpr int A = H2 / LPH;          // elements per lane per rotary half
+    constexpr int B = (D - R) / LPH;     // tail elements per lane
+    constexpr int A2 = A / 2;
+    constexpr int B2 = B > 0 ? B / 2 : 1;
+    static_assert(A * LPH == H2 && B * LPH == D - R && A % 2 == 0 && B % 2 == 0,
+                  "bad lane layout");
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const QkArgs &a = args.q;
+    const int S = args.stages;
+    const int TPS = args.tps;
+    const int Hq = a.Hq;
+    const int H = a.Hq + a.Hkv;
+    const uint32_t tok_bytes = static_cast<uint32_t>(H) * D * 2;
+    const uint32_t cs_bytes = R * 4;
+    const uint32_t stage_bytes = static_cast<uint32_t>(TPS) * (tok_bytes + cs_bytes);
+    const int64_t W = static_cast<int64_t>(a.Hq + 2 * a.Hkv) * D;
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage_bytes);
+    uint64_t *empty = full + S;
+    volatile int *valid = reinterpret_cast<volatile int *>(empty + S);  // [S][TPS]
+    volatile int *abort_flag = valid + S * TPS;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const UnitSchedule sched(a.T, gridDim.x, TPS);
+    const int64_t bid = blockIdx.x;
+    const int64_t n_units = sched.units(bid);
+
+    if (warp == NW) {
+        // ---- producer warp ----
+        const uint64_t pol = l2_policy_evict_first();
+        int64_t p_next = 0;
+        if (n_units > 0) {
+            int64_t r0;
+            int rows;
+            sched.unit(bid, 0, &r0, &rows);
+            if (lane < rows) p_next = __ldg(a.pos + r0 + lane);
+        }
+        int64_t k = 0;
+        for (; k < n_units; ++k) {
+            const int s = static_cast<int>(k % S);
+            if (k >= S) {
+                const uint32_t par = static_cast<uint32_t>((k / S - 1) & 1);
+                const bool ok = __all_sync(
+                    0xffffffffu, mbar_wait_bounded(&empty[s], par, args.timeout_ns, abort_flag));
+                if (!ok) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        raise_qk_status(RN_STATUS_WAIT_TIMEOUT);
+                    }
+                    break;
+                }
+            }
+            int64_t r0;
+            int rows;
+            sched.unit(bid, k, &r0, &rows);
+            const int64_t p = p_next;
+            if (k + 1 < n_units) {
+                int64_t r1;
+                int rows1;
+                sched.unit(bid, k + 1, &r1, &rows1);
+                if (lane < rows1) p_next = __ldg(a.pos + r1 + lane);
+            }
+            bool pos_ok = true;
+            if (lane < rows) {
+                if (a.max_pos > 0 && (p < 0 || p >= a.max_pos)) {
+                    pos_ok = false;
+                    atomicOr(a.err, RN_STATUS_BAD_POSITION);
+                }
+                valid[s * TPS + lane] = pos_ok ? 1 : 0;
+            }
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rows) * (tok_bytes + cs_bytes));
+            __syncwarp();
+            if (lane < rows && !(args.debug & 1)) {
+                uint8_t *st = ring + static_cast<size_t>(s) * stage_bytes;
+                bulk_copy_g2s(st + lane * tok_bytes, a.qkv + (r0 + lane) * W, tok_bytes, &full[s],
+                              pol);
+                // A rejected position still completes the stage's byte count
+                // (row 0 is copied); its token is flagged and never stored.
+                bulk_copy_g2s_plain(st + static_cast<size_t>(TPS) * tok_bytes + lane * cs_bytes,
+                                    a.cos_sin + (pos_ok ? p : 0) * R, cs_bytes, &full[s]);
+            }
+        }
+        if (lane == 0) {
+            // Drain: every copy issued into this CTA's ring lands before exit.
+            const int64_t issued = k;
+            const uint64_t t0 = globaltimer_ns();
+            for (int64_t kk = (issued > S ? issued - S : 0); kk < issued; ++kk) {
+                const uint64_t spent = globaltimer_ns() - t0;
+                const uint64_t budget = spent < args.timeout_ns ? args.timeout_ns - spent : 0;
+                if (!mbar_wait_bounded(&full[kk % S], static_cast<uint32_t>((kk / S) & 1), budget,
+                                       nullptr)) {
+                    raise_qk_status(RN_STATUS_WAIT_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---- consumer warps ----
+    const int sub = lane % LPH;
+    const int grp = lane / LPH;
+    uint32_t wq1[A2], wq2[A2], wq3[B2], wk1[A2], wk2[A2], wk3[B2];
+    load_words<A>(a.wq + sub * A, wq1);
+    load_words<A>(a.wq + H2 + sub * A, wq2);
+    load_words<A>(a.wk + sub * A, wk1);
+    load_words<A>(a.wk + H2 + sub * A, wk2);
+    if constexpr (B > 0) {
+        load_words<B>(a.wq + R + sub * B, wq3);
+        load_words<B>(a.wk + R + sub * B, wk3);
+    }
+
+    for (int64_t k = 0; k < n_units; ++k) {
+        const int s = static_cast<int>(k % S);
+        const uint32_t par = static_cast<uint32_t>((k / S) & 1);
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait_bounded(&full[s], par, args.timeout_ns, abort_flag));
+        if (!ok) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                raise_qk_status(RN_STATUS_WAIT_TIMEOUT);
+            }
+            break;
+        }
+        int64_t r0;
+        int rows;
+        sched.unit(bid, k, &r0, &rows);
+        const uint8_t *st = ring + static_cast<size_t>(s) * stage_bytes;
+        const float *cs_base =
+            reinterpret_cast<const float *>(st + static_cast<size_t>(TPS) * tok_bytes);
+        const int heads = rows * H;
+        const int quads = (heads + HPW - 1) / HPW;
+        for (int q = static_cast<int>((warp + k) % NW); q < quads; q += NW) {
+            const uint32_t hh = static_cast<uint32_t>(q * HPW + grp);
+            const bool act = hh < static_cast<uint32_t>(heads);
+            const uint32_t ts =
+                act ? static_cast<uint32_t>((static_cast<uint64_t>(hh) * args.inv_h) >> 32) : 0u;
+            const uint32_t h = act ? hh - ts * H : 0u;
+            const bool good = act && valid[s * TPS + ts] != 0;
+            const uint16_t *xs =
+                reinterpret_cast<const uint16_t *>(st + ts * tok_bytes) + static_cast<size_t>(h) * D;
+            uint32_t x1[A2], x2[A2], x3[B2];
+            load_words<A>(xs + sub * A, x1);
+            load_words<A>(xs + H2 + sub * A, x2);
+            if constexpr (B > 0) load_words<B>(xs + R + sub * B, x3);
+            const float *cs = cs_base + ts * R;
+            float c[A], sn[A];
+            load_f32_smem<A>(cs + sub * A, c);
+            load_f32_smem<A>(cs + H2 + sub * A, sn);
+
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < A2; ++i) {
+                const float2 u = bf2f(x1[i]);
+                const float2 v = bf2f(x2[i]);
+                acc = __ffma2_rn(u, u, acc);
+                acc = __ffma2_rn(v, v, acc);
+            }
+            if constexpr (B > 0) {
+#pragma unroll
+                for (int i = 0; i < B2; ++i) {
+                    const float2 u = bf2f(x3[i]);
+                    acc = __ffma2_rn(u, u, acc);
+                }
+            }
+            const float ss = group_sum<LPH>(acc.x + acc.y);
+            const float rstd = __frsqrt_rn(ss / static_cast<float>(D) + a.eps);
+            const float2 r2 = make_float2(rstd, rstd);
+            const bool isq = h < static_cast<uint32_t>(Hq);
+            uint32_t o1[A2], o2[A2];
+#pragma unroll
+            for (int i = 0; i < A2; ++i) {
+                const float2 n1 = __fmul2_rn(__fmul2_rn(bf2f(x1[i]), r2), bf2f(isq ? wq1[i] : wk1[i]));
+                const float2 n2 = __fmul2_rn(__fmul2_rn(bf2f(x2[i]), r2), bf2f(isq ? wq2[i] : wk2[i]));
+                const float2 cc = make_float2(c[2 * i], c[2 * i + 1]);
+                const float2 sv = make_float2(sn[2 * i], sn[2 * i + 1]);
+                const float2 nsv = make_float2(-sn[2 * i], -sn[2 * i + 1]);
+                o1[i] = pack_f2(__ffma2_rn(n1, cc, __fmul2_rn(n2, nsv)));
+                o2[i] = pack_f2(__ffma2_rn(n2, cc, __fmul2_rn(n1, sv)));
+            }
+            if (good) {
+                uint16_t *head = a.qkv + (r0 + ts) * W + static_cast<int64_t>(h) * D;
+                store_words<A>(head + sub * A, o1);
+                store_words<A>(head + H2 + sub * A, o2);
+                if constexpr (B > 0) {
+                    uint32_t o3[B2];
+#pragma unroll
+                    for (int i = 0; i < B2; ++i)
+                        o3[i] = pack_f2(
+                            __fmul2_rn(__fmul2_rn(bf2f(x3[i]), r2), bf2f(isq ? wq3[i] : wk3[i])));
+                    store_words<B>(head + R + sub * B, o3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
 // ---- table builder ----------------------------------------------------------------
 
 // fp64 angle and trig, rounded once to fp32.
@@ -264,18 +603,59 @@ static int launch_qk_lph(const QkArgs &a, int lph, bool persistent, cudaStream_t
     return RN_ERR_SHAPE;
 }
 
-// Heads-per-warp schedule by token count: one head per warp for 1-2
-// tokens, two through 256 tokens, four (persistent grid) beyond.
+template <int D, int R>
+static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &dev,
+                          uint64_t timeout_ns, int debug_flags) {
+    static std::atomic<int> attr_done[kMaxDevices];
+    const int H = a.Hq + a.Hkv;
+    const int tok_bytes = H * D * 2;
+    const int cs_bytes = R * 4;
+    int tps = 32768 / (tok_bytes + cs_bytes);
+    if (tps < 1) tps = 1;
+    if (tps > 32) tps = 32;
+    // Consumers hold a stage while they compute, so four stages keep about
+    // three in flight.
+    int stages = 4;
+    const int forced = (debug_flags >> 8) & 0x1F;
+    if (forced >= 2) stages = forced;
+    const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
+    const size_t smem = qk_bulk_smem_bytes(stages, tps, tok_bytes, cs_bytes);
+    if (smem > static_cast<size_t>(smem_cap)) return RN_ERR_SHAPE;
+    const int dev_idx = current_device_index();
+    if (dev_idx < 0 || dev_idx >= kMaxDevices) return RN_ERR_DEVICE;
+    if (!attr_done[dev_idx].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(qk_persistent_bulk_kernel<D, R>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_cap) != cudaSuccess) {
+            cudaGetLastError();
+            return RN_ERR_DEVICE;
+        }
+        attr_done[dev_idx].store(1, std::memory_order_release);
+    }
+    int64_t grid = dev.sm_count;
+    if (grid > a.T) grid = a.T;
+    const uint64_t inv_h = ((1ull << 32) + H - 1) / H;
+    QkBulkArgs b{a, tps, stages, debug_flags & 1, inv_h, timeout_ns ? timeout_ns : 2000000000ull};
+    qk_persistent_bulk_kernel<D, R>
+        <<<static_cast<unsigned>(grid), qk_bulk_consumers<D>() + 32, smem, st>>>(b);
+    return launch_status();
+}
+
+// Schedule by token count (measured on GB300): one head per warp for 1-2
+// tokens, two heads per warp through 256 tokens, four heads per warp on a
+// persistent grid up to 2047 tokens, and the bulk-copy token ring beyond,
+// where its deeper prefetch pays for its longer start-up.
 static int auto_qk_schedule(int64_t T) {
     if (T <= 2) return RN_QK_HEAD_PER_WARP;
     if (T <= 256) return RN_QK_TWO_HEADS;
-    return RN_QK_PERSISTENT;
+    if (T < 2048) return RN_QK_PERSISTENT;
+    return RN_QK_BULK;
 }
 
 static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                        const float *cos_sin, const int64_t *positions, int64_t T, int Hq,
                        int Hkv, int D, int rotary_dim, float eps, int64_t max_pos, int *err,
-                       int schedule, rn_stream_t stream) {
+                       int schedule, uint64_t timeout_ns, int debug_flags, rn_stream_t stream) {
     if (T < 0 || Hq < 0 || Hkv < 0) return RN_ERR_SHAPE;
     if (D != 64 && D != 128 && D != 256) return RN_ERR_SHAPE;
     if (rotary_dim != D && rotary_dim != D / 2 && rotary_dim != D / 4) return RN_ERR_SHAPE;
@@ -288,12 +668,18 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
         return RN_ERR_ALIGN;
     int lph;
     bool persistent = false;
-    if (schedule == RN_QK_AUTO) schedule = auto_qk_schedule(T);
+    const bool automatic = schedule == RN_QK_AUTO;
+    if (automatic) {
+        schedule = auto_qk_schedule(T);
+        // (64, 16) has one element per lane per half: the warp grid serves it
+        if (schedule == RN_QK_BULK && D == 64 && rotary_dim == 16) schedule = RN_QK_PERSISTENT;
+    }
     switch (schedule) {
         case RN_QK_HEAD_PER_WARP: lph = 32; break;
         case RN_QK_TWO_HEADS: lph = 16; break;
         case RN_QK_FOUR_HEADS: lph = 8; break;
         case RN_QK_PERSISTENT: lph = 8; persistent = true; break;
+        case RN_QK_BULK: lph = 8; break;
         default: return RN_ERR_ARG;
     }
     const DeviceInfo *dev = current_device_info();
@@ -302,6 +688,18 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
              eps, max_pos, err};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int r = rotary_dim;
+    if (schedule == RN_QK_BULK) {
+        int rc = RN_ERR_SHAPE;
+#define RN_QK_BULK_GO(D_, R_) \
+    if (D == (D_) && r == (R_)) rc = launch_qk_bulk<D_, R_>(a, st, *dev, timeout_ns, debug_flags);
+        // (64, 16) leaves one element per lane per half: the warp schedules serve it.
+        RN_QK_BULK_GO(64, 64) RN_QK_BULK_GO(64, 32)
+        RN_QK_BULK_GO(128, 128) RN_QK_BULK_GO(128, 64) RN_QK_BULK_GO(128, 32)
+        RN_QK_BULK_GO(256, 256) RN_QK_BULK_GO(256, 128) RN_QK_BULK_GO(256, 64)
+#undef RN_QK_BULK_GO
+        if (rc != RN_ERR_SHAPE || !automatic) return rc;
+        persistent = true;  // a token too wide for the ring: the warp grid serves it
+    }
 #define RN_QK_GO(D_, R_)                                                               \
     if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_>(a, lph, persistent, st, *dev);
     RN_QK_GO(64, 64) RN_QK_GO(64, 32) RN_QK_GO(64, 16)
@@ -309,6 +707,23 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
     RN_QK_GO(256, 256) RN_QK_GO(256, 128) RN_QK_GO(256, 64)
 #undef RN_QK_GO
     return RN_ERR_SHAPE;
+}
+
+int qk_status(unsigned int *out, int clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_qk_status, sizeof v) != cudaSuccess) {
+        cudaGetLastError();
+        return RN_ERR_DEVICE;
+    }
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_qk_status, &zero, sizeof zero) != cudaSuccess) {
+            cudaGetLastError();
+            return RN_ERR_DEVICE;
+        }
+    }
+    *out = v;
+    return RN_OK;
 }
 
 }  // namespace rn
@@ -319,15 +734,15 @@ int qk_norm_rope_fwd(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk, const f
                      const int64_t *positions, int64_t T, int Hq, int Hkv, int D,
                      int rotary_dim, float eps, rn_stream_t stream) {
     return rn::qk_dispatch(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps, 0,
-                           nullptr, RN_QK_AUTO, stream);
+                           nullptr, RN_QK_AUTO, 0, 0, stream);
 }
 
 int qk_norm_rope_fwd_sched(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                            const float *cos_sin, const int64_t *positions, int64_t T, int Hq,
                            int Hkv, int D, int rotary_dim, float eps, int schedule,
-                           rn_stream_t stream) {
+                           uint64_t wait_timeout_ns, int debug_flags, rn_stream_t stream) {
     return rn::qk_dispatch(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps, 0,
-                           nullptr, schedule, stream);
+                           nullptr, schedule, wait_timeout_ns, debug_flags, stream);
 }
 
 int qk_norm_rope_fwd_checked(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
@@ -337,7 +752,7 @@ int qk_norm_rope_fwd_checked(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
     if (max_pos < 1) return RN_ERR_SHAPE;
     if (!d_err_flag && T > 0 && Hq + Hkv > 0) return RN_ERR_NULL;
     return rn::qk_dispatch(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
-                           max_pos, d_err_flag, RN_QK_AUTO, stream);
+                           max_pos, d_err_flag, RN_QK_AUTO, 0, 0, stream);
 }
 
 int qk_norm_rope_select_schedule(int64_t T) {

@@ -167,37 +167,6 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N) {
            static_cast<size_t>(2) * R * 32 * 4 + 16;
 }
 
-// Which rows the k-th unit of CTA b covers.  Units go round-robin: round q
-// gives CTA b rows [q*G*R + b*R, +R), so at any moment the grid streams one
-// contiguous band of memory.  A last, partial round is re-split evenly (rows
-// per CTA ceil(rem / G)) so no CTA is left with a whole extra unit.
-struct UnitSchedule {
-    int64_t full_rounds;  // rounds in which every CTA gets R rows
-    int64_t rem;          // rows left for the final round
-    int64_t last_r;       // rows per CTA in the final round
-    int64_t G;
-    int R;
-
-    __device__ __forceinline__ UnitSchedule(int64_t M, int64_t G_, int R_) : G(G_), R(R_) {
-        full_rounds = M / (G * R);
-        rem = M - full_rounds * G * R;
-        last_r = (rem + G - 1) / G;
-    }
-    __device__ __forceinline__ int64_t units(int64_t b) const {
-        return full_rounds + ((rem > 0 && b * last_r < rem) ? 1 : 0);
-    }
-    __device__ __forceinline__ void unit(int64_t b, int64_t k, int64_t *r0, int *rows) const {
-        if (k < full_rounds) {
-            *r0 = k * G * R + b * R;
-            *rows = R;
-        } else {
-            *r0 = full_rounds * G * R + b * last_r;
-            const int64_t left = rem - b * last_r;
-            *rows = static_cast<int>(left < last_r ? left : last_r);
-        }
-    }
-};
-
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
 template <int VPR, int R, int NT>
 __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const BulkArgs a) {
@@ -549,7 +518,10 @@ int rn_device_status(unsigned int *out, int clear) {
             return RN_ERR_DEVICE;
         }
     }
-    *out = v;
+    unsigned int q = 0;
+    const int rc = rn::qk_status(&q, clear);
+    if (rc != RN_OK) return rc;
+    *out = v | q;
     return RN_OK;
 }
 

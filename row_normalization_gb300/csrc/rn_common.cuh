@@ -153,4 +153,35 @@ __device__ __forceinline__ uint4 ld_shared16(const void *p) {
     return v;
 }
 
+// Which rows (or tokens) the k-th unit of persistent CTA b covers.  Units go round-robin: round q
+// gives CTA b rows [q*G*R + b*R, +R), so at any moment the grid streams one
+// contiguous band of memory.  A last, partial round is re-split evenly (rows
+// per CTA ceil(rem / G)) so no CTA is left with a whole extra unit.
+struct UnitSchedule {
+    int64_t full_rounds;  // rounds in which every CTA gets R rows
+    int64_t rem;          // rows left for the final round
+    int64_t last_r;       // rows per CTA in the final round
+    int64_t G;
+    int R;
+
+    __device__ __forceinline__ UnitSchedule(int64_t M, int64_t G_, int R_) : G(G_), R(R_) {
+        full_rounds = M / (G * R);
+        rem = M - full_rounds * G * R;
+        last_r = (rem + G - 1) / G;
+    }
+    __device__ __forceinline__ int64_t units(int64_t b) const {
+        return full_rounds + ((rem > 0 && b * last_r < rem) ? 1 : 0);
+    }
+    __device__ __forceinline__ void unit(int64_t b, int64_t k, int64_t *r0, int *rows) const {
+        if (k < full_rounds) {
+            *r0 = k * G * R + b * R;
+            *rows = R;
+        } else {
+            *r0 = full_rounds * G * R + b * last_r;
+            const int64_t left = rem - b * last_r;
+            *rows = static_cast<int>(left < last_r ? left : last_r);
+        }
+    }
+};
+
 }  // namespace rn

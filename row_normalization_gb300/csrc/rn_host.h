@@ -54,6 +54,9 @@ inline int current_device_index() {
     return dev;
 }
 
+// Reads (and optionally clears) the status word of the QK translation unit.
+int qk_status(unsigned int *out, int clear);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int launch_status() {

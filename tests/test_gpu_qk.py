@@ -22,7 +22,7 @@ from tests.parity import assert_parity
 pytestmark = pytest.mark.gpu
 
 QK_SCHEDULES = [binding.RN_QK_AUTO, binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_TWO_HEADS,
-                binding.RN_QK_FOUR_HEADS, binding.RN_QK_PERSISTENT]
+                binding.RN_QK_FOUR_HEADS, binding.RN_QK_PERSISTENT, binding.RN_QK_BULK]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -31,7 +31,7 @@ def _gpu():
 
 
 def run_case(T, Hq, Hkv, D, r, *, positions="arange", max_pos=None, theta=1e6, eps=1e-6,
-             schedule=binding.RN_QK_AUTO, device_inputs=False, seed=0):
+             schedule=binding.RN_QK_AUTO, device_inputs=False, seed=0, debug_flags=0):
     max_pos = max_pos or max(T, 1)
     qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions=positions, max_pos=max_pos,
                                   device="cuda" if device_inputs else "cpu", seed=seed)
@@ -42,7 +42,7 @@ def run_case(T, Hq, Hkv, D, r, *, positions="arange", max_pos=None, theta=1e6, e
     buf, q = padded_empty(tuple(qkv.shape), torch.bfloat16, pad, 0x7FC3)
     q.copy_(qkv)
     binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(), pos.cuda(),
-                             Hq, Hkv, D, r, eps, schedule=schedule)
+                             Hq, Hkv, D, r, eps, schedule=schedule, debug_flags=debug_flags)
     torch.cuda.synchronize()
     got = bf16_bits(q)
     assert canary_intact(buf, pad, 0x7FC3), "write outside qkv"
@@ -60,17 +60,54 @@ LAYOUTS = [(64, 64), (64, 32), (64, 16), (128, 128), (128, 64), (128, 32),
 @pytest.mark.parametrize("schedule", QK_SCHEDULES)
 @pytest.mark.parametrize("D,r", LAYOUTS)
 def test_layouts_every_schedule(D, r, schedule):
+    if schedule == binding.RN_QK_BULK and (D, r) == (64, 16):
+        # one element per lane per rotary half: only the warp schedules take it
+        with pytest.raises(binding.RowNormError) as ei:
+            run_case(5, 4, 2, D, r, positions="uniform", max_pos=97, schedule=schedule)
+        assert ei.value.code == binding.RN_ERR_SHAPE
+        return
     got, want = run_case(5, 4, 2, D, r, positions="uniform", max_pos=97, schedule=schedule,
                          seed=D + r)
     assert_parity(got, want, f"D={D} r={r} sched={schedule}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (1, 0), (0, 2), (7, 3), (1, 1)])
-@pytest.mark.parametrize("T", [1, 2, 3, 33])
-def test_head_counts_ragged(T, Hq, Hkv):
+@pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_BULK])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (1, 0), (0, 2), (7, 3), (1, 1), (64, 0)])
+@pytest.mark.parametrize("T", [1, 2, 3, 33, 1000])
+def test_head_counts_ragged(T, Hq, Hkv, schedule):
     got, want = run_case(T, Hq, Hkv, 128, 128, positions="uniform", max_pos=4096,
-                         seed=T * 100 + Hq)
-    assert_parity(got, want, f"T={T} Hq={Hq} Hkv={Hkv}")
+                         seed=T * 100 + Hq, schedule=schedule)
+    assert_parity(got, want, f"T={T} Hq={Hq} Hkv={Hkv} sched={schedule}")
+
+
+@pytest.mark.parametrize("D,r", [lr for lr in LAYOUTS if lr != (64, 16)])
+def test_bulk_ring_many_units_every_layout(D, r):
+    # thousands of tokens: every CTA wraps its two-stage ring many times and the
+    # last round is split unevenly
+    got, want = run_case(3001, 8, 2, D, r, positions="uniform", max_pos=9000,
+                         schedule=binding.RN_QK_BULK, seed=D * 3 + r)
+    assert_parity(got, want, f"bulk D={D} r={r}")
+    for stages in (2, 3, 6):
+        got, want = run_case(777, 8, 2, D, r, positions="uniform", max_pos=9000,
+                             schedule=binding.RN_QK_BULK, seed=stages, debug_flags=stages << 8)
+        assert_parity(got, want, f"bulk D={D} r={r} stages={stages}")
+
+
+def test_bulk_wait_timeout_reports_status_and_context_survives():
+    # The bulk schedule is told never to issue its copies: its bounded waits
+    # run out (2 ms), the status word records it, and the context stays usable.
+    binding.device_status(clear=True)
+    qkv, wq, wk, pos = qkv_inputs(4, 4, 2, 128, positions="arange", seed=9)
+    table = torch.from_numpy(oracle_table(1e6, 8, 128)).cuda()
+    q = qkv.cuda()
+    binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), table, pos.cuda(), 4, 2, 128, 128, 1e-6,
+                             schedule=binding.RN_QK_BULK, wait_timeout_ns=2_000_000,
+                             debug_flags=1)
+    assert binding.device_status(clear=True) & binding.RN_STATUS_WAIT_TIMEOUT
+    got, want = run_case(4, 4, 2, 128, 128, positions="arange", schedule=binding.RN_QK_BULK,
+                         seed=9)
+    assert_parity(got, want, "after timeout")
+    assert binding.device_status(clear=True) == 0
 
 
 @pytest.mark.parametrize("T", [1, 2, 16, 64, 256])
@@ -99,14 +136,18 @@ def test_schedules_agree_at_scale():
     assert np.array_equal(a, b)  # same lane layout and arithmetic: bit-identical
 
 
-def test_checked_positions_skip_bad_tokens():
-    T, Hq, Hkv, D, r = 9, 4, 2, 128, 128
+@pytest.mark.parametrize("T", [9, 3000])
+def test_checked_positions_skip_bad_tokens(T):
+    Hq, Hkv, D, r = 4, 2, 128, 128
     max_pos = 64
     qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions="uniform", max_pos=max_pos, seed=11)
-    bad = [1, 4, 8]
+    bad = [1, 4, 8] + ([1500, 2999] if T > 9 else [])
     pos[1] = -1
     pos[4] = max_pos
     pos[8] = max_pos + 1000
+    if T > 9:
+        pos[1500] = -(1 << 40)
+        pos[2999] = 1 << 40
     table = oracle_table(1e6, max_pos, r)
     good_pos = pos.clone()
     good_pos[bad] = 0
