@@ -326,6 +326,33 @@ __device__ __forceinline__ uint32_t pack_f2(float2 v) { return pack_bf2(v.x, v.y
 template <int D>
 constexpr int qk_bulk_consumers() { return D >= 256 ? 256 : 512; }
 
+// Normalise + rotate one head's lane slice with the given weights (packed
+// bf16): o = rotate(x * rstd * w), tail = x * rstd * w.  fp32 pairs.
+template <int A2, int B2, bool TAIL>
+__device__ __forceinline__ void qk_rotate_slice(const uint32_t (&x1)[A2], const uint32_t (&x2)[A2],
+                                                const uint32_t (&x3)[B2], const uint32_t (&w1)[A2],
+                                                const uint32_t (&w2)[A2], const uint32_t (&w3)[B2],
+                                                const float (&c)[2 * A2],
+                                                const float (&sn)[2 * A2], float rstd,
+                                                uint32_t (&o1)[A2], uint32_t (&o2)[A2],
+                                                uint32_t (&o3)[B2]) {
+    const float2 r2 = make_float2(rstd, rstd);
+#pragma unroll
+    for (int i = 0; i < A2; ++i) {
+        const float2 n1 = __fmul2_rn(__fmul2_rn(bf2f(x1[i]), r2), bf2f(w1[i]));
+        const float2 n2 = __fmul2_rn(__fmul2_rn(bf2f(x2[i]), r2), bf2f(w2[i]));
+        const float2 cc = make_float2(c[2 * i], c[2 * i + 1]);
+        const float2 sv = make_float2(sn[2 * i], sn[2 * i + 1]);
+        const float2 nsv = make_float2(-sn[2 * i], -sn[2 * i + 1]);
+        o1[i] = pack_f2(__ffma2_rn(n1, cc, __fmul2_rn(n2, nsv)));
+        o2[i] = pack_f2(__ffma2_rn(n2, cc, __fmul2_rn(n1, sv)));
+    }
+    if constexpr (TAIL) {
+#pragma unroll
+        for (int i = 0; i < B2; ++i) o3[i] = pack_f2(__fmul2_rn(__fmul2_rn(bf2f(x3[i]), r2), bf2f(w3[i])));
+    }
+}
+
 template <int D, int R>
 __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
     qk_persistent_bulk_kernel(const QkBulkArgs args) {
@@ -515,32 +542,32 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
                 }
             }
             const float ss = group_sum<LPH>(acc.x + acc.y);
-            const float rstd = __frsqrt_rn(ss / static_cast<float>(D) + a.eps);
-            const float2 r2 = make_float2(rstd, rstd);
+            // D is a power of two: multiplying by 1/D is the exact division.
+            const float rstd = __frsqrt_rn(ss * (1.0f / static_cast<float>(D)) + a.eps);
             const bool isq = h < static_cast<uint32_t>(Hq);
-            uint32_t o1[A2], o2[A2];
+            uint32_t o1[A2], o2[A2], o3[B2];
+            // The quad's heads are usually all query or all key heads: pick the
+            // weights once for the warp instead of element by element.
+            if (__all_sync(0xffffffffu, isq || !act)) {
+                qk_rotate_slice<A2, B2, (B > 0)>(x1, x2, x3, wq1, wq2, wq3, c, sn, rstd, o1, o2, o3);
+            } else if (__all_sync(0xffffffffu, !isq || !act)) {
+                qk_rotate_slice<A2, B2, (B > 0)>(x1, x2, x3, wk1, wk2, wk3, c, sn, rstd, o1, o2, o3);
+            } else {
+                uint32_t w1[A2], w2[A2], w3[B2];
 #pragma unroll
-            for (int i = 0; i < A2; ++i) {
-                const float2 n1 = __fmul2_rn(__fmul2_rn(bf2f(x1[i]), r2), bf2f(isq ? wq1[i] : wk1[i]));
-                const float2 n2 = __fmul2_rn(__fmul2_rn(bf2f(x2[i]), r2), bf2f(isq ? wq2[i] : wk2[i]));
-                const float2 cc = make_float2(c[2 * i], c[2 * i + 1]);
-                const float2 sv = make_float2(sn[2 * i], sn[2 * i + 1]);
-                const float2 nsv = make_float2(-sn[2 * i], -sn[2 * i + 1]);
-                o1[i] = pack_f2(__ffma2_rn(n1, cc, __fmul2_rn(n2, nsv)));
-                o2[i] = pack_f2(__ffma2_rn(n2, cc, __fmul2_rn(n1, sv)));
+                for (int i = 0; i < A2; ++i) {
+                    w1[i] = isq ? wq1[i] : wk1[i];
+                    w2[i] = isq ? wq2[i] : wk2[i];
+                }
+#pragma unroll
+                for (int i = 0; i < B2; ++i) w3[i] = isq ? wq3[i] : wk3[i];
+                qk_rotate_slice<A2, B2, (B > 0)>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
             }
             if (good) {
                 uint16_t *head = a.qkv + (r0 + ts) * W + static_cast<int64_t>(h) * D;
                 store_words<A>(head + sub * A, o1);
                 store_words<A>(head + H2 + sub * A, o2);
-                if constexpr (B > 0) {
-                    uint32_t o3[B2];
-#pragma unroll
-                    for (int i = 0; i < B2; ++i)
-                        o3[i] = pack_f2(
-                            __fmul2_rn(__fmul2_rn(bf2f(x3[i]), r2), bf2f(isq ? wq3[i] : wk3[i])));
-                    store_words<B>(head + R + sub * B, o3);
-                }
+                if constexpr (B > 0) store_words<B>(head + R + sub * B, o3);
             }
         }
         __syncwarp();
