@@ -108,9 +108,9 @@ enum {
  * returns.  `debug_flags` is 0 in normal use.  Tests and tuning set:
  *   bit 0      the persistent schedule never issues its copies, so its
  *              waits run out (exercises the timeout path);
- *   bits 4-7   persistent schedule: CTAs per SM (0 = 1);
+ *   bits 4-7   persistent schedule: CTAs per SM (0 = the tuned value);
  *   bits 8-12  persistent schedule: ring stages, capped by shared memory
- *              (0 = as many as fit, at most 16). */
+ *              (0 = the tuned value). */
 int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps,
                       int64_t M, int64_t N, rn_bf16 *y, int schedule,
                       uint64_t wait_timeout_ns, int debug_flags,
@@ -143,7 +143,8 @@ int rmsnorm_select_schedule(int64_t M, int64_t N);
  *              position outside the table reads outside cos_sin).  Use
  *              qk_norm_rope_fwd_checked for untrusted positions.
  *   Requirements: T >= 0, Hq >= 0, Hkv >= 0; D in {64, 128, 256};
- *   rotary_dim in {D, D/2, D/4}; all pointers 16-byte aligned.
+ *   rotary_dim in {D, D/2, D/4}; T * (Hq + Hkv) < 2^31; qkv, wq, wk and
+ *   cos_sin 16-byte aligned, positions 8-byte aligned.
  * The schedule (1, 2 or 4 heads per warp; persistent grid for large T) is
  * chosen from T.  Errors: RN_ERR_NULL, RN_ERR_ALIGN, RN_ERR_SHAPE,
  * RN_ERR_DEVICE, RN_ERR_LAUNCH. */

@@ -690,8 +690,9 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
         return RN_ERR_SHAPE;
     if (T == 0 || Hq + Hkv == 0) return RN_OK;
     if (!qkv || !wq || !wk || !cos_sin || !positions) return RN_ERR_NULL;
+    // positions are read one int64 at a time: 8-byte alignment suffices
     if (!aligned16(qkv) || !aligned16(wq) || !aligned16(wk) || !aligned16(cos_sin) ||
-        !aligned16(positions))
+        (reinterpret_cast<uintptr_t>(positions) & 7u) != 0)
         return RN_ERR_ALIGN;
     int lph;
     bool persistent = false;

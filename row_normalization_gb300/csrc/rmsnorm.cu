@@ -373,23 +373,27 @@ static int launch_cta_rows(const uint16_t *x, const uint16_t *w, float eps, int6
 
 // Chooses (consumer threads, chunks per thread per row, rows per stage) for
 // the persistent schedule; false when N does not fit it.
-// Geometry of the persistent schedule per row width, measured on GB300:
-// NT consumer threads x VPR 16-byte chunks cover one row exactly, R rows make
-// a stage, and two stages in flight per SM (32-64 KiB each) stream best --
-// deeper rings measured slower (more concurrent DRAM streams, no more
-// bandwidth).
+// Geometry of the persistent schedule, measured on GB300: NT consumer threads
+// x VPR 16-byte chunks cover one row exactly, R rows make a stage, `stages`
+// stages per CTA, `ctas` co-resident CTAs per SM.  Two stages in flight per
+// CTA stream best; deeper rings measured slower (more concurrent DRAM streams,
+// no more bandwidth).  Up to M = 8192 rows the 4096-wide rows run two CTAs
+// per SM with 32 KiB stages: more independent pipelines shorten the ramp that
+// dominates such short launches (measured inside the bench step; for 8192-wide
+// rows the second CTA measured slower).  Larger M runs one CTA per SM.
 struct BulkGeometry {
-    int nt, vpr, R, stages;
+    int nt, vpr, R, stages, ctas;
 };
 
-static bool bulk_geometry(int N, BulkGeometry *g) {
+static bool bulk_geometry(int64_t M, int N, BulkGeometry *g) {
+    const bool few_rows = M <= 8192;
     switch (N) {
-        case 1024: *g = {128, 1, 8, 2}; break;
-        case 2048: *g = {256, 1, 8, 2}; break;
-        case 4096: *g = {256, 2, 8, 2}; break;
-        case 8192: *g = {256, 4, 2, 2}; break;
-        case 16384: *g = {512, 4, 1, 2}; break;
-        case 32768: *g = {512, 8, 1, 2}; break;
+        case 1024: *g = {128, 1, 8, 2, 1}; break;
+        case 2048: *g = {256, 1, 8, 2, 1}; break;
+        case 4096: *g = few_rows ? BulkGeometry{256, 2, 4, 2, 2} : BulkGeometry{256, 2, 8, 2, 1}; break;
+        case 8192: *g = {256, 4, 2, 2, 1}; break;
+        case 16384: *g = {512, 4, 1, 2, 1}; break;
+        case 32768: *g = {512, 8, 1, 2, 1}; break;
         default: return false;
     }
     return true;
@@ -418,7 +422,7 @@ static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float ep
                                   int N, uint16_t *y, cudaStream_t st, const DeviceInfo &dev,
                                   uint64_t timeout_ns, int debug_flags) {
     BulkGeometry geo;
-    if (!bulk_geometry(N, &geo)) return RN_ERR_SHAPE;
+    if (!bulk_geometry(M, N, &geo)) return RN_ERR_SHAPE;
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
     const size_t stage_cost = static_cast<size_t>(geo.R) * N * 2 + 16;
     int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N)) / stage_cost);
@@ -427,7 +431,7 @@ static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float ep
     const int forced_stages = (debug_flags >> 8) & 0x1F;
     if (forced_stages > 0) stages = forced_stages;
     int ctas_per_sm = (debug_flags >> 4) & 0xF;
-    if (ctas_per_sm <= 0) ctas_per_sm = 1;
+    if (ctas_per_sm <= 0) ctas_per_sm = geo.ctas;
     if (stages * ctas_per_sm > max_stages) stages = max_stages / ctas_per_sm;
     if (stages < 2) return RN_ERR_SHAPE;
     const size_t smem = bulk_smem_bytes(stages, geo.R, N);
@@ -439,7 +443,9 @@ static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float ep
     switch (N) {
         case 1024: return launch_bulk_inst<1, 8, 128>(a, g, smem, smem_cap, st);
         case 2048: return launch_bulk_inst<1, 8, 256>(a, g, smem, smem_cap, st);
-        case 4096: return launch_bulk_inst<2, 8, 256>(a, g, smem, smem_cap, st);
+        case 4096:
+            return geo.R == 4 ? launch_bulk_inst<2, 4, 256>(a, g, smem, smem_cap, st)
+                              : launch_bulk_inst<2, 8, 256>(a, g, smem, smem_cap, st);
         case 8192: return launch_bulk_inst<4, 2, 256>(a, g, smem, smem_cap, st);
         case 16384: return launch_bulk_inst<4, 1, 512>(a, g, smem, smem_cap, st);
         case 32768: return launch_bulk_inst<8, 1, 512>(a, g, smem, smem_cap, st);
@@ -450,7 +456,7 @@ static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float ep
 static int auto_schedule(int64_t M, int N, const DeviceInfo &dev) {
     BulkGeometry geo;
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    if (bulk_geometry(N, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
+    if (bulk_geometry(M, N, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
     return RN_SCHED_CTA_ROW;
 }

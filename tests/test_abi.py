@@ -94,7 +94,8 @@ def test_qk_shape_checks(lib, T, Hq, Hkv, D, r, expect):
 
 def test_qk_null_alignment_and_checked_args(lib):
     assert lib.qk_norm_rope_fwd(P, P, None, P, P, 4, 2, 1, 128, 128, 1e-6, None) == binding.RN_ERR_NULL
-    assert lib.qk_norm_rope_fwd(P, P, P, P, MISALIGNED, 4, 2, 1, 128, 128, 1e-6, None) == binding.RN_ERR_ALIGN
+    assert lib.qk_norm_rope_fwd(P, P, P, P, P + 4, 4, 2, 1, 128, 128, 1e-6, None) == binding.RN_ERR_ALIGN
+    assert lib.qk_norm_rope_fwd(P, P, P, MISALIGNED, P, 4, 2, 1, 128, 128, 1e-6, None) == binding.RN_ERR_ALIGN
     assert lib.qk_norm_rope_fwd_checked(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 0, P, None) == binding.RN_ERR_SHAPE
     assert lib.qk_norm_rope_fwd_checked(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 16, None, None) == binding.RN_ERR_NULL
     assert lib.qk_norm_rope_fwd_sched(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 3, 0, 0, None) == binding.RN_ERR_ARG

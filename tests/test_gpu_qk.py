@@ -190,3 +190,19 @@ def test_table_builder_matches_oracle(theta, max_pos, r):
     ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
     assert np.all(np.abs(got - ref) <= ulp + 1e-10)
     assert np.mean(got == ref) > 0.999
+
+
+@pytest.mark.parametrize("schedule", [binding.RN_QK_FOUR_HEADS, binding.RN_QK_BULK])
+def test_positions_view_at_8_byte_offset(schedule):
+    # positions only need 8-byte alignment: a view one int64 into a buffer works
+    T, Hq, Hkv, D, r = 2049, 4, 2, 128, 64
+    qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions="uniform", max_pos=500, seed=21)
+    table = oracle_table(1e6, 500, r)
+    want = oracle.qk_norm_rope(bf16_bits(qkv[1:]), bf16_bits(wq), bf16_bits(wk), table,
+                               pos[1:].numpy(), Hq, Hkv, D, r, 1e-6)
+    q = qkv[1:].cuda()
+    pos_view = pos.cuda()[1:]
+    assert pos_view.data_ptr() % 16 == 8
+    binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(), pos_view,
+                             Hq, Hkv, D, r, 1e-6, schedule=schedule)
+    assert_parity(bf16_bits(q), want, f"offset positions sched={schedule}")
