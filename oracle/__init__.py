@@ -13,6 +13,8 @@ Passages followed:
   * RMSNorm -- "[Inductor] Codegen Gluon", section 3.1.
   * fused Q/K RMSNorm + neox RoPE -- "[pretuned] Optimize fused_qk_norm_rope
     on B200", section "Summary".
+  * fused residual add + RMSNorm -- "TorchInductor: from ATen IR to Triton
+    kernel", sections 14.3 and 14.27.
   * LayerNorm -- "TorchInductor: from ATen IR to Triton kernel", section
     14.12.2.
 """
@@ -83,6 +85,9 @@ def _load():
             u16p, u16p, u16p, f32p, i64p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float]
         lib.rn_oracle_qk_norm_rope.restype = ctypes.c_int
+        lib.rn_oracle_add_rmsnorm.argtypes = [u16p, u16p, u16p, ctypes.c_float, ctypes.c_int64,
+                                              ctypes.c_int64, u16p, u16p]
+        lib.rn_oracle_add_rmsnorm.restype = ctypes.c_int
         lib.rn_oracle_layernorm.argtypes = [u16p, u16p, u16p, ctypes.c_float,
                                             ctypes.c_int64, ctypes.c_int64, u16p]
         lib.rn_oracle_layernorm.restype = ctypes.c_int
@@ -176,6 +181,23 @@ def qk_norm_rope(qkv: np.ndarray, wq: np.ndarray, wk: np.ndarray,
         _ptr(cos_sin, ctypes.c_float), _ptr(positions, ctypes.c_int64),
         cos_sin.shape[0], T, Hq, Hkv, D, rotary_dim, ctypes.c_float(eps)), "qk_norm_rope")
     return out
+
+
+def add_rmsnorm(x: np.ndarray, res: np.ndarray, w: np.ndarray, eps: float):
+    """(h, y): h = bf16(x + res), y = rmsnorm(h) row by row."""
+    x = _u16(x)
+    res = _u16(res)
+    w = _u16(w)
+    if x.shape != res.shape or x.ndim != 2 or w.shape != (x.shape[1],):
+        raise ValueError("x and res must be [M, N] and w [N]")
+    M, N = x.shape
+    h = np.zeros_like(x)
+    y = np.zeros_like(x)
+    _check(_load().rn_oracle_add_rmsnorm(_ptr(x, ctypes.c_uint16), _ptr(res, ctypes.c_uint16),
+                                         _ptr(w, ctypes.c_uint16), ctypes.c_float(eps), M, N,
+                                         _ptr(h, ctypes.c_uint16), _ptr(y, ctypes.c_uint16)),
+           "add_rmsnorm")
+    return h, y
 
 
 def layernorm(x: np.ndarray, w: np.ndarray, b: np.ndarray | None, eps: float) -> np.ndarray:

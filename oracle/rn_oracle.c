@@ -16,6 +16,8 @@
  *     "Summary" (norm over the whole head, Q/K weights, RoPE, one store per
  *     half; partial rotary still normalises the non-rotary tail).
  *   - The rotary cos/sin table used as an input by the above.
+ *   - Fused residual add + RMSNorm: "TorchInductor: from ATen IR to Triton
+ *     kernel", sections 14.3 and 14.27.
  *   - LayerNorm (mean and biased variance, then affine): "TorchInductor: from
  *     ATen IR to Triton kernel", section 14.12.2, and "[Inductor] Codegen
  *     Gluon", section 3.2.
@@ -214,6 +216,28 @@ int rn_oracle_qk_norm_rope(uint16_t *qkv, const uint16_t *wq,
         }
     }
     return bad ? -3 : 0;
+}
+
+/* ---- fused residual add + RMSNorm ---------------------------------------- */
+
+/* h[r, j] = bf16(x[r, j] + res[r, j])   (the exact sum, rounded once)
+ * y[r, :] = rmsnorm(h[r, :]) with the rounded h, exactly as the unfused pair
+ * "add, then RMSNorm" would give: fusing the two ops removes HBM round trips
+ * and changes nothing else ("TorchInductor: from ATen IR to Triton kernel",
+ * sections 14.3 and 14.27: the norm / residual-add chain fused into one
+ * kernel). */
+int rn_oracle_add_rmsnorm(const uint16_t *x, const uint16_t *res, const uint16_t *w,
+                          float eps, int64_t M, int64_t N, uint16_t *h, uint16_t *y)
+{
+    if (M < 0 || N <= 0) return -3;
+    if (M == 0) return 0;
+    if (!x || !res || !w || !h || !y) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t j = 0; j < N; ++j)
+            h[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) +
+                                                    rn_oracle_bf16_to_double(res[r * N + j]));
+    }
+    return rn_oracle_rmsnorm(h, w, eps, M, N, y);
 }
 
 /* ---- LayerNorm ---------------------------------------------------------- */

@@ -493,3 +493,55 @@ def test_layernorm_exact_brute_force_and_numpy():
     got = oracle.layernorm(x, w, None, 1e-5)
     mism = np.count_nonzero(got != want)
     assert mism == 0
+
+
+# ---------------------------------------------------------------------------
+# fused residual add + RMSNorm
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("row", _parse_golden("add_rmsnorm_hand.txt"), ids=lambda r: r[0])
+def test_add_rmsnorm_hand_worked(row):
+    _, eps, xs, rs, ws, hs, ys = row
+    x = bf([float(v) for v in xs.split()])[None, :]
+    r = bf([float(v) for v in rs.split()])[None, :]
+    w = bf([float(v) for v in ws.split()])
+    h, y = oracle.add_rmsnorm(x, r, w, float(eps))
+    assert [hex(v) for v in h[0]] == [hex(int(t, 16)) for t in hs.split()]
+    assert [hex(v) for v in y[0]] == [hex(int(t, 16)) for t in ys.split()]
+
+
+def test_add_rmsnorm_sum_is_the_correctly_rounded_sum():
+    # h must be the single rounding of the exact sum: compare with exact
+    # rationals, and with torch's bf16 addition (library routine).
+    rng = np.random.default_rng(71)
+    x = rand_bf16(rng, (16, 64), scale=3.0)
+    r = rand_bf16(rng, (16, 64), scale=0.01)
+    r[:, :8] = (x[:, :8] ^ 0x8000)               # exact cancellation
+    r[:, 8:16] = rand_bf16(rng, (16, 8), scale=1e-6)  # far smaller addend
+    w = rand_bf16(rng, (64,))
+    h, _ = oracle.add_rmsnorm(x, r, w, 1e-6)
+    for i in range(16):
+        for j in range(64):
+            assert h[i, j] == round_bf16(bits_to_fraction(x[i, j]) + bits_to_fraction(r[i, j]))
+    tx = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    tr = torch.from_numpy(r.view(np.int16)).view(torch.bfloat16)
+    th = (tx + tr).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(np.where(bits_to_f64(h) == 0, 0, h), np.where(bits_to_f64(th) == 0, 0, th))
+
+
+def test_add_rmsnorm_is_the_composition():
+    # The fused op changes nothing: y equals RMSNorm of the rounded sum, bit for
+    # bit, on random rows (which also catches a y taken from the unrounded sum).
+    rng = np.random.default_rng(73)
+    x = rand_bf16(rng, (32, 257 * 8))
+    r = rand_bf16(rng, (32, 257 * 8), scale=0.5)
+    w = rand_bf16(rng, (257 * 8,))
+    h, y = oracle.add_rmsnorm(x, r, w, 1e-6)
+    assert np.array_equal(y, oracle.rmsnorm(h, w, 1e-6))
+    # and y is NOT what the unrounded sum would give on at least some elements
+    xf, rf, wf = bits_to_f64(x), bits_to_f64(r), bits_to_f64(w)
+    s = xf + rf
+    unrounded = s / np.sqrt((s * s).mean(-1, keepdims=True) + np.float64(np.float32(1e-6))) * wf
+    yu = np.array([[round_bf16(Fraction(float(v))) for v in row] for row in unrounded[:4]],
+                  dtype=np.uint16)
+    assert np.count_nonzero(yu != y[:4]) > 0
