@@ -43,6 +43,7 @@ METRIC = "achieved HBM GB/s and % of GB300 peak for bf16 RMSNorm / QK-norm+RoPE"
 SPEC_GBS = 7928.0
 
 RMS_SHAPES = [(M, N) for M in (4096, 8192, 16384, 32768) for N in (4096, 8192, 16384)]
+ADD_SHAPES: list = []   # fused residual add + RMSNorm: only with --only add:MxN
 RMS_EPS = 1e-6
 QK_T = 16384
 QK_ROT = (128, 64)
@@ -65,15 +66,22 @@ def qk_bytes(T: int, r: int) -> int:
     return T * (2 * (HQ + HKV) * D * 2 + r * 4 + 8) + 2 * D * 2
 
 
+def add_bytes(M: int, N: int) -> int:
+    """Ideal bytes of the fused residual add: read x and r, write h and y, w once."""
+    return 8 * M * N + 2 * N
+
+
 def step_bytes() -> int:
-    return sum(rms_bytes(M, N) for M, N in RMS_SHAPES) + sum(qk_bytes(QK_T, r) for r in QK_ROT)
+    return (sum(rms_bytes(M, N) for M, N in RMS_SHAPES) + sum(qk_bytes(QK_T, r) for r in QK_ROT)
+            + sum(add_bytes(M, N) for M, N in ADD_SHAPES))
 
 
 def restrict_workload(spec: str) -> None:
-    """--only: keep a subset of the step, e.g. "rms:8192x16384,qk:16384:128".
-    Used for profiling one launch; the printed line names the reduced workload."""
-    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD
-    rms, rot = [], []
+    """--only: keep a subset of the step, e.g. "rms:8192x16384,qk:16384:128",
+    or measure the fused residual add with "add:8192x8192".  Used for
+    profiling one launch; the printed line names the reduced workload."""
+    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD, ADD_SHAPES
+    rms, rot, add = [], [], []
     for item in spec.split(","):
         kind, _, rest = item.partition(":")
         if kind == "rms":
@@ -83,9 +91,12 @@ def restrict_workload(spec: str) -> None:
             T, r = rest.split(":")
             QK_T = int(T)
             rot.append(int(r))
+        elif kind == "add":
+            M, N = rest.split("x")
+            add.append((int(M), int(N)))
         else:
             raise SystemExit(f"bad --only item {item!r}")
-    RMS_SHAPES, QK_ROT = rms, tuple(rot)
+    RMS_SHAPES, QK_ROT, ADD_SHAPES = rms, tuple(rot), add
     WORKLOAD = "subset: " + spec
 
 
@@ -212,6 +223,11 @@ def build_inputs(torch, binding, inputs, device):
         x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=100 * i)
         y = torch.empty_like(x)
         rms.append({"M": M, "N": N, "x": x, "w": w, "y": y})
+    for i, (M, N) in enumerate(ADD_SHAPES):
+        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=500 + i)
+        r, _ = inputs.rmsnorm_inputs(M, N, device=device, seed=550 + i)
+        rms.append({"M": M, "N": N, "x": x, "w": w, "y": torch.empty_like(x), "r": r,
+                    "h": torch.empty_like(x)})
     qk = []
     for j, r in enumerate(QK_ROT):
         qkv, wq, wk, pos = inputs.qkv_inputs(QK_T, HQ, HKV, D, positions="uniform",
@@ -231,7 +247,11 @@ def launch_step(binding, rms, qk, events=None):
         if events is not None:
             events[k].record()
         k += 1
-        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
+        if "r" in c:
+            binding.add_rmsnorm_fwd(c["x"], c["r"], c["w"], RMS_EPS, c["h"], c["y"],
+                                    schedule=FORCE["rms"])
+        else:
+            binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
     for c in qk:
         if events is not None:
             events[k].record()
@@ -307,9 +327,11 @@ def run_ours(args) -> int:
 
     per_shape = []
     for k, c in enumerate(rms):
-        sched = FORCE["rms"] or binding.rmsnorm_select_schedule(c["M"], c["N"])
-        b = rms_bytes(c["M"], c["N"])
-        per_shape.append({"op": "rmsnorm", "M": c["M"], "N": c["N"],
+        fused = "r" in c
+        sched = FORCE["rms"] or (binding.add_rmsnorm_select_schedule if fused
+                                 else binding.rmsnorm_select_schedule)(c["M"], c["N"])
+        b = add_bytes(c["M"], c["N"]) if fused else rms_bytes(c["M"], c["N"])
+        per_shape.append({"op": "add_rmsnorm" if fused else "rmsnorm", "M": c["M"], "N": c["N"],
                           "kernel": RMS_KERNELS.get(sched, str(sched)),
                           "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
                           "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
@@ -324,7 +346,7 @@ def run_ours(args) -> int:
     for p in per_shape:
         p["frac_of_measured"] = round(p["gbs"] / hbm_peak, 4)
     dom = max(per_shape, key=lambda p: p["us"])
-    dom_wl = (f"rmsnorm M={dom['M']} N={dom['N']}" if dom["op"] == "rmsnorm"
+    dom_wl = (f"{dom['op']} M={dom['M']} N={dom['N']}" if dom["op"] != "qk_norm_rope"
               else f"qk_norm_rope T={dom['T']} r={dom['rotary_dim']}")
     achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -333,12 +355,13 @@ def run_ours(args) -> int:
                 "kernel": dom["kernel"], "launch": dom_wl,
                 "algorithmic_bytes_per_launch": dom["bytes"]}
 
-    e2e = run_e2e(torch, binding, rms, qk, args, dist, device) if args.e2e_steps > 0 else None
+    e2e = (run_e2e(torch, binding, rms, qk, args, dist, device)
+           if args.e2e_steps > 0 and not ADD_SHAPES else None)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(budget_s=args.cpu_seconds)
 
-    rms_ms = sum(per_launch_ms[:len(rms)])
+    rms_ms = sum(per_launch_ms[:len(RMS_SHAPES)])
     qk_ms = sum(per_launch_ms[len(rms):])
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,

@@ -15,6 +15,9 @@
  *                     weight and the rotation, store each half once; partial
  *                     rotary still normalises the non-rotary tail.
  *   rope_cos_sin_table  builds the cos/sin table the rotary step reads.
+ *   add_rmsnorm_fwd   h = x + residual (written out) and y = rmsnorm(h), one
+ *                     kernel: the norm / residual-add chain fused ("TorchInductor:
+ *                     from ATen IR to Triton kernel", sections 14.3 and 14.27).
  *
  * Conventions shared by every entry point
  *   - bf16 tensors are passed as pointers to their raw 16-bit patterns
@@ -120,6 +123,35 @@ int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps,
  * current device; RN_ERR_SHAPE / RN_ERR_DEVICE as rmsnorm_fwd would return.
  * Host-only query: launches nothing. */
 int rmsnorm_select_schedule(int64_t M, int64_t N);
+
+/* Fused residual add + RMSNorm, one pass:
+ *   h[r, j] = bf16(x[r, j] + residual[r, j])   (the exact sum rounded once)
+ *   y[r, :] = bf16( h[r, :] * 1/sqrt(sum_j h[r, j]^2 / N + eps) * w[:] )
+ * y is computed from the rounded h, so the result is exactly that of the two
+ * unfused operations; fusing saves the HBM round trip of h.
+ *   x, residual  [M, N] bf16, each read once.
+ *   h_out        [M, N] bf16 output; may be `residual` itself (in-place
+ *                residual update) or `x`.
+ *   y            [M, N] bf16 output; may be `x` itself.  Must differ from h_out.
+ * Outputs may equal an input pointer exactly but must not partially overlap
+ * one.  Requirements and errors as rmsnorm_fwd; h_out == y gives RN_ERR_ARG.
+ * The persistent schedule streams x and residual rows through its ring
+ * (N a power of two, 1024 <= N <= 16384); 32768-wide rows use a row schedule. */
+int add_rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *residual, const rn_bf16 *w,
+                    float eps, int64_t M, int64_t N, rn_bf16 *h_out, rn_bf16 *y,
+                    rn_stream_t stream);
+
+/* The schedule (RN_SCHED_*) add_rmsnorm_fwd launches for (M, N) on the
+ * current device.  Host-only query: launches nothing. */
+int add_rmsnorm_select_schedule(int64_t M, int64_t N);
+
+/* add_rmsnorm_fwd with an explicit schedule, wait limit and test flags, as
+ * rmsnorm_fwd_sched. */
+int add_rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *residual,
+                          const rn_bf16 *w, float eps, int64_t M, int64_t N,
+                          rn_bf16 *h_out, rn_bf16 *y, int schedule,
+                          uint64_t wait_timeout_ns, int debug_flags,
+                          rn_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Fused Q/K RMSNorm + neox RoPE                                              */

@@ -82,6 +82,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qk_norm_rope_fwd_checked.restype = i32
         L.rope_cos_sin_table.argtypes = [f64, i64, i32, vp, vp]
         L.rope_cos_sin_table.restype = i32
+        L.add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
+        L.add_rmsnorm_fwd.restype = i32
+        L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
+        L.add_rmsnorm_fwd_sched.restype = i32
+        L.add_rmsnorm_select_schedule.argtypes = [i64, i64]
+        L.add_rmsnorm_select_schedule.restype = i32
         L.rmsnorm_select_schedule.argtypes = [i64, i64]
         L.rmsnorm_select_schedule.restype = i32
         L.qk_norm_rope_select_schedule.argtypes = [i64]
@@ -149,6 +155,36 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
                                  schedule, wait_timeout_ns, debug_flags, _stream(stream))
     _check(rc, "rmsnorm_fwd")
     return y
+
+
+def add_rmsnorm_fwd(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: float,
+                    h: torch.Tensor | None = None, y: torch.Tensor | None = None, *,
+                    schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0,
+                    debug_flags: int = 0, stream=None):
+    """h = x + residual (bf16), y = rmsnorm(h); returns (h, y).  Pass
+    h=residual for an in-place residual update."""
+    _need(x, "x", torch.bfloat16)
+    _need(residual, "residual", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    if x.dim() != 2 or residual.shape != x.shape or w.dim() != 1 or w.shape[0] != x.shape[1]:
+        raise ValueError("x and residual must be [M, N] and w [N]")
+    h = torch.empty_like(x) if h is None else h
+    y = torch.empty_like(x) if y is None else y
+    _need(h, "h", torch.bfloat16)
+    _need(y, "y", torch.bfloat16)
+    if h.shape != x.shape or y.shape != x.shape:
+        raise ValueError("h and y must have x's shape")
+    M, N = x.shape
+    L = load()
+    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+        rc = L.add_rmsnorm_fwd(x.data_ptr(), residual.data_ptr(), w.data_ptr(), eps, M, N,
+                               h.data_ptr(), y.data_ptr(), _stream(stream))
+    else:
+        rc = L.add_rmsnorm_fwd_sched(x.data_ptr(), residual.data_ptr(), w.data_ptr(), eps, M, N,
+                                     h.data_ptr(), y.data_ptr(), schedule, wait_timeout_ns,
+                                     debug_flags, _stream(stream))
+    _check(rc, "add_rmsnorm_fwd")
+    return h, y
 
 
 def _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim):
@@ -228,6 +264,14 @@ def rmsnorm_select_schedule(M: int, N: int) -> int:
     rc = int(load().rmsnorm_select_schedule(int(M), int(N)))
     if rc < 0:
         raise RowNormError("rmsnorm_select_schedule", rc)
+    return rc
+
+
+def add_rmsnorm_select_schedule(M: int, N: int) -> int:
+    """The RN_SCHED_* schedule add_rmsnorm_fwd picks for (M, N) on the current device."""
+    rc = int(load().add_rmsnorm_select_schedule(int(M), int(N)))
+    if rc < 0:
+        raise RowNormError("add_rmsnorm_select_schedule", rc)
     return rc
 
 

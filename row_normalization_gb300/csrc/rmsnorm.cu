@@ -50,6 +50,19 @@ __device__ __forceinline__ uint4 scale8(uint4 xv, uint4 wv, float rstd) {
     return o;
 }
 
+// h = bf16(x + r) for 8 packed elements.  Each sum of two bf16 is formed in
+// fp32 and rounded once: either the fp32 sum is exact (exponents within 16 of
+// each other) or the smaller addend is below 2^-16 of the larger, too small to
+// reach a bf16 rounding midpoint.  So h is the correctly rounded exact sum.
+__device__ __forceinline__ uint4 add8(uint4 a, uint4 b) {
+    uint4 o;
+    o.x = pack_bf2(bf_lo(a.x) + bf_lo(b.x), bf_hi(a.x) + bf_hi(b.x));
+    o.y = pack_bf2(bf_lo(a.y) + bf_lo(b.y), bf_hi(a.y) + bf_hi(b.y));
+    o.z = pack_bf2(bf_lo(a.z) + bf_lo(b.z), bf_hi(a.z) + bf_hi(b.z));
+    o.w = pack_bf2(bf_lo(a.w) + bf_lo(b.w), bf_hi(a.w) + bf_hi(b.w));
+    return o;
+}
+
 __device__ __forceinline__ float row_rstd(float ss, int N, float eps) {
     return __frsqrt_rn(ss / static_cast<float>(N) + eps);
 }
@@ -57,11 +70,13 @@ __device__ __forceinline__ float row_rstd(float ss, int N, float eps) {
 // ---------------------------------------------------------------------------
 // warp_rows: one warp per row; lane l holds 16-byte chunks l, l+32, ...
 // ---------------------------------------------------------------------------
-template <int VPT>
-__global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *__restrict__ x,
+// With ADD, the row is h = bf16(x + r) (stored to h_out) and y = rmsnorm(h).
+template <int VPT, bool ADD>
+__global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
-                                                            uint16_t *__restrict__ y) {
+                                                            uint16_t *y, const uint16_t *r,
+                                                            uint16_t *h_out) {
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int cpr = N >> 3;
@@ -73,6 +88,16 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *__re
         for (int i = 0; i < VPT; ++i) {
             const int c = lane + 32 * i;
             v[i] = (c < cpr) ? ld_stream16(xr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if constexpr (ADD) {
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = lane + 32 * i;
+                if (c < cpr) {
+                    v[i] = add8(v[i], ld_stream16(r + row * N + 8 * c));
+                    st16(h_out + row * N + 8 * c, v[i]);
+                }
+            }
         }
         float ss = 0.f;
 #pragma unroll
@@ -91,11 +116,12 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *__re
 // ---------------------------------------------------------------------------
 // cta_rows: one CTA per row; thread t holds chunks t, t+nt, ...
 // ---------------------------------------------------------------------------
-template <int VPT, int MAXT>
-__global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *__restrict__ x,
+template <int VPT, int MAXT, bool ADD>
+__global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
-                                                            uint16_t *__restrict__ y) {
+                                                            uint16_t *y, const uint16_t *r,
+                                                            uint16_t *h_out) {
     __shared__ float red[2][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -109,6 +135,16 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *__re
         for (int i = 0; i < VPT; ++i) {
             const int c = tid + nt * i;
             v[i] = (c < cpr) ? ld_stream16(xr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if constexpr (ADD) {
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = tid + nt * i;
+                if (c < cpr) {
+                    v[i] = add8(v[i], ld_stream16(r + row * N + 8 * c));
+                    st16(h_out + row * N + 8 * c, v[i]);
+                }
+            }
         }
         float ss = 0.f;
 #pragma unroll
@@ -152,6 +188,8 @@ struct BulkArgs {
     const uint16_t *x;
     const uint16_t *w;
     uint16_t *y;
+    const uint16_t *r;  // residual (fused add) or nullptr
+    uint16_t *h;        // x + r output (fused add) or nullptr
     int64_t M;
     int N;
     float eps;
@@ -160,21 +198,24 @@ struct BulkArgs {
     uint64_t timeout_ns;
 };
 
-// Shared memory: [stages x R rows of x][full mbarriers][empty mbarriers]
-//                [partial sums 2 x R x 32 floats][flags: 4 ints]
-__host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N) {
-    return static_cast<size_t>(stages) * R * N * 2 + static_cast<size_t>(stages) * 16 +
+// Shared memory: [stages x (R rows of x [+ R rows of r])][full mbarriers]
+//                [empty mbarriers][partial sums 2 x R x 32 floats][flags: 4 ints]
+// `nin` is the number of row inputs streamed through the ring (1, or 2 with
+// the fused residual add).
+__host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1) {
+    return static_cast<size_t>(stages) * nin * R * N * 2 + static_cast<size_t>(stages) * 16 +
            static_cast<size_t>(2) * R * 32 * 4 + 16;
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
-template <int VPR, int R, int NT>
+template <int VPR, int R, int NT, bool ADD>
 __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const BulkArgs a) {
+    constexpr int NIN = ADD ? 2 : 1;
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = a.stages;
     const int N = a.N;
     const uint32_t row_bytes = static_cast<uint32_t>(N) * 2u;
-    const uint32_t stage_bytes = row_bytes * R;
+    const uint32_t stage_bytes = row_bytes * R * NIN;  // x rows, then r rows
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage_bytes);
     uint64_t *empty = full + S;
@@ -223,10 +264,13 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
                 int rows;
                 sched.unit(bid, k, &r0, &rows);
                 const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
-                mbar_arrive_expect_tx(&full[s], bytes);
-                if (!(a.debug & 1))
-                    bulk_copy_g2s(ring + static_cast<size_t>(s) * stage_bytes, a.x + r0 * N, bytes,
-                                  &full[s], pol);
+                mbar_arrive_expect_tx(&full[s], bytes * NIN);
+                if (!(a.debug & 1)) {
+                    uint8_t *dst = ring + static_cast<size_t>(s) * stage_bytes;
+                    bulk_copy_g2s(dst, a.x + r0 * N, bytes, &full[s], pol);
+                    if constexpr (ADD)
+                        bulk_copy_g2s(dst + row_bytes * R, a.r + r0 * N, bytes, &full[s], pol);
+                }
             }
             // Drain: every copy issued into this CTA's ring lands before the
             // CTA may exit.  The last use of each stage is among the last S.
@@ -273,6 +317,24 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
             for (int j = 0; j < VPR; ++j)
                 xv[rr][j] = ok ? ld_shared16(st + rr * row_bytes + 16u * (tid + j * NT))
                                : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (ADD) {
+            // h = x + r, stored at once; the rest of the row works on h
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr)
+#pragma unroll
+                for (int j = 0; j < VPR; ++j)
+                    xv[rr][j] = add8(xv[rr][j],
+                                     ok ? ld_shared16(st + (R + rr) * row_bytes + 16u * (tid + j * NT))
+                                        : make_uint4(0u, 0u, 0u, 0u));
+            if (ok) {
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr)
+                    if (rr < rows)
+#pragma unroll
+                        for (int j = 0; j < VPR; ++j)
+                            st16(a.h + (r0 + rr) * N + 8 * (tid + j * NT), xv[rr][j]);
+            }
+        }
         __syncwarp();
         if (lane == 0) {
             if (ok) {
@@ -324,55 +386,71 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 // host side
 // ---------------------------------------------------------------------------
 
-static int launch_warp_rows(const uint16_t *x, const uint16_t *w, float eps, int64_t M, int N,
-                            uint16_t *y, cudaStream_t st, const DeviceInfo &dev) {
-    const int cpr = N >> 3;
+// Everything one launch needs; r and h are set only for the fused residual add.
+struct RowJob {
+    const uint16_t *x;
+    const uint16_t *w;
+    float eps;
+    int64_t M;
+    int N;
+    uint16_t *y;
+    const uint16_t *r;
+    uint16_t *h;
+};
+
+template <bool ADD>
+static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &dev) {
+    const int cpr = j.N >> 3;
     const int wpb = 8;
-    const int64_t want = (M + wpb - 1) / wpb;
+    const int64_t want = (j.M + wpb - 1) / wpb;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 64;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+#define RN_WARP(V) \
+    rms_warp_rows_kernel<V, ADD><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, j.h)
     if (cpr <= 32)
-        rms_warp_rows_kernel<1><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+        RN_WARP(1);
     else if (cpr <= 64)
-        rms_warp_rows_kernel<2><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+        RN_WARP(2);
     else if (cpr <= 128)
-        rms_warp_rows_kernel<4><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+        RN_WARP(4);
     else if (cpr <= 256)
-        rms_warp_rows_kernel<8><<<grid, 32 * wpb, 0, st>>>(x, w, eps, M, N, y);
+        RN_WARP(8);
     else
         return RN_ERR_SHAPE;
+#undef RN_WARP
     return launch_status();
 }
 
-static int launch_cta_rows(const uint16_t *x, const uint16_t *w, float eps, int64_t M, int N,
-                           uint16_t *y, cudaStream_t st, const DeviceInfo &dev) {
-    const int cpr = N >> 3;
+template <bool ADD>
+static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &dev) {
+    const int cpr = j.N >> 3;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 2048;
-    const unsigned grid = static_cast<unsigned>(M < cap ? M : cap);
+    const unsigned grid = static_cast<unsigned>(j.M < cap ? j.M : cap);
     // Threads: enough 16-byte chunks per thread to keep several loads in
     // flight, at most 1024 threads.
     auto nthreads = [&](int vpt) {
         int t = (cpr + vpt - 1) / vpt;
         return ((t + 31) / 32) * 32;
     };
-    if (cpr <= 512) {
-        rms_cta_rows_kernel<1, 512><<<grid, nthreads(1), 0, st>>>(x, w, eps, M, N, y);
-    } else if (cpr <= 1024) {
-        rms_cta_rows_kernel<2, 512><<<grid, nthreads(2), 0, st>>>(x, w, eps, M, N, y);
-    } else if (cpr <= 2048) {
-        rms_cta_rows_kernel<4, 512><<<grid, nthreads(4), 0, st>>>(x, w, eps, M, N, y);
-    } else if (cpr <= 4096) {
-        rms_cta_rows_kernel<8, 512><<<grid, nthreads(8), 0, st>>>(x, w, eps, M, N, y);
-    } else if (cpr <= 8192) {
-        rms_cta_rows_kernel<8, 1024><<<grid, nthreads(8), 0, st>>>(x, w, eps, M, N, y);
-    } else {
+#define RN_CTA(V, T)                                                                      \
+    rms_cta_rows_kernel<V, T, ADD><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
+                                                                 j.y, j.r, j.h)
+    if (cpr <= 512)
+        RN_CTA(1, 512);
+    else if (cpr <= 1024)
+        RN_CTA(2, 512);
+    else if (cpr <= 2048)
+        RN_CTA(4, 512);
+    else if (cpr <= 4096)
+        RN_CTA(8, 512);
+    else if (cpr <= 8192)
+        RN_CTA(8, 1024);
+    else
         return RN_ERR_SHAPE;
-    }
+#undef RN_CTA
     return launch_status();
 }
 
-// Chooses (consumer threads, chunks per thread per row, rows per stage) for
-// the persistent schedule; false when N does not fit it.
 // Geometry of the persistent schedule, measured on GB300: NT consumer threads
 // x VPR 16-byte chunks cover one row exactly, R rows make a stage, `stages`
 // stages per CTA, `ctas` co-resident CTAs per SM.  Two stages in flight per
@@ -380,13 +458,27 @@ static int launch_cta_rows(const uint16_t *x, const uint16_t *w, float eps, int6
 // no more bandwidth).  Up to M = 8192 rows the 4096-wide rows run two CTAs
 // per SM with 32 KiB stages: more independent pipelines shorten the ramp that
 // dominates such short launches (measured inside the bench step; for 8192-wide
-// rows the second CTA measured slower).  Larger M runs one CTA per SM.
+// rows the second CTA measured slower).  Larger M runs one CTA per SM.  With
+// the fused residual add a stage carries R rows of x and R rows of r, so R is
+// halved where needed to keep a stage at 64 KiB or less; 32768-wide rows do
+// not fit two such stages and take the CTA-per-row schedule.
 struct BulkGeometry {
     int nt, vpr, R, stages, ctas;
 };
 
-static bool bulk_geometry(int64_t M, int N, BulkGeometry *g) {
+static bool bulk_geometry(int64_t M, int N, bool add, BulkGeometry *g) {
     const bool few_rows = M <= 8192;
+    if (add) {
+        switch (N) {
+            case 1024: *g = {128, 1, 8, 2, 1}; break;
+            case 2048: *g = {256, 1, 8, 2, 1}; break;
+            case 4096: *g = {256, 2, 4, 2, 1}; break;
+            case 8192: *g = {256, 4, 2, 2, 1}; break;
+            case 16384: *g = {512, 4, 1, 2, 1}; break;
+            default: return false;
+        }
+        return true;
+    }
     switch (N) {
         case 1024: *g = {128, 1, 8, 2, 1}; break;
         case 2048: *g = {256, 1, 8, 2, 1}; break;
@@ -399,14 +491,14 @@ static bool bulk_geometry(int64_t M, int N, BulkGeometry *g) {
     return true;
 }
 
-template <int VPR, int R, int NT>
+template <int VPR, int R, int NT, bool ADD>
 static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_cap,
                             cudaStream_t st) {
     static std::atomic<int> attr_done[kMaxDevices];
     const int dev = current_device_index();
     if (dev < 0 || dev >= kMaxDevices) return RN_ERR_DEVICE;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<VPR, R, NT>,
+        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<VPR, R, NT, ADD>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_cap) != cudaSuccess) {
             cudaGetLastError();
@@ -414,18 +506,20 @@ static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_c
         }
         attr_done[dev].store(1, std::memory_order_release);
     }
-    rms_persistent_bulk_kernel<VPR, R, NT><<<grid, NT + 32, smem, st>>>(a);
+    rms_persistent_bulk_kernel<VPR, R, NT, ADD><<<grid, NT + 32, smem, st>>>(a);
     return launch_status();
 }
 
-static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float eps, int64_t M,
-                                  int N, uint16_t *y, cudaStream_t st, const DeviceInfo &dev,
+template <bool ADD>
+static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const DeviceInfo &dev,
                                   uint64_t timeout_ns, int debug_flags) {
+    constexpr int NIN = ADD ? 2 : 1;
     BulkGeometry geo;
-    if (!bulk_geometry(M, N, &geo)) return RN_ERR_SHAPE;
+    const int N = j.N;
+    if (!bulk_geometry(j.M, N, ADD, &geo)) return RN_ERR_SHAPE;
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
-    const size_t stage_cost = static_cast<size_t>(geo.R) * N * 2 + 16;
-    int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N)) / stage_cost);
+    const size_t stage_cost = static_cast<size_t>(NIN) * geo.R * N * 2 + 16;
+    int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N, NIN)) / stage_cost);
     if (max_stages > 16) max_stages = 16;
     int stages = geo.stages;
     const int forced_stages = (debug_flags >> 8) & 0x1F;
@@ -434,53 +528,81 @@ static int launch_persistent_bulk(const uint16_t *x, const uint16_t *w, float ep
     if (ctas_per_sm <= 0) ctas_per_sm = geo.ctas;
     if (stages * ctas_per_sm > max_stages) stages = max_stages / ctas_per_sm;
     if (stages < 2) return RN_ERR_SHAPE;
-    const size_t smem = bulk_smem_bytes(stages, geo.R, N);
+    const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN);
     int64_t grid = static_cast<int64_t>(dev.sm_count) * ctas_per_sm;
-    if (grid > M) grid = M;
-    BulkArgs a{x, w, y, M, N, eps, stages, debug_flags & 1,
+    if (grid > j.M) grid = j.M;
+    BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.M, N, j.eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
     const int g = static_cast<int>(grid);
     switch (N) {
-        case 1024: return launch_bulk_inst<1, 8, 128>(a, g, smem, smem_cap, st);
-        case 2048: return launch_bulk_inst<1, 8, 256>(a, g, smem, smem_cap, st);
+        case 1024: return launch_bulk_inst<1, 8, 128, ADD>(a, g, smem, smem_cap, st);
+        case 2048: return launch_bulk_inst<1, 8, 256, ADD>(a, g, smem, smem_cap, st);
         case 4096:
-            return geo.R == 4 ? launch_bulk_inst<2, 4, 256>(a, g, smem, smem_cap, st)
-                              : launch_bulk_inst<2, 8, 256>(a, g, smem, smem_cap, st);
-        case 8192: return launch_bulk_inst<4, 2, 256>(a, g, smem, smem_cap, st);
-        case 16384: return launch_bulk_inst<4, 1, 512>(a, g, smem, smem_cap, st);
-        case 32768: return launch_bulk_inst<8, 1, 512>(a, g, smem, smem_cap, st);
+            return geo.R == 4 ? launch_bulk_inst<2, 4, 256, ADD>(a, g, smem, smem_cap, st)
+                              : launch_bulk_inst<2, 8, 256, ADD>(a, g, smem, smem_cap, st);
+        case 8192: return launch_bulk_inst<4, 2, 256, ADD>(a, g, smem, smem_cap, st);
+        case 16384: return launch_bulk_inst<4, 1, 512, ADD>(a, g, smem, smem_cap, st);
+        case 32768:
+            if constexpr (!ADD) return launch_bulk_inst<8, 1, 512, ADD>(a, g, smem, smem_cap, st);
+            break;
     }
     return RN_ERR_SHAPE;
 }
 
-static int auto_schedule(int64_t M, int N, const DeviceInfo &dev) {
+static int auto_schedule(int64_t M, int N, bool add, const DeviceInfo &dev) {
     BulkGeometry geo;
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    if (bulk_geometry(M, N, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
+    if (bulk_geometry(M, N, add, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
     return RN_SCHED_CTA_ROW;
+}
+
+static int check_rows(int64_t M, int64_t N) {
+    if (M < 0 || N < 8 || N > 65536 || (N % 8) != 0) return RN_ERR_SHAPE;
+    return RN_OK;
+}
+
+template <bool ADD>
+static int rows_dispatch(const RowJob &j, int schedule, uint64_t timeout_ns, int debug_flags,
+                         rn_stream_t stream) {
+    if (schedule < RN_SCHED_AUTO || schedule > RN_SCHED_PERSIST_BULK) return RN_ERR_ARG;
+    const DeviceInfo *dev = current_device_info();
+    if (!dev) return RN_ERR_DEVICE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, *dev);
+    switch (schedule) {
+        case RN_SCHED_WARP_ROW: return launch_warp_rows<ADD>(j, st, *dev);
+        case RN_SCHED_CTA_ROW: return launch_cta_rows<ADD>(j, st, *dev);
+        case RN_SCHED_PERSIST_BULK:
+            return launch_persistent_bulk<ADD>(j, st, *dev, timeout_ns, debug_flags);
+    }
+    return RN_ERR_ARG;
 }
 
 static int rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N,
                             rn_bf16 *y, int schedule, uint64_t timeout_ns, int debug_flags,
                             rn_stream_t stream) {
-    if (M < 0 || N < 8 || N > 65536 || (N % 8) != 0) return RN_ERR_SHAPE;
+    const int rc = check_rows(M, N);
+    if (rc != RN_OK) return rc;
     if (M == 0) return RN_OK;
     if (!x || !w || !y) return RN_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return RN_ERR_ALIGN;
-    if (schedule < RN_SCHED_AUTO || schedule > RN_SCHED_PERSIST_BULK) return RN_ERR_ARG;
-    const DeviceInfo *dev = current_device_info();
-    if (!dev) return RN_ERR_DEVICE;
-    const int n = static_cast<int>(N);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(M, n, *dev);
-    switch (schedule) {
-        case RN_SCHED_WARP_ROW: return launch_warp_rows(x, w, eps, M, n, y, st, *dev);
-        case RN_SCHED_CTA_ROW: return launch_cta_rows(x, w, eps, M, n, y, st, *dev);
-        case RN_SCHED_PERSIST_BULK:
-            return launch_persistent_bulk(x, w, eps, M, n, y, st, *dev, timeout_ns, debug_flags);
-    }
-    return RN_ERR_ARG;
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr};
+    return rows_dispatch<false>(j, schedule, timeout_ns, debug_flags, stream);
+}
+
+static int add_rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *res, const rn_bf16 *w, float eps,
+                                int64_t M, int64_t N, rn_bf16 *h, rn_bf16 *y, int schedule,
+                                uint64_t timeout_ns, int debug_flags, rn_stream_t stream) {
+    const int rc = check_rows(M, N);
+    if (rc != RN_OK) return rc;
+    if (M == 0) return RN_OK;
+    if (!x || !res || !w || !h || !y) return RN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(res) || !aligned16(w) || !aligned16(h) || !aligned16(y))
+        return RN_ERR_ALIGN;
+    if (h == y) return RN_ERR_ARG;  // two different outputs
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, res, h};
+    return rows_dispatch<true>(j, schedule, timeout_ns, debug_flags, stream);
 }
 
 }  // namespace rn
@@ -500,10 +622,31 @@ int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, 
 }
 
 int rmsnorm_select_schedule(int64_t M, int64_t N) {
-    if (M < 0 || N < 8 || N > 65536 || (N % 8) != 0) return RN_ERR_SHAPE;
+    if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
     const rn::DeviceInfo *dev = rn::current_device_info();
     if (!dev) return RN_ERR_DEVICE;
-    return rn::auto_schedule(M, static_cast<int>(N), *dev);
+    return rn::auto_schedule(M, static_cast<int>(N), false, *dev);
+}
+
+int add_rmsnorm_select_schedule(int64_t M, int64_t N) {
+    if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
+    const rn::DeviceInfo *dev = rn::current_device_info();
+    if (!dev) return RN_ERR_DEVICE;
+    return rn::auto_schedule(M, static_cast<int>(N), true, *dev);
+}
+
+int add_rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *residual, const rn_bf16 *w, float eps,
+                    int64_t M, int64_t N, rn_bf16 *h_out, rn_bf16 *y, rn_stream_t stream) {
+    return rn::add_rmsnorm_dispatch(x, residual, w, eps, M, N, h_out, y, RN_SCHED_AUTO, 0, 0,
+                                    stream);
+}
+
+int add_rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *residual, const rn_bf16 *w,
+                          float eps, int64_t M, int64_t N, rn_bf16 *h_out, rn_bf16 *y,
+                          int schedule, uint64_t wait_timeout_ns, int debug_flags,
+                          rn_stream_t stream) {
+    return rn::add_rmsnorm_dispatch(x, residual, w, eps, M, N, h_out, y, schedule,
+                                    wait_timeout_ns, debug_flags, stream);
 }
 
 int rn_device_status(unsigned int *out, int clear) {

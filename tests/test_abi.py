@@ -32,7 +32,7 @@ def declared_functions() -> list[str]:
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ("rmsnorm_fwd", "qk_norm_rope_fwd", "qk_norm_rope_fwd_checked",
+    for required in ("rmsnorm_fwd", "add_rmsnorm_fwd", "qk_norm_rope_fwd", "qk_norm_rope_fwd_checked",
                      "rope_cos_sin_table", "rn_error_string", "rn_device_status"):
         assert required in names
 
@@ -99,6 +99,14 @@ def test_qk_null_alignment_and_checked_args(lib):
     assert lib.qk_norm_rope_fwd_checked(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 0, P, None) == binding.RN_ERR_SHAPE
     assert lib.qk_norm_rope_fwd_checked(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 16, None, None) == binding.RN_ERR_NULL
     assert lib.qk_norm_rope_fwd_sched(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 3, 0, 0, None) == binding.RN_ERR_ARG
+
+
+def test_add_rmsnorm_checks(lib):
+    assert lib.add_rmsnorm_fwd(P, P, P, 1e-6, 4, 7, P, P + 4096, None) == binding.RN_ERR_SHAPE
+    assert lib.add_rmsnorm_fwd(P, P, P, 1e-6, 0, 64, P, P + 4096, None) == binding.RN_OK
+    assert lib.add_rmsnorm_fwd(P, None, P, 1e-6, 4, 64, P, P + 4096, None) == binding.RN_ERR_NULL
+    assert lib.add_rmsnorm_fwd(P, P, P, 1e-6, 4, 64, MISALIGNED, P + 4096, None) == binding.RN_ERR_ALIGN
+    assert lib.add_rmsnorm_fwd(P, P, P, 1e-6, 4, 64, P + 4096, P + 4096, None) == binding.RN_ERR_ARG
 
 
 def test_table_checks(lib):
