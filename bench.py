@@ -44,6 +44,7 @@ SPEC_GBS = 7928.0
 
 RMS_SHAPES = [(M, N) for M in (4096, 8192, 16384, 32768) for N in (4096, 8192, 16384)]
 ADD_SHAPES: list = []   # fused residual add + RMSNorm: only with --only add:MxN
+LN_SHAPES: list = []    # LayerNorm (with bias): only with --only ln:MxN
 RMS_EPS = 1e-6
 QK_T = 16384
 QK_ROT = (128, 64)
@@ -71,17 +72,23 @@ def add_bytes(M: int, N: int) -> int:
     return 8 * M * N + 2 * N
 
 
+def ln_bytes(M: int, N: int) -> int:
+    """Ideal bytes of LayerNorm: read x, write y, w and b once."""
+    return 4 * M * N + 4 * N
+
+
 def step_bytes() -> int:
     return (sum(rms_bytes(M, N) for M, N in RMS_SHAPES) + sum(qk_bytes(QK_T, r) for r in QK_ROT)
-            + sum(add_bytes(M, N) for M, N in ADD_SHAPES))
+            + sum(add_bytes(M, N) for M, N in ADD_SHAPES)
+            + sum(ln_bytes(M, N) for M, N in LN_SHAPES))
 
 
 def restrict_workload(spec: str) -> None:
     """--only: keep a subset of the step, e.g. "rms:8192x16384,qk:16384:128",
     or measure the fused residual add with "add:8192x8192".  Used for
     profiling one launch; the printed line names the reduced workload."""
-    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD, ADD_SHAPES
-    rms, rot, add = [], [], []
+    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD, ADD_SHAPES, LN_SHAPES
+    rms, rot, add, ln = [], [], [], []
     for item in spec.split(","):
         kind, _, rest = item.partition(":")
         if kind == "rms":
@@ -94,9 +101,12 @@ def restrict_workload(spec: str) -> None:
         elif kind == "add":
             M, N = rest.split("x")
             add.append((int(M), int(N)))
+        elif kind == "ln":
+            M, N = rest.split("x")
+            ln.append((int(M), int(N)))
         else:
             raise SystemExit(f"bad --only item {item!r}")
-    RMS_SHAPES, QK_ROT, ADD_SHAPES = rms, tuple(rot), add
+    RMS_SHAPES, QK_ROT, ADD_SHAPES, LN_SHAPES = rms, tuple(rot), add, ln
     WORKLOAD = "subset: " + spec
 
 
@@ -228,6 +238,10 @@ def build_inputs(torch, binding, inputs, device):
         r, _ = inputs.rmsnorm_inputs(M, N, device=device, seed=550 + i)
         rms.append({"M": M, "N": N, "x": x, "w": w, "y": torch.empty_like(x), "r": r,
                     "h": torch.empty_like(x)})
+    for i, (M, N) in enumerate(LN_SHAPES):
+        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=700 + i)
+        rms.append({"M": M, "N": N, "x": x, "w": w, "y": torch.empty_like(x),
+                    "b": inputs.norm_bias(N, device=device, seed=750 + i)})
     qk = []
     for j, r in enumerate(QK_ROT):
         qkv, wq, wk, pos = inputs.qkv_inputs(QK_T, HQ, HKV, D, positions="uniform",
@@ -250,6 +264,8 @@ def launch_step(binding, rms, qk, events=None):
         if "r" in c:
             binding.add_rmsnorm_fwd(c["x"], c["r"], c["w"], RMS_EPS, c["h"], c["y"],
                                     schedule=FORCE["rms"])
+        elif "b" in c:
+            binding.layernorm_fwd(c["x"], c["w"], c["b"], 1e-5, c["y"], schedule=FORCE["rms"])
         else:
             binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
     for c in qk:
@@ -327,11 +343,13 @@ def run_ours(args) -> int:
 
     per_shape = []
     for k, c in enumerate(rms):
-        fused = "r" in c
-        sched = FORCE["rms"] or (binding.add_rmsnorm_select_schedule if fused
-                                 else binding.rmsnorm_select_schedule)(c["M"], c["N"])
-        b = add_bytes(c["M"], c["N"]) if fused else rms_bytes(c["M"], c["N"])
-        per_shape.append({"op": "add_rmsnorm" if fused else "rmsnorm", "M": c["M"], "N": c["N"],
+        op = "add_rmsnorm" if "r" in c else ("layernorm" if "b" in c else "rmsnorm")
+        select = {"add_rmsnorm": binding.add_rmsnorm_select_schedule,
+                  "layernorm": binding.layernorm_select_schedule,
+                  "rmsnorm": binding.rmsnorm_select_schedule}[op]
+        sched = FORCE["rms"] or select(c["M"], c["N"])
+        b = {"add_rmsnorm": add_bytes, "layernorm": ln_bytes, "rmsnorm": rms_bytes}[op](c["M"], c["N"])
+        per_shape.append({"op": op, "M": c["M"], "N": c["N"],
                           "kernel": RMS_KERNELS.get(sched, str(sched)),
                           "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
                           "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
@@ -356,7 +374,7 @@ def run_ours(args) -> int:
                 "algorithmic_bytes_per_launch": dom["bytes"]}
 
     e2e = (run_e2e(torch, binding, rms, qk, args, dist, device)
-           if args.e2e_steps > 0 and not ADD_SHAPES else None)
+           if args.e2e_steps > 0 and not ADD_SHAPES and not LN_SHAPES else None)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(budget_s=args.cpu_seconds)

@@ -15,6 +15,10 @@
  *                     weight and the rotation, store each half once; partial
  *                     rotary still normalises the non-rotary tail.
  *   rope_cos_sin_table  builds the cos/sin table the rotary step reads.
+ *   layernorm_fwd     y = (x - mean) / sqrt(var + eps) * w + b, row by row
+ *                     (biased variance), the same single HBM pass:
+ *                     "TorchInductor: from ATen IR to Triton kernel", section
+ *                     14.12.2, and "[Inductor] Codegen Gluon", section 3.2.
  *   add_rmsnorm_fwd   h = x + residual (written out) and y = rmsnorm(h), one
  *                     kernel: the norm / residual-add chain fused ("TorchInductor:
  *                     from ATen IR to Triton kernel", sections 14.3 and 14.27).
@@ -123,6 +127,28 @@ int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps,
  * current device; RN_ERR_SHAPE / RN_ERR_DEVICE as rmsnorm_fwd would return.
  * Host-only query: launches nothing. */
 int rmsnorm_select_schedule(int64_t M, int64_t N);
+
+/* LayerNorm, one HBM pass:
+ *   mean_r = sum_j x[r, j] / N,  var_r = sum_j (x[r, j] - mean_r)^2 / N
+ *   y[r, :] = bf16( (x[r, :] - mean_r) * 1/sqrt(var_r + eps) * w[:] + b[:] )
+ * The row stays in registers for two exact passes (mean, then the centred
+ * sum of squares), so the variance does not suffer from E[x^2] - mean^2
+ * cancellation.  b may be NULL (no bias).  Requirements and errors as
+ * rmsnorm_fwd (b, when given, 16-byte aligned).  The persistent schedule
+ * serves power-of-two N from 1024 to 16384; wider rows use a row schedule. */
+int layernorm_fwd(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps,
+                  int64_t M, int64_t N, rn_bf16 *y, rn_stream_t stream);
+
+/* layernorm_fwd with an explicit schedule, wait limit and test flags, as
+ * rmsnorm_fwd_sched. */
+int layernorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b,
+                        float eps, int64_t M, int64_t N, rn_bf16 *y, int schedule,
+                        uint64_t wait_timeout_ns, int debug_flags,
+                        rn_stream_t stream);
+
+/* The schedule (RN_SCHED_*) layernorm_fwd launches for (M, N) on the current
+ * device.  Host-only query: launches nothing. */
+int layernorm_select_schedule(int64_t M, int64_t N);
 
 /* Fused residual add + RMSNorm, one pass:
  *   h[r, j] = bf16(x[r, j] + residual[r, j])   (the exact sum rounded once)

@@ -86,6 +86,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.add_rmsnorm_fwd.restype = i32
         L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
         L.add_rmsnorm_fwd_sched.restype = i32
+        L.layernorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp]
+        L.layernorm_fwd.restype = i32
+        L.layernorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, i32, u64, i32, vp]
+        L.layernorm_fwd_sched.restype = i32
+        L.layernorm_select_schedule.argtypes = [i64, i64]
+        L.layernorm_select_schedule.restype = i32
         L.add_rmsnorm_select_schedule.argtypes = [i64, i64]
         L.add_rmsnorm_select_schedule.restype = i32
         L.rmsnorm_select_schedule.argtypes = [i64, i64]
@@ -155,6 +161,43 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
                                  schedule, wait_timeout_ns, debug_flags, _stream(stream))
     _check(rc, "rmsnorm_fwd")
     return y
+
+
+def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None, eps: float,
+                  y: torch.Tensor | None = None, *, schedule: int = RN_SCHED_AUTO,
+                  wait_timeout_ns: int = 0, debug_flags: int = 0, stream=None) -> torch.Tensor:
+    """y = (x - mean) / sqrt(var + eps) * w + b per row (biased variance); b may be None."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    if b is not None:
+        _need(b, "b", torch.bfloat16)
+        if b.shape != w.shape:
+            raise ValueError("b must have w's shape")
+    if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1]:
+        raise ValueError("x must be [M, N] and w [N]")
+    y = torch.empty_like(x) if y is None else y
+    _need(y, "y", torch.bfloat16)
+    if y.shape != x.shape:
+        raise ValueError("y must have x's shape")
+    M, N = x.shape
+    bp = None if b is None else b.data_ptr()
+    L = load()
+    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+        rc = L.layernorm_fwd(x.data_ptr(), w.data_ptr(), bp, eps, M, N, y.data_ptr(),
+                             _stream(stream))
+    else:
+        rc = L.layernorm_fwd_sched(x.data_ptr(), w.data_ptr(), bp, eps, M, N, y.data_ptr(),
+                                   schedule, wait_timeout_ns, debug_flags, _stream(stream))
+    _check(rc, "layernorm_fwd")
+    return y
+
+
+def layernorm_select_schedule(M: int, N: int) -> int:
+    """The RN_SCHED_* schedule layernorm_fwd picks for (M, N) on the current device."""
+    rc = int(load().layernorm_select_schedule(int(M), int(N)))
+    if rc < 0:
+        raise RowNormError("layernorm_select_schedule", rc)
+    return rc
 
 
 def add_rmsnorm_fwd(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: float,

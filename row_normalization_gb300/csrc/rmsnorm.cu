@@ -63,6 +63,41 @@ __device__ __forceinline__ uint4 add8(uint4 a, uint4 b) {
     return o;
 }
 
+// LayerNorm pieces: sum of 8, sum of squared deviations from `mean`, and
+// y = (x - mean) * rstd * w (+ b) rounded once.
+__device__ __forceinline__ float sum8(uint4 v) {
+    return ((bf_lo(v.x) + bf_hi(v.x)) + (bf_lo(v.y) + bf_hi(v.y))) +
+           ((bf_lo(v.z) + bf_hi(v.z)) + (bf_lo(v.w) + bf_hi(v.w)));
+}
+
+__device__ __forceinline__ float sqdev8(uint4 v, float m) {
+    float a = bf_lo(v.x) - m, b = bf_hi(v.x) - m, c = bf_lo(v.y) - m, d = bf_hi(v.y) - m;
+    float e = bf_lo(v.z) - m, f = bf_hi(v.z) - m, g = bf_lo(v.w) - m, h = bf_hi(v.w) - m;
+    return ((a * a + b * b) + (c * c + d * d)) + ((e * e + f * f) + (g * g + h * h));
+}
+
+__device__ __forceinline__ float ln1(float x, float w, float b, float m, float rstd) {
+    return fmaf((x - m) * rstd, w, b);
+}
+
+__device__ __forceinline__ uint4 ln8(uint4 xv, uint4 wv, uint4 bv, float m, float rstd) {
+    uint4 o;
+    o.x = pack_bf2(ln1(bf_lo(xv.x), bf_lo(wv.x), bf_lo(bv.x), m, rstd),
+                   ln1(bf_hi(xv.x), bf_hi(wv.x), bf_hi(bv.x), m, rstd));
+    o.y = pack_bf2(ln1(bf_lo(xv.y), bf_lo(wv.y), bf_lo(bv.y), m, rstd),
+                   ln1(bf_hi(xv.y), bf_hi(wv.y), bf_hi(bv.y), m, rstd));
+    o.z = pack_bf2(ln1(bf_lo(xv.z), bf_lo(wv.z), bf_lo(bv.z), m, rstd),
+                   ln1(bf_hi(xv.z), bf_hi(wv.z), bf_hi(bv.z), m, rstd));
+    o.w = pack_bf2(ln1(bf_lo(xv.w), bf_lo(wv.w), bf_lo(bv.w), m, rstd),
+                   ln1(bf_hi(xv.w), bf_hi(wv.w), bf_hi(bv.w), m, rstd));
+    return o;
+}
+
+// Bias chunk, or zeros when there is no bias.
+__device__ __forceinline__ uint4 bias16(const uint16_t *b, int c) {
+    return b ? ld_ro16(b + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 __device__ __forceinline__ float row_rstd(float ss, int N, float eps) {
     return __frsqrt_rn(ss / static_cast<float>(N) + eps);
 }
@@ -71,12 +106,13 @@ __device__ __forceinline__ float row_rstd(float ss, int N, float eps) {
 // warp_rows: one warp per row; lane l holds 16-byte chunks l, l+32, ...
 // ---------------------------------------------------------------------------
 // With ADD, the row is h = bf16(x + r) (stored to h_out) and y = rmsnorm(h).
-template <int VPT, bool ADD>
+// With LN, y = layernorm(x) = (x - mean) * rstd * w + b (b may be null).
+template <int VPT, bool ADD, bool LN>
 __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
                                                             uint16_t *y, const uint16_t *r,
-                                                            uint16_t *h_out) {
+                                                            uint16_t *h_out, const uint16_t *b) {
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int cpr = N >> 3;
@@ -99,16 +135,33 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                 }
             }
         }
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
-        ss = warp_sum(ss);
-        const float rstd = row_rstd(ss, N, eps);
         uint16_t *yr = y + row * N;
+        if constexpr (LN) {
+            float s1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int c = lane + 32 * i;
-            if (c < cpr) st16(yr + 8 * c, scale8(v[i], ld_ro16(w + 8 * c), rstd));
+            for (int i = 0; i < VPT; ++i) s1 += sum8(v[i]);  // absent chunks are zero
+            const float mean = warp_sum(s1) / static_cast<float>(N);
+            float s2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i)
+                if (lane + 32 * i < cpr) s2 += sqdev8(v[i], mean);
+            const float rstd = row_rstd(warp_sum(s2), N, eps);
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = lane + 32 * i;
+                if (c < cpr) st16(yr + 8 * c, ln8(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
+            }
+        } else {
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
+            ss = warp_sum(ss);
+            const float rstd = row_rstd(ss, N, eps);
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = lane + 32 * i;
+                if (c < cpr) st16(yr + 8 * c, scale8(v[i], ld_ro16(w + 8 * c), rstd));
+            }
         }
     }
 }
@@ -116,13 +169,14 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
 // ---------------------------------------------------------------------------
 // cta_rows: one CTA per row; thread t holds chunks t, t+nt, ...
 // ---------------------------------------------------------------------------
-template <int VPT, int MAXT, bool ADD>
+template <int VPT, int MAXT, bool ADD, bool LN>
 __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
                                                             uint16_t *y, const uint16_t *r,
-                                                            uint16_t *h_out) {
+                                                            uint16_t *h_out, const uint16_t *b) {
     __shared__ float red[2][32];
+    __shared__ float red2[2][32];  // LayerNorm's second reduction
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
     const int nw = nt >> 5;
@@ -146,6 +200,37 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                 }
             }
         }
+        uint16_t *yr = y + row * N;
+        if constexpr (LN) {
+            // mean first, then the centred sum of squares: two exact passes
+            // over the register-resident row, two CTA reductions.
+            float s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) s1 += sum8(v[i]);  // absent chunks are zero
+            s1 = warp_sum(s1);
+            if ((tid & 31) == 0) red[par][tid >> 5] = s1;
+            __syncthreads();
+            float t1 = 0.f;
+            for (int k = 0; k < nw; ++k) t1 += red[par][k];
+            const float mean = t1 / static_cast<float>(N);
+            float s2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i)
+                if (tid + nt * i < cpr) s2 += sqdev8(v[i], mean);
+            s2 = warp_sum(s2);
+            if ((tid & 31) == 0) red2[par][tid >> 5] = s2;
+            __syncthreads();
+            float t2 = 0.f;
+            for (int k = 0; k < nw; ++k) t2 += red2[par][k];
+            const float rstd = row_rstd(t2, N, eps);
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = tid + nt * i;
+                if (c < cpr)
+                    st16(yr + 8 * c, ln8(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
+            }
+            continue;
+        }
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
@@ -155,7 +240,6 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
         float tot = 0.f;
         for (int k = 0; k < nw; ++k) tot += red[par][k];
         const float rstd = row_rstd(tot, N, eps);
-        uint16_t *yr = y + row * N;
         if constexpr (MAXT < 1024) {
             // issue every weight load before the first store
             uint4 wv[VPT];
@@ -190,6 +274,7 @@ struct BulkArgs {
     uint16_t *y;
     const uint16_t *r;  // residual (fused add) or nullptr
     uint16_t *h;        // x + r output (fused add) or nullptr
+    const uint16_t *b;  // LayerNorm bias or nullptr
     int64_t M;
     int N;
     float eps;
@@ -199,17 +284,19 @@ struct BulkArgs {
 };
 
 // Shared memory: [stages x (R rows of x [+ R rows of r])][full mbarriers]
-//                [empty mbarriers][partial sums 2 x R x 32 floats][flags: 4 ints]
+//                [empty mbarriers][partial sums 4 x R x 32 floats][flags: 4 ints]
+// (two double-buffered sets of partial sums: LayerNorm reduces twice a row)
 // `nin` is the number of row inputs streamed through the ring (1, or 2 with
 // the fused residual add).
 __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1) {
     return static_cast<size_t>(stages) * nin * R * N * 2 + static_cast<size_t>(stages) * 16 +
-           static_cast<size_t>(2) * R * 32 * 4 + 16;
+           static_cast<size_t>(4) * R * 32 * 4 + 16;
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
-template <int VPR, int R, int NT, bool ADD>
+template <int VPR, int R, int NT, bool ADD, bool LN>
 __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const BulkArgs a) {
+    static_assert(!(ADD && LN), "the fused add is an RMSNorm prologue");
     constexpr int NIN = ADD ? 2 : 1;
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = a.stages;
@@ -223,7 +310,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
     // flags[0], flags[1]: "consumers give up" for even / odd units (decided
     // before a named barrier, read after it); flags[2]: "someone gave up",
     // polled inside waits so nobody waits out a full timeout needlessly.
-    volatile int *flags = reinterpret_cast<volatile int *>(red + 2 * R * 32);
+    volatile int *flags = reinterpret_cast<volatile int *>(red + 4 * R * 32);
 
     constexpr int NW = NT / 32;
     const int warp = threadIdx.x >> 5;
@@ -345,6 +432,56 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
                 raise_status(RN_STATUS_WAIT_TIMEOUT);
             }
         }
+        if constexpr (LN) {
+            // LayerNorm: mean, then the centred sum of squares, each reduced
+            // over the CTA's consumer warps (two named barriers a unit).
+            float s1[R];
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < VPR; ++j) acc += sum8(xv[rr][j]);
+                s1[rr] = warp_sum(acc);
+            }
+            float *rb1 = red + (k & 1) * R * 32;
+            float *rb2 = red + (2 + (k & 1)) * R * 32;
+            if (lane == 0) {
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) rb1[rr * 32 + warp] = s1[rr];
+            }
+            named_bar_sync(1, NT);
+            if (flags[k & 1]) break;  // same decision in every consumer warp
+            float mean[R];
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                float t = 0.f;
+                for (int q = 0; q < NW; ++q) t += rb1[rr * 32 + q];
+                mean[rr] = t / static_cast<float>(N);
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < VPR; ++j) acc += sqdev8(xv[rr][j], mean[rr]);
+                s1[rr] = warp_sum(acc);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) rb2[rr * 32 + warp] = s1[rr];
+            }
+            named_bar_sync(1, NT);
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                if (rr < rows) {
+                    float t = 0.f;
+                    for (int q = 0; q < NW; ++q) t += rb2[rr * 32 + q];
+                    const float rstd = row_rstd(t, N, a.eps);
+                    uint16_t *yr = a.y + (r0 + rr) * N;
+#pragma unroll
+                    for (int j = 0; j < VPR; ++j)
+                        st16(yr + 8 * (tid + j * NT),
+                             ln8(xv[rr][j], wv[j], bias16(a.b, tid + j * NT), mean[rr], rstd));
+                }
+            }
+            continue;
+        }
         float ss[R];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
@@ -386,7 +523,8 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 // host side
 // ---------------------------------------------------------------------------
 
-// Everything one launch needs; r and h are set only for the fused residual add.
+// Everything one launch needs; r and h are set only for the fused residual
+// add, b only for LayerNorm.
 struct RowJob {
     const uint16_t *x;
     const uint16_t *w;
@@ -396,9 +534,10 @@ struct RowJob {
     uint16_t *y;
     const uint16_t *r;
     uint16_t *h;
+    const uint16_t *b;  // LayerNorm bias (may be null)
 };
 
-template <bool ADD>
+template <bool ADD, bool LN>
 static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &dev) {
     const int cpr = j.N >> 3;
     const int wpb = 8;
@@ -406,7 +545,8 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 64;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
 #define RN_WARP(V) \
-    rms_warp_rows_kernel<V, ADD><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, j.h)
+    rms_warp_rows_kernel<V, ADD, LN><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, \
+                                                                 j.h, j.b)
     if (cpr <= 32)
         RN_WARP(1);
     else if (cpr <= 64)
@@ -421,7 +561,7 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     return launch_status();
 }
 
-template <bool ADD>
+template <bool ADD, bool LN>
 static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &dev) {
     const int cpr = j.N >> 3;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 2048;
@@ -433,8 +573,8 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
         return ((t + 31) / 32) * 32;
     };
 #define RN_CTA(V, T)                                                                      \
-    rms_cta_rows_kernel<V, T, ADD><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
-                                                                 j.y, j.r, j.h)
+    rms_cta_rows_kernel<V, T, ADD, LN><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
+                                                                     j.y, j.r, j.h, j.b)
     if (cpr <= 512)
         RN_CTA(1, 512);
     else if (cpr <= 1024)
@@ -466,8 +606,21 @@ struct BulkGeometry {
     int nt, vpr, R, stages, ctas;
 };
 
-static bool bulk_geometry(int64_t M, int N, bool add, BulkGeometry *g) {
+static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) {
     const bool few_rows = M <= 8192;
+    if (ln) {
+        // LayerNorm keeps its mean and the bias loads live too: 4-row stages at
+        // 4096 and no ring at 32768 (both spill otherwise).
+        switch (N) {
+            case 1024: *g = {128, 1, 8, 2, 1}; break;
+            case 2048: *g = {256, 1, 8, 2, 1}; break;
+            case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1}; break;
+            case 8192: *g = {256, 4, 2, 2, 1}; break;
+            case 16384: *g = {512, 4, 1, 2, 1}; break;
+            default: return false;
+        }
+        return true;
+    }
     if (add) {
         switch (N) {
             case 1024: *g = {128, 1, 8, 2, 1}; break;
@@ -491,14 +644,14 @@ static bool bulk_geometry(int64_t M, int N, bool add, BulkGeometry *g) {
     return true;
 }
 
-template <int VPR, int R, int NT, bool ADD>
+template <int VPR, int R, int NT, bool ADD, bool LN>
 static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_cap,
                             cudaStream_t st) {
     static std::atomic<int> attr_done[kMaxDevices];
     const int dev = current_device_index();
     if (dev < 0 || dev >= kMaxDevices) return RN_ERR_DEVICE;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<VPR, R, NT, ADD>,
+        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<VPR, R, NT, ADD, LN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_cap) != cudaSuccess) {
             cudaGetLastError();
@@ -506,17 +659,17 @@ static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_c
         }
         attr_done[dev].store(1, std::memory_order_release);
     }
-    rms_persistent_bulk_kernel<VPR, R, NT, ADD><<<grid, NT + 32, smem, st>>>(a);
+    rms_persistent_bulk_kernel<VPR, R, NT, ADD, LN><<<grid, NT + 32, smem, st>>>(a);
     return launch_status();
 }
 
-template <bool ADD>
+template <bool ADD, bool LN>
 static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const DeviceInfo &dev,
                                   uint64_t timeout_ns, int debug_flags) {
     constexpr int NIN = ADD ? 2 : 1;
     BulkGeometry geo;
     const int N = j.N;
-    if (!bulk_geometry(j.M, N, ADD, &geo)) return RN_ERR_SHAPE;
+    if (!bulk_geometry(j.M, N, ADD, LN, &geo)) return RN_ERR_SHAPE;
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
     const size_t stage_cost = static_cast<size_t>(NIN) * geo.R * N * 2 + 16;
     int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N, NIN)) / stage_cost);
@@ -531,28 +684,31 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN);
     int64_t grid = static_cast<int64_t>(dev.sm_count) * ctas_per_sm;
     if (grid > j.M) grid = j.M;
-    BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.M, N, j.eps, stages, debug_flags & 1,
+    BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.M, N, j.eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
     const int g = static_cast<int>(grid);
     switch (N) {
-        case 1024: return launch_bulk_inst<1, 8, 128, ADD>(a, g, smem, smem_cap, st);
-        case 2048: return launch_bulk_inst<1, 8, 256, ADD>(a, g, smem, smem_cap, st);
+        case 1024: return launch_bulk_inst<1, 8, 128, ADD, LN>(a, g, smem, smem_cap, st);
+        case 2048: return launch_bulk_inst<1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
         case 4096:
-            return geo.R == 4 ? launch_bulk_inst<2, 4, 256, ADD>(a, g, smem, smem_cap, st)
-                              : launch_bulk_inst<2, 8, 256, ADD>(a, g, smem, smem_cap, st);
-        case 8192: return launch_bulk_inst<4, 2, 256, ADD>(a, g, smem, smem_cap, st);
-        case 16384: return launch_bulk_inst<4, 1, 512, ADD>(a, g, smem, smem_cap, st);
+            if constexpr (ADD || LN) return launch_bulk_inst<2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
+            else
+                return geo.R == 4 ? launch_bulk_inst<2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st)
+                                  : launch_bulk_inst<2, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 8192: return launch_bulk_inst<4, 2, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 16384: return launch_bulk_inst<4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
         case 32768:
-            if constexpr (!ADD) return launch_bulk_inst<8, 1, 512, ADD>(a, g, smem, smem_cap, st);
+            if constexpr (!ADD && !LN)
+                return launch_bulk_inst<8, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
             break;
     }
     return RN_ERR_SHAPE;
 }
 
-static int auto_schedule(int64_t M, int N, bool add, const DeviceInfo &dev) {
+static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &dev) {
     BulkGeometry geo;
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    if (bulk_geometry(M, N, add, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
+    if (bulk_geometry(M, N, add, ln, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
     return RN_SCHED_CTA_ROW;
 }
@@ -562,19 +718,19 @@ static int check_rows(int64_t M, int64_t N) {
     return RN_OK;
 }
 
-template <bool ADD>
+template <bool ADD, bool LN>
 static int rows_dispatch(const RowJob &j, int schedule, uint64_t timeout_ns, int debug_flags,
                          rn_stream_t stream) {
     if (schedule < RN_SCHED_AUTO || schedule > RN_SCHED_PERSIST_BULK) return RN_ERR_ARG;
     const DeviceInfo *dev = current_device_info();
     if (!dev) return RN_ERR_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, *dev);
+    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, LN, *dev);
     switch (schedule) {
-        case RN_SCHED_WARP_ROW: return launch_warp_rows<ADD>(j, st, *dev);
-        case RN_SCHED_CTA_ROW: return launch_cta_rows<ADD>(j, st, *dev);
+        case RN_SCHED_WARP_ROW: return launch_warp_rows<ADD, LN>(j, st, *dev);
+        case RN_SCHED_CTA_ROW: return launch_cta_rows<ADD, LN>(j, st, *dev);
         case RN_SCHED_PERSIST_BULK:
-            return launch_persistent_bulk<ADD>(j, st, *dev, timeout_ns, debug_flags);
+            return launch_persistent_bulk<ADD, LN>(j, st, *dev, timeout_ns, debug_flags);
     }
     return RN_ERR_ARG;
 }
@@ -587,8 +743,8 @@ static int rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, float eps, int64
     if (M == 0) return RN_OK;
     if (!x || !w || !y) return RN_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return RN_ERR_ALIGN;
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr};
-    return rows_dispatch<false>(j, schedule, timeout_ns, debug_flags, stream);
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, nullptr};
+    return rows_dispatch<false, false>(j, schedule, timeout_ns, debug_flags, stream);
 }
 
 static int add_rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *res, const rn_bf16 *w, float eps,
@@ -601,8 +757,21 @@ static int add_rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *res, const rn_b
     if (!aligned16(x) || !aligned16(res) || !aligned16(w) || !aligned16(h) || !aligned16(y))
         return RN_ERR_ALIGN;
     if (h == y) return RN_ERR_ARG;  // two different outputs
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, res, h};
-    return rows_dispatch<true>(j, schedule, timeout_ns, debug_flags, stream);
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, res, h, nullptr};
+    return rows_dispatch<true, false>(j, schedule, timeout_ns, debug_flags, stream);
+}
+
+static int layernorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps,
+                              int64_t M, int64_t N, rn_bf16 *y, int schedule,
+                              uint64_t timeout_ns, int debug_flags, rn_stream_t stream) {
+    const int rc = check_rows(M, N);
+    if (rc != RN_OK) return rc;
+    if (M == 0) return RN_OK;
+    if (!x || !w || !y) return RN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (b && !aligned16(b)))
+        return RN_ERR_ALIGN;
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, b};
+    return rows_dispatch<false, true>(j, schedule, timeout_ns, debug_flags, stream);
 }
 
 }  // namespace rn
@@ -625,14 +794,33 @@ int rmsnorm_select_schedule(int64_t M, int64_t N) {
     if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
     const rn::DeviceInfo *dev = rn::current_device_info();
     if (!dev) return RN_ERR_DEVICE;
-    return rn::auto_schedule(M, static_cast<int>(N), false, *dev);
+    return rn::auto_schedule(M, static_cast<int>(N), false, false, *dev);
+}
+
+int layernorm_fwd(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps, int64_t M,
+                  int64_t N, rn_bf16 *y, rn_stream_t stream) {
+    return rn::layernorm_dispatch(x, w, b, eps, M, N, y, RN_SCHED_AUTO, 0, 0, stream);
+}
+
+int layernorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps,
+                        int64_t M, int64_t N, rn_bf16 *y, int schedule, uint64_t wait_timeout_ns,
+                        int debug_flags, rn_stream_t stream) {
+    return rn::layernorm_dispatch(x, w, b, eps, M, N, y, schedule, wait_timeout_ns, debug_flags,
+                                  stream);
 }
 
 int add_rmsnorm_select_schedule(int64_t M, int64_t N) {
     if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
     const rn::DeviceInfo *dev = rn::current_device_info();
     if (!dev) return RN_ERR_DEVICE;
-    return rn::auto_schedule(M, static_cast<int>(N), true, *dev);
+    return rn::auto_schedule(M, static_cast<int>(N), true, false, *dev);
+}
+
+int layernorm_select_schedule(int64_t M, int64_t N) {
+    if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
+    const rn::DeviceInfo *dev = rn::current_device_info();
+    if (!dev) return RN_ERR_DEVICE;
+    return rn::auto_schedule(M, static_cast<int>(N), false, true, *dev);
 }
 
 int add_rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *residual, const rn_bf16 *w, float eps,

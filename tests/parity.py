@@ -19,17 +19,22 @@ REL_BOUND = 2.0**-7
 MAX_ONE_ULP_FRACTION = 1e-3
 
 
-def parity_report(gpu_bits, ref_bits) -> dict:
+def parity_report(gpu_bits, ref_bits, abs_floor=None) -> dict:
+    """`abs_floor` (scalar or per-element array) replaces the 1e-6 absolute
+    floor where an operation's own fp32 error bound is larger (LayerNorm rows
+    with a large mean: the centring x - mean carries |mean| * 2^-24)."""
     gpu_bits = np.asarray(gpu_bits, dtype=np.uint16).ravel()
     ref_bits = np.asarray(ref_bits, dtype=np.uint16).ravel()
     assert gpu_bits.shape == ref_bits.shape
+    floor = ABS_FLOOR if abs_floor is None else np.maximum(
+        ABS_FLOOR, np.broadcast_to(np.asarray(abs_floor, dtype=np.float64), gpu_bits.shape))
     g = bits_to_f64(gpu_bits)
     r = bits_to_f64(ref_bits)
     diff = np.abs(g - r)
     ulp = ulp_distance_bf16(gpu_bits, ref_bits)
     finite = np.isfinite(g) & np.isfinite(r)
-    over_bound = ~(diff <= REL_BOUND * np.abs(r) + ABS_FLOOR) | ~finite
-    multi_ulp = (ulp > 1) & (diff > ABS_FLOOR)
+    over_bound = ~(diff <= REL_BOUND * np.abs(r) + floor) | ~finite
+    multi_ulp = (ulp > 1) & (diff > floor)
     bad = over_bound | multi_ulp
     n = max(1, gpu_bits.size)
     return {
@@ -37,16 +42,17 @@ def parity_report(gpu_bits, ref_bits) -> dict:
         "bad": int(bad.sum()),
         "one_ulp": int((ulp == 1).sum()),
         "one_ulp_frac": float((ulp == 1).sum()) / n,
-        "near_zero_multi_ulp": int(((ulp > 1) & (diff <= ABS_FLOOR)).sum()),
+        "near_zero_multi_ulp": int(((ulp > 1) & (diff <= floor)).sum()),
         "exact": int((ulp == 0).sum()),
         "max_ulp": int(ulp.max()) if ulp.size else 0,
         "first_bad": (np.flatnonzero(bad)[:8].tolist()),
     }
 
 
-def assert_parity(gpu_bits, ref_bits, what: str = "") -> dict:
-    rep = parity_report(gpu_bits, ref_bits)
+def assert_parity(gpu_bits, ref_bits, what: str = "", abs_floor=None,
+                  max_one_ulp_frac: float = MAX_ONE_ULP_FRACTION) -> dict:
+    rep = parity_report(gpu_bits, ref_bits, abs_floor)
     assert rep["bad"] == 0, f"{what}: {rep['bad']} elements outside tolerance: {rep}"
-    assert rep["one_ulp_frac"] <= MAX_ONE_ULP_FRACTION, \
-        f"{what}: {rep['one_ulp_frac']:.5%} elements one bf16 step off (> 0.1%): {rep}"
+    assert rep["one_ulp_frac"] <= max_one_ulp_frac, \
+        f"{what}: {rep['one_ulp_frac']:.5%} elements one bf16 step off (> {max_one_ulp_frac:.2%}): {rep}"
     return rep

@@ -109,6 +109,14 @@ def test_add_rmsnorm_checks(lib):
     assert lib.add_rmsnorm_fwd(P, P, P, 1e-6, 4, 64, P + 4096, P + 4096, None) == binding.RN_ERR_ARG
 
 
+def test_layernorm_checks(lib):
+    assert lib.layernorm_fwd(P, P, None, 1e-5, 4, 7, P, None) == binding.RN_ERR_SHAPE
+    assert lib.layernorm_fwd(P, P, None, 1e-5, 0, 64, P, None) == binding.RN_OK
+    assert lib.layernorm_fwd(P, None, P, 1e-5, 4, 64, P, None) == binding.RN_ERR_NULL
+    assert lib.layernorm_fwd(P, P, MISALIGNED, 1e-5, 4, 64, P, None) == binding.RN_ERR_ALIGN
+    assert lib.layernorm_fwd_sched(P, P, None, 1e-5, 4, 64, P, 7, 0, 0, None) == binding.RN_ERR_ARG
+
+
 def test_table_checks(lib):
     assert lib.rope_cos_sin_table(1e6, 16, 7, P, None) == binding.RN_ERR_SHAPE
     assert lib.rope_cos_sin_table(-1.0, 16, 8, P, None) == binding.RN_ERR_SHAPE

@@ -1,0 +1,122 @@
+"""GPU parity: LayerNorm (CUDA, through the C ABI) against the fp64 oracle.
+
+Operation: "TorchInductor: from ATen IR to Triton kernel", section 14.12.2
+(var_mean -> add(eps) -> rsqrt -> sub -> mul -> mul(weight) -> add(bias), one
+fused kernel) and "[Inductor] Codegen Gluon", section 3.2 (LayerNorm reuses
+its input in both the statistics and the normalise pass).  The oracle uses
+the plain two-pass mean and biased variance in double.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from row_normalization_gb300 import binding
+from row_normalization_gb300.inputs import bf16_bits, norm_bias, rmsnorm_inputs
+from tests.exact import bits_to_f64
+from tests.gpu_util import canary_intact, padded_empty, require_gpu
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+SCHEDULES = [binding.RN_SCHED_AUTO, binding.RN_SCHED_WARP_ROW, binding.RN_SCHED_CTA_ROW,
+             binding.RN_SCHED_PERSIST_BULK]
+
+
+def eligible(schedule: int, N: int) -> bool:
+    if schedule == binding.RN_SCHED_WARP_ROW:
+        return N <= 2048
+    if schedule == binding.RN_SCHED_PERSIST_BULK:
+        return N in (1024, 2048, 4096, 8192, 16384)
+    return True
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+SHAPES = [(1, 8), (7, 64), (5, 1000), (33, 2048), (3, 4104), (130, 1024), (300, 4096),
+          (17, 8192), (9, 16384), (5, 32768), (2, 65536), (1000, 512), (2311, 4096)]
+
+
+@pytest.mark.parametrize("bias", [True, False])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_small_shapes_every_schedule(M, N, schedule, bias):
+    x, w = rmsnorm_inputs(M, N, outlier_frac=0.02 if M >= 50 else 0.0, seed=M + 2 * N)
+    b = norm_bias(N, seed=M + N) if bias else None
+    want = oracle.layernorm(bf16_bits(x), bf16_bits(w), None if b is None else bf16_bits(b), 1e-5)
+    pad = 64
+    yb, y = padded_empty((M, N), torch.bfloat16, pad, 0x7FC7)
+    args = (x.cuda(), w.cuda(), None if b is None else b.cuda(), 1e-5, y)
+    if not eligible(schedule, N):
+        with pytest.raises(binding.RowNormError) as ei:
+            binding.layernorm_fwd(*args, schedule=schedule)
+        assert ei.value.code == binding.RN_ERR_SHAPE
+        return
+    binding.layernorm_fwd(*args, schedule=schedule)
+    torch.cuda.synchronize()
+    assert_parity(bf16_bits(y), want, f"ln M={M} N={N} sched={schedule} bias={bias}")
+    assert canary_intact(yb, pad, 0x7FC7)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES[1:])
+def test_constant_row_gives_the_bias_exactly(schedule):
+    N = 2048 if schedule == binding.RN_SCHED_WARP_ROW else 4096
+    x = torch.full((4, N), 3.25, dtype=torch.bfloat16)
+    w = torch.ones(N, dtype=torch.bfloat16)
+    b = norm_bias(N, seed=3)
+    y = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), 1e-5, schedule=schedule)
+    assert np.array_equal(bf16_bits(y), np.tile(bf16_bits(b), (4, 1)))
+
+
+@pytest.mark.parametrize("shift", [8.0, 1000.0])
+@pytest.mark.parametrize("schedule", SCHEDULES[1:])
+def test_rows_with_a_large_mean(shift, schedule):
+    # Two-pass statistics keep the variance accurate far from zero mean.  The
+    # fp32 centring carries |mean| * 2^-24 of absolute error, which rstd * |w|
+    # scales; that is the floor here (it is below 1e-6 for shift 8).  The same
+    # error, relative to |x - mean| ~ 1, is ~1e-5 at shift 1000, which moves
+    # about 0.2% of outputs by one bf16 step: the one-step budget is 1% there.
+    N = 2048 if schedule == binding.RN_SCHED_WARP_ROW else 8192
+    M = 64
+    g = torch.Generator().manual_seed(11)
+    x = (shift + torch.randn(M, N, generator=g)).to(torch.bfloat16)
+    w = rmsnorm_inputs(1, N, seed=5)[1]
+    b = norm_bias(N, seed=6)
+    want = oracle.layernorm(bf16_bits(x), bf16_bits(w), bf16_bits(b), 1e-5)
+    y = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), 1e-5, schedule=schedule)
+    xf = bits_to_f64(bf16_bits(x))
+    rstd = 1 / np.sqrt(xf.var(-1, keepdims=True) + 1e-5)
+    floor = 4 * np.abs(xf.mean(-1, keepdims=True)) * 2.0**-24 * rstd * np.abs(bits_to_f64(bf16_bits(w)))
+    assert_parity(bf16_bits(y), want, f"ln shift={shift} sched={schedule}",
+                  abs_floor=np.broadcast_to(floor, (M, N)).ravel(),
+                  max_one_ulp_frac=1e-3 if shift < 100 else 1e-2)
+
+
+def test_wait_timeout_reports_status_and_context_survives():
+    binding.device_status(clear=True)
+    x, w = rmsnorm_inputs(2, 1024, seed=3)
+    xd, wd = x.cuda(), w.cuda()
+    binding.layernorm_fwd(xd, wd, None, 1e-5, schedule=binding.RN_SCHED_PERSIST_BULK,
+                          wait_timeout_ns=2_000_000, debug_flags=1)
+    assert binding.device_status(clear=True) & binding.RN_STATUS_WAIT_TIMEOUT
+    y = binding.layernorm_fwd(xd, wd, None, 1e-5, schedule=binding.RN_SCHED_PERSIST_BULK)
+    assert_parity(bf16_bits(y), oracle.layernorm(bf16_bits(x), bf16_bits(w), None, 1e-5), "after")
+    assert binding.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("M,N", [(8192, 8192), (32768, 4096), (4096, 16384), (1024, 32768)])
+def test_full_size_sampled_rows(M, N):
+    x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, device="cuda", seed=9)
+    b = norm_bias(N, device="cuda", seed=10)
+    y = binding.layernorm_fwd(x, w, b, 1e-5)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(M * 3 + N)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, size=96, replace=False)]))
+    idx = torch.from_numpy(rows).cuda()
+    want = oracle.layernorm(bf16_bits(x.index_select(0, idx)), bf16_bits(w), bf16_bits(b), 1e-5)
+    assert_parity(bf16_bits(y.index_select(0, idx)), want, f"ln sampled M={M} N={N}")
