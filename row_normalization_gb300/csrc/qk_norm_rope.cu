@@ -526,22 +526,26 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
             load_f32_smem<A>(cs + sub * A, c);
             load_f32_smem<A>(cs + H2 + sub * A, sn);
 
-            float2 acc = make_float2(0.f, 0.f);
+            // two independent accumulators: half the dependent FMA chain
+            float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < A2; ++i) {
                 const float2 u = bf2f(x1[i]);
                 const float2 v = bf2f(x2[i]);
                 acc = __ffma2_rn(u, u, acc);
-                acc = __ffma2_rn(v, v, acc);
+                acc2 = __ffma2_rn(v, v, acc2);
             }
             if constexpr (B > 0) {
 #pragma unroll
                 for (int i = 0; i < B2; ++i) {
                     const float2 u = bf2f(x3[i]);
-                    acc = __ffma2_rn(u, u, acc);
+                    if (i & 1)
+                        acc2 = __ffma2_rn(u, u, acc2);
+                    else
+                        acc = __ffma2_rn(u, u, acc);
                 }
             }
-            const float ss = group_sum<LPH>(acc.x + acc.y);
+            const float ss = group_sum<LPH>((acc.x + acc.y) + (acc2.x + acc2.y));
             // D is a power of two: multiplying by 1/D is the exact division.
             const float rstd = __frsqrt_rn(ss * (1.0f / static_cast<float>(D)) + a.eps);
             const bool isq = h < static_cast<uint32_t>(Hq);

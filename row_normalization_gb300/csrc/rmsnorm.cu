@@ -76,20 +76,22 @@ __device__ __forceinline__ float sqdev8(uint4 v, float m) {
     return ((a * a + b * b) + (c * c + d * d)) + ((e * e + f * f) + (g * g + h * h));
 }
 
-__device__ __forceinline__ float ln1(float x, float w, float b, float m, float rstd) {
-    return fmaf((x - m) * rstd, w, b);
+// Same, on fp32 pairs (Blackwell FADD2/FMUL2/FFMA2): per pair one subtract,
+// one multiply by rstd, one fused multiply-add with (w, b).
+__device__ __forceinline__ uint32_t ln2w(uint32_t x, uint32_t w, uint32_t b, float2 nm, float2 r) {
+    const float2 d = __fmul2_rn(__fadd2_rn(make_float2(bf_lo(x), bf_hi(x)), nm), r);
+    const float2 y = __ffma2_rn(d, make_float2(bf_lo(w), bf_hi(w)), make_float2(bf_lo(b), bf_hi(b)));
+    return pack_bf2(y.x, y.y);
 }
 
 __device__ __forceinline__ uint4 ln8(uint4 xv, uint4 wv, uint4 bv, float m, float rstd) {
+    const float2 nm = make_float2(-m, -m);
+    const float2 r = make_float2(rstd, rstd);
     uint4 o;
-    o.x = pack_bf2(ln1(bf_lo(xv.x), bf_lo(wv.x), bf_lo(bv.x), m, rstd),
-                   ln1(bf_hi(xv.x), bf_hi(wv.x), bf_hi(bv.x), m, rstd));
-    o.y = pack_bf2(ln1(bf_lo(xv.y), bf_lo(wv.y), bf_lo(bv.y), m, rstd),
-                   ln1(bf_hi(xv.y), bf_hi(wv.y), bf_hi(bv.y), m, rstd));
-    o.z = pack_bf2(ln1(bf_lo(xv.z), bf_lo(wv.z), bf_lo(bv.z), m, rstd),
-                   ln1(bf_hi(xv.z), bf_hi(wv.z), bf_hi(bv.z), m, rstd));
-    o.w = pack_bf2(ln1(bf_lo(xv.w), bf_lo(wv.w), bf_lo(bv.w), m, rstd),
-                   ln1(bf_hi(xv.w), bf_hi(wv.w), bf_hi(bv.w), m, rstd));
+    o.x = ln2w(xv.x, wv.x, bv.x, nm, r);
+    o.y = ln2w(xv.y, wv.y, bv.y, nm, r);
+    o.z = ln2w(xv.z, wv.z, bv.z, nm, r);
+    o.w = ln2w(xv.w, wv.w, bv.w, nm, r);
     return o;
 }
 
@@ -381,6 +383,11 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
     uint4 wv[VPR];
 #pragma unroll
     for (int j = 0; j < VPR; ++j) wv[j] = ld_ro16(a.w + 8 * (tid + j * NT));
+    uint4 bv[LN ? VPR : 1];  // LayerNorm bias, held like the weights
+    if constexpr (LN) {
+#pragma unroll
+        for (int j = 0; j < VPR; ++j) bv[j] = bias16(a.b, tid + j * NT);
+    }
 
     for (int64_t k = 0; k < n_units; ++k) {
         int64_t r0;
@@ -392,6 +399,11 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 #pragma unroll
         for (int j = 0; j < VPR; ++j)
             asm volatile("" : "+r"(wv[j].x), "+r"(wv[j].y), "+r"(wv[j].z), "+r"(wv[j].w));
+        if constexpr (LN) {
+#pragma unroll
+            for (int j = 0; j < VPR; ++j)
+                asm volatile("" : "+r"(bv[j].x), "+r"(bv[j].y), "+r"(bv[j].z), "+r"(bv[j].w));
+        }
         const int s = static_cast<int>(k % S);
         const uint32_t par = static_cast<uint32_t>((k / S) & 1);
         const bool ok =
@@ -477,7 +489,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
                         st16(yr + 8 * (tid + j * NT),
-                             ln8(xv[rr][j], wv[j], bias16(a.b, tid + j * NT), mean[rr], rstd));
+                             ln8(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
                 }
             }
             continue;
