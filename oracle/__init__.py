@@ -13,6 +13,7 @@ Passages followed:
   * RMSNorm -- "[Inductor] Codegen Gluon", section 3.1.
   * fused Q/K RMSNorm + neox RoPE -- "[pretuned] Optimize fused_qk_norm_rope
     on B200", section "Summary".
+  * L2Norm -- "[Inductor] Codegen Gluon", section 3.2.
   * fused residual add + RMSNorm -- "TorchInductor: from ATen IR to Triton
     kernel", sections 14.3 and 14.27.
   * LayerNorm -- "TorchInductor: from ATen IR to Triton kernel", section
@@ -85,6 +86,8 @@ def _load():
             u16p, u16p, u16p, f32p, i64p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float]
         lib.rn_oracle_qk_norm_rope.restype = ctypes.c_int
+        lib.rn_oracle_l2norm.argtypes = [u16p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64, u16p]
+        lib.rn_oracle_l2norm.restype = ctypes.c_int
         lib.rn_oracle_add_rmsnorm.argtypes = [u16p, u16p, u16p, ctypes.c_float, ctypes.c_int64,
                                               ctypes.c_int64, u16p, u16p]
         lib.rn_oracle_add_rmsnorm.restype = ctypes.c_int
@@ -181,6 +184,16 @@ def qk_norm_rope(qkv: np.ndarray, wq: np.ndarray, wk: np.ndarray,
         _ptr(cos_sin, ctypes.c_float), _ptr(positions, ctypes.c_int64),
         cos_sin.shape[0], T, Hq, Hkv, D, rotary_dim, ctypes.c_float(eps)), "qk_norm_rope")
     return out
+
+
+def l2norm(x: np.ndarray, eps: float) -> np.ndarray:
+    """y = bf16(x / max(||x||_2, eps)) row by row."""
+    x = _u16(x)
+    M, N = x.shape
+    y = np.zeros_like(x)
+    _check(_load().rn_oracle_l2norm(_ptr(x, ctypes.c_uint16), ctypes.c_float(eps), M, N,
+                                    _ptr(y, ctypes.c_uint16)), "l2norm")
+    return y
 
 
 def add_rmsnorm(x: np.ndarray, res: np.ndarray, w: np.ndarray, eps: float):

@@ -16,6 +16,7 @@
  *     "Summary" (norm over the whole head, Q/K weights, RoPE, one store per
  *     half; partial rotary still normalises the non-rotary tail).
  *   - The rotary cos/sin table used as an input by the above.
+ *   - L2Norm (x / max(||x||, eps)): "[Inductor] Codegen Gluon", section 3.2.
  *   - Fused residual add + RMSNorm: "TorchInductor: from ATen IR to Triton
  *     kernel", sections 14.3 and 14.27.
  *   - LayerNorm (mean and biased variance, then affine): "TorchInductor: from
@@ -216,6 +217,30 @@ int rn_oracle_qk_norm_rope(uint16_t *qkv, const uint16_t *wq,
         }
     }
     return bad ? -3 : 0;
+}
+
+/* ---- L2Norm ------------------------------------------------------------- */
+
+/* y[r, j] = bf16( x[r, j] / max(||x[r, :]||_2, eps) ): one reduction, then a
+ * scale by the inverse norm ("[Inductor] Codegen Gluon", section 3.2).  The
+ * norm is sqrt(sum_j x^2) in double; eps guards rows whose norm is below it. */
+int rn_oracle_l2norm(const uint16_t *x, float eps, int64_t M, int64_t N, uint16_t *y)
+{
+    if (M < 0 || N <= 0) return -3;
+    if (M == 0) return 0;
+    if (!x || !y) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double v = rn_oracle_bf16_to_double(x[r * N + j]);
+            ss += v * v;
+        }
+        double nrm = sqrt(ss);
+        double d = nrm > (double)eps ? nrm : (double)eps;
+        for (int64_t j = 0; j < N; ++j)
+            y[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) / d);
+    }
+    return 0;
 }
 
 /* ---- fused residual add + RMSNorm ---------------------------------------- */

@@ -40,6 +40,8 @@ MUTANTS = {
                           "double f = pow(theta, -1.0 * (double)i / (double)rotary_dim);"),
     "table_sin_first": ("row[i] = (float)cos(a);\n            row[half + i] = (float)sin(a);",
                         "row[i] = (float)sin(a);\n            row[half + i] = (float)cos(a);"),
+    "l2_norm_squared": ("double nrm = sqrt(ss);", "double nrm = ss;"),
+    "l2_eps_added": ("double d = nrm > (double)eps ? nrm : (double)eps;", "double d = nrm + (double)eps;"),
     "add_sum_not_rounded": ("h[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) +",
                             "h[r * N + j] = rn_oracle_double_to_bf16(0.999 * rn_oracle_bf16_to_double(x[r * N + j]) +"),
     "add_norm_of_x_only": ("return rn_oracle_rmsnorm(h, w, eps, M, N, y);", "return rn_oracle_rmsnorm(x, w, eps, M, N, y);"),

@@ -545,3 +545,56 @@ def test_add_rmsnorm_is_the_composition():
     yu = np.array([[round_bf16(Fraction(float(v))) for v in row] for row in unrounded[:4]],
                   dtype=np.uint16)
     assert np.count_nonzero(yu != y[:4]) > 0
+
+
+# ---------------------------------------------------------------------------
+# L2Norm
+# ---------------------------------------------------------------------------
+
+def test_l2norm_closed_forms():
+    N = 64
+    eps = 1e-12
+    # constant row c: ||x|| = |c| sqrt(N) -> y = sign(c) / 8 exactly
+    for c in (3.0, -0.5):
+        y = oracle.l2norm(np.full((1, N), bf([c])[0], dtype=np.uint16), eps)[0]
+        assert np.all(bits_to_f64(y) == np.sign(c) / 8.0)
+    # one-hot: y = sign(a) at k, zero elsewhere
+    x = np.zeros((1, N), dtype=np.uint16)
+    x[0, 5] = bf([-7.25])[0]
+    y = bits_to_f64(oracle.l2norm(x, eps)[0])
+    assert y[5] == -1.0 and np.all(np.delete(y, 5) == 0.0)
+    # a row whose norm is below eps is divided by eps, not by its norm
+    x = np.full((1, 4), bf([2.0**-20])[0], dtype=np.uint16)  # ||x|| = 2^-19
+    y = bits_to_f64(oracle.l2norm(x, 2.0**-10)[0])
+    assert np.all(y == 2.0**-10)
+    # norm = eps / 2: max(norm, eps) = eps gives 0.25; adding eps would give 1/6
+    x = np.full((1, 4), bf([2.0**-11])[0], dtype=np.uint16)  # ||x|| = 2^-10
+    y = bits_to_f64(oracle.l2norm(x, 2.0**-9)[0])
+    assert np.all(y == 0.25)
+    # zero row stays zero
+    assert np.all(oracle.l2norm(np.zeros((2, 8), np.uint16), eps) == 0)
+
+
+def test_l2norm_unit_norm_and_exact_brute_force():
+    rng = np.random.default_rng(81)
+    x = rand_bf16(rng, (5, 300), scale=2.0)
+    y = bits_to_f64(oracle.l2norm(x, 1e-12))
+    np.testing.assert_allclose((y * y).sum(-1), 1.0, rtol=2**-7)
+    for N in (1, 3, 8, 13):
+        x = rand_bf16(rng, (2, N))
+        got = oracle.l2norm(x, 1e-12)
+        for r in range(2):
+            xs = [bits_to_fraction(v) for v in x[r]]
+            den = dsqrt(sum(v * v for v in xs))
+            for j in range(N):
+                assert got[r, j] == round_bf16(to_dec(xs[j]) / den)
+
+
+def test_l2norm_matches_library_normalize():
+    # torch.nn.functional.normalize in float64 (a library routine), rounded once
+    rng = np.random.default_rng(83)
+    x = rand_bf16(rng, (6, 520))
+    xf = torch.from_numpy(bits_to_f64(x))
+    ref = torch.nn.functional.normalize(xf, p=2.0, dim=-1, eps=1e-12).numpy()
+    want = np.array([[round_bf16(Fraction(float(v))) for v in row] for row in ref], dtype=np.uint16)
+    assert np.array_equal(oracle.l2norm(x, 1e-12), want)
