@@ -86,6 +86,8 @@ def _load():
             u16p, u16p, u16p, f32p, i64p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float]
         lib.rn_oracle_qk_norm_rope.restype = ctypes.c_int
+        lib.rn_oracle_qk_norm_rope_ex.argtypes = lib.rn_oracle_qk_norm_rope.argtypes + [ctypes.c_int]
+        lib.rn_oracle_qk_norm_rope_ex.restype = ctypes.c_int
         lib.rn_oracle_l2norm.argtypes = [u16p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64, u16p]
         lib.rn_oracle_l2norm.restype = ctypes.c_int
         lib.rn_oracle_add_rmsnorm.argtypes = [u16p, u16p, u16p, ctypes.c_float, ctypes.c_int64,
@@ -165,8 +167,9 @@ def rope_cos_sin(theta: float, max_pos: int, rotary_dim: int) -> np.ndarray:
 
 def qk_norm_rope(qkv: np.ndarray, wq: np.ndarray, wk: np.ndarray,
                  cos_sin: np.ndarray, positions: np.ndarray, Hq: int, Hkv: int,
-                 D: int, rotary_dim: int, eps: float) -> np.ndarray:
-    """Return a copy of qkv [T, (Hq+2Hkv)*D] with Q/K heads normed and rotated."""
+                 D: int, rotary_dim: int, eps: float, style: int = 0) -> np.ndarray:
+    """Return a copy of qkv [T, (Hq+2Hkv)*D] with Q/K heads normed and rotated.
+    style 0: neox pairs (i, i + r/2); style 1: GPT-J pairs (2i, 2i + 1)."""
     out = _u16(qkv).copy()
     wq = _u16(wq)
     wk = _u16(wk)
@@ -179,10 +182,12 @@ def qk_norm_rope(qkv: np.ndarray, wq: np.ndarray, wk: np.ndarray,
         raise ValueError("cos_sin must be [max_pos, rotary_dim]")
     if positions.shape != (T,):
         raise ValueError("positions must be [T]")
-    _check(_load().rn_oracle_qk_norm_rope(
+    fn = _load().rn_oracle_qk_norm_rope_ex if style else _load().rn_oracle_qk_norm_rope
+    extra = (int(style),) if style else ()
+    _check(fn(
         _ptr(out, ctypes.c_uint16), _ptr(wq, ctypes.c_uint16), _ptr(wk, ctypes.c_uint16),
         _ptr(cos_sin, ctypes.c_float), _ptr(positions, ctypes.c_int64),
-        cos_sin.shape[0], T, Hq, Hkv, D, rotary_dim, ctypes.c_float(eps)), "qk_norm_rope")
+        cos_sin.shape[0], T, Hq, Hkv, D, rotary_dim, ctypes.c_float(eps), *extra), "qk_norm_rope")
     return out
 
 

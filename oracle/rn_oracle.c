@@ -170,17 +170,19 @@ int rn_oracle_rope_cos_sin(double theta, int64_t max_pos, int rotary_dim,
  *         o_{i+r/2} = n_{i+r/2} * c + n_i * s
  *   o_j = n_j for r <= j < D (the non-rotary tail);
  * each o rounded once to bf16.  Value heads are neither read nor written.
- * Follows "[pretuned] Optimize fused_qk_norm_rope on B200", section
- * "Summary".  A position outside [0, max_pos) is an error (-3) and nothing
+ * style 0 is the neox pairing above; style 1 pairs interleaved neighbours
+ * (GPT-J): o_{2i} = n_{2i} c - n_{2i+1} s, o_{2i+1} = n_{2i+1} c + n_{2i} s,
+ * with the same table row.  Follows "[pretuned] Optimize fused_qk_norm_rope on
+ * B200", section "Summary".  A position outside [0, max_pos) is an error (-3) and nothing
  * is written for that token. */
-int rn_oracle_qk_norm_rope(uint16_t *qkv, const uint16_t *wq,
+int rn_oracle_qk_norm_rope_ex(uint16_t *qkv, const uint16_t *wq,
                            const uint16_t *wk, const float *cos_sin,
                            const int64_t *positions, int64_t max_pos,
                            int64_t T, int Hq, int Hkv, int D, int rotary_dim,
-                           float eps)
+                           float eps, int style)
 {
     if (T < 0 || Hq < 0 || Hkv < 0 || D <= 0 || rotary_dim <= 0 ||
-        (rotary_dim & 1) || rotary_dim > D || D > 4096)
+        (rotary_dim & 1) || rotary_dim > D || D > 4096 || (style != 0 && style != 1))
         return -3;
     if (T == 0 || Hq + Hkv == 0) return 0;
     if (!qkv || !wq || !wk || !cos_sin || !positions) return -1;
@@ -209,14 +211,28 @@ int rn_oracle_qk_norm_rope(uint16_t *qkv, const uint16_t *wq,
             for (int i = 0; i < half; ++i) {
                 double c = (double)cs[i];
                 double s = (double)cs[half + i];
-                o[i] = n[i] * c - n[i + half] * s;
-                o[i + half] = n[i + half] * c + n[i] * s;
+                /* neox pairs (i, i + r/2); GPT-J pairs (2i, 2i + 1) */
+                int a = style ? 2 * i : i;
+                int b = style ? 2 * i + 1 : i + half;
+                o[a] = n[a] * c - n[b] * s;
+                o[b] = n[b] * c + n[a] * s;
             }
             for (int j = rotary_dim; j < D; ++j) o[j] = n[j];
             for (int j = 0; j < D; ++j) head[j] = rn_oracle_double_to_bf16(o[j]);
         }
     }
     return bad ? -3 : 0;
+}
+
+/* The neox form of rn_oracle_qk_norm_rope_ex (style 0). */
+int rn_oracle_qk_norm_rope(uint16_t *qkv, const uint16_t *wq,
+                           const uint16_t *wk, const float *cos_sin,
+                           const int64_t *positions, int64_t max_pos,
+                           int64_t T, int Hq, int Hkv, int D, int rotary_dim,
+                           float eps)
+{
+    return rn_oracle_qk_norm_rope_ex(qkv, wq, wk, cos_sin, positions, max_pos, T, Hq, Hkv, D,
+                                     rotary_dim, eps, 0);
 }
 
 /* ---- L2Norm ------------------------------------------------------------- */

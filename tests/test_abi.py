@@ -109,6 +109,13 @@ def test_add_rmsnorm_checks(lib):
     assert lib.add_rmsnorm_fwd(P, P, P, 1e-6, 4, 64, P + 4096, P + 4096, None) == binding.RN_ERR_ARG
 
 
+def test_l2norm_checks(lib):
+    assert lib.l2norm_fwd(P, 1e-12, 4, 7, P, None) == binding.RN_ERR_SHAPE
+    assert lib.l2norm_fwd(P, 1e-12, 0, 64, P, None) == binding.RN_OK
+    assert lib.l2norm_fwd(None, 1e-12, 4, 64, P, None) == binding.RN_ERR_NULL
+    assert lib.l2norm_fwd(P, 1e-12, 4, 64, MISALIGNED, None) == binding.RN_ERR_ALIGN
+
+
 def test_layernorm_checks(lib):
     assert lib.layernorm_fwd(P, P, None, 1e-5, 4, 7, P, None) == binding.RN_ERR_SHAPE
     assert lib.layernorm_fwd(P, P, None, 1e-5, 0, 64, P, None) == binding.RN_OK

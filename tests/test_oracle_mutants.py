@@ -25,9 +25,9 @@ MUTANTS = {
     "no_weight": ("yr[j] = rn_oracle_double_to_bf16(v * rs * g);", "yr[j] = rn_oracle_double_to_bf16(v * rs + 0.0 * g);"),
     "round_via_float": ("double n = nearbyint(v / q);", "double n = nearbyint((double)(float)v / q);"),
     "ties_away": ("double n = nearbyint(v / q);", "double n = round(v / q);"),
-    "rope_sign_first": ("o[i] = n[i] * c - n[i + half] * s;", "o[i] = n[i] * c + n[i + half] * s;"),
-    "rope_sign_second": ("o[i + half] = n[i + half] * c + n[i] * s;", "o[i + half] = n[i + half] * c - n[i] * s;"),
-    "rope_partner_d_half": ("o[i] = n[i] * c - n[i + half] * s;", "o[i] = n[i] * c - n[i + D / 2] * s;"),
+    "rope_sign_first": ("o[a] = n[a] * c - n[b] * s;", "o[a] = n[a] * c + n[b] * s;"),
+    "rope_sign_second": ("o[b] = n[b] * c + n[a] * s;", "o[b] = n[b] * c - n[a] * s;"),
+    "rope_partner_d_half": ("int b = style ? 2 * i + 1 : i + half;", "int b = style ? 2 * i + 1 : i + D / 2;"),
     "rope_cos_sin_swapped": ("double c = (double)cs[i];\n                double s = (double)cs[half + i];",
                              "double s = (double)cs[i];\n                double c = (double)cs[half + i];"),
     "qk_weights_swapped": ("const uint16_t *w = (h < Hq) ? wq : wk;", "const uint16_t *w = (h < Hq) ? wk : wq;"),
@@ -40,6 +40,8 @@ MUTANTS = {
                           "double f = pow(theta, -1.0 * (double)i / (double)rotary_dim);"),
     "table_sin_first": ("row[i] = (float)cos(a);\n            row[half + i] = (float)sin(a);",
                         "row[i] = (float)sin(a);\n            row[half + i] = (float)cos(a);"),
+    "gptj_partner": ("int b = style ? 2 * i + 1 : i + half;", "int b = style ? 2 * i + 2 - (2 * i + 2) / rotary_dim : i + half;"),
+    "gptj_cos_index": ("int a = style ? 2 * i : i;", "int a = style ? 2 * i + 1 : i;"),
     "l2_norm_squared": ("double nrm = sqrt(ss);", "double nrm = ss;"),
     "l2_eps_added": ("double d = nrm > (double)eps ? nrm : (double)eps;", "double d = nrm + (double)eps;"),
     "add_sum_not_rounded": ("h[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) +",

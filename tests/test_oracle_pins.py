@@ -598,3 +598,52 @@ def test_l2norm_matches_library_normalize():
     ref = torch.nn.functional.normalize(xf, p=2.0, dim=-1, eps=1e-12).numpy()
     want = np.array([[round_bf16(Fraction(float(v))) for v in row] for row in ref], dtype=np.uint16)
     assert np.array_equal(oracle.l2norm(x, 1e-12), want)
+
+
+# ---------------------------------------------------------------------------
+# GPT-J (interleaved) rotary pairing
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D,r", [(16, 16), (16, 8), (128, 64)])
+def test_gptj_quarter_turn_swaps_neighbours(D, r):
+    # cos = 0, sin = 1: o_{2i} = -n_{2i+1}, o_{2i+1} = n_{2i}; the tail passes
+    rng = np.random.default_rng(91)
+    qkv, wq, wk = _layout(1, 2, 1, D, rng)
+    h2 = r // 2
+    table = np.concatenate([np.zeros(h2), np.ones(h2)]).astype(np.float32)[None, :]
+    out = oracle.qk_norm_rope(qkv, wq, wk, table, np.array([0]), 2, 1, D, r, 1e-6, style=1)
+    for h in range(3):
+        n = _norm_only(qkv[0, h * D:(h + 1) * D], wq if h < 2 else wk, 1e-6)
+        o = out[0, h * D:(h + 1) * D]
+        assert np.array_equal(o[0:r:2], _flip(n[1:r:2]))
+        assert np.array_equal(o[1:r:2], n[0:r:2])
+        assert np.array_equal(o[r:], n[r:])
+
+
+def test_gptj_exact_brute_force_and_position_zero():
+    rng = np.random.default_rng(93)
+    for D, r in [(8, 8), (8, 4), (6, 2)]:
+        qkv, wq, wk = _layout(2, 2, 1, D, rng)
+        table = rng.standard_normal((5, r)).astype(np.float32)
+        pos = np.array([3, 0], dtype=np.int64)
+        out = oracle.qk_norm_rope(qkv, wq, wk, table, pos, 2, 1, D, r, 1e-6, style=1)
+        h2 = r // 2
+        for t in range(2):
+            cs = [Fraction(float(v)) for v in table[pos[t]]]
+            for h in range(3):
+                w = wq if h < 2 else wk
+                xs = [bits_to_fraction(v) for v in qkv[t, h * D:(h + 1) * D]]
+                den = dsqrt(sum(v * v for v in xs) / D + f32_to_fraction(1e-6))
+                a = [xs[j] * bits_to_fraction(w[j]) for j in range(D)]
+                o = list(a)
+                for i in range(h2):
+                    o[2 * i] = a[2 * i] * cs[i] - a[2 * i + 1] * cs[h2 + i]
+                    o[2 * i + 1] = a[2 * i + 1] * cs[i] + a[2 * i] * cs[h2 + i]
+                want = [round_bf16(to_dec(v) / den) for v in o]
+                assert list(out[t, h * D:(h + 1) * D]) == want
+    # identity row: GPT-J and neox agree at position 0
+    qkv, wq, wk = _layout(1, 2, 1, 16, rng)
+    table = oracle.rope_cos_sin(1e6, 4, 16)
+    a = oracle.qk_norm_rope(qkv, wq, wk, table, np.array([0]), 2, 1, 16, 16, 1e-6, style=1)
+    b = oracle.qk_norm_rope(qkv, wq, wk, table, np.array([0]), 2, 1, 16, 16, 1e-6, style=0)
+    assert np.array_equal(a, b)
