@@ -15,6 +15,9 @@
  *                     weight and the rotation, store each half once; partial
  *                     rotary still normalises the non-rotary tail.
  *   rope_cos_sin_table  builds the cos/sin table the rotary step reads.
+ *   l2norm_fwd        y = x / max(||x||_2, eps), row by row: one reduction, a
+ *                     scale by the inverse norm ("[Inductor] Codegen Gluon",
+ *                     section 3.2).
  *   layernorm_fwd     y = (x - mean) / sqrt(var + eps) * w + b, row by row
  *                     (biased variance), the same single HBM pass:
  *                     "TorchInductor: from ATen IR to Triton kernel", section
@@ -127,6 +130,18 @@ int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps,
  * current device; RN_ERR_SHAPE / RN_ERR_DEVICE as rmsnorm_fwd would return.
  * Host-only query: launches nothing. */
 int rmsnorm_select_schedule(int64_t M, int64_t N);
+
+/* L2Norm, one HBM pass: y[r, :] = bf16( x[r, :] / max(||x[r, :]||_2, eps) ).
+ * No weight.  Requirements, errors and schedules as rmsnorm_fwd (the same
+ * kernels run it with a unit weight and the L2 scale). */
+int l2norm_fwd(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
+               rn_stream_t stream);
+
+/* l2norm_fwd with an explicit schedule, wait limit and test flags, as
+ * rmsnorm_fwd_sched. */
+int l2norm_fwd_sched(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
+                     int schedule, uint64_t wait_timeout_ns, int debug_flags,
+                     rn_stream_t stream);
 
 /* LayerNorm, one HBM pass:
  *   mean_r = sum_j x[r, j] / N,  var_r = sum_j (x[r, j] - mean_r)^2 / N
@@ -242,6 +257,28 @@ int qk_norm_rope_fwd_sched(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                            int64_t T, int Hq, int Hkv, int D, int rotary_dim,
                            float eps, int schedule, uint64_t wait_timeout_ns,
                            int debug_flags, rn_stream_t stream);
+
+/* Rotary pairing styles for qk_norm_rope_fwd_ex. */
+enum {
+    RN_ROPE_NEOX = 0,  /* pairs (i, i + r/2): the half-split layout (default)   */
+    RN_ROPE_GPTJ = 1   /* pairs (2i, 2i + 1): interleaved neighbours; the same
+                          table row, c = cos_sin[pos, i], s = cos_sin[pos, r/2+i],
+                          rotates pair i: o_{2i} = n_{2i} c - n_{2i+1} s,
+                          o_{2i+1} = n_{2i+1} c + n_{2i} s                      */
+};
+
+/* The general form of the fused Q/K norm + RoPE: every other qk_norm_rope_fwd*
+ * entry point is this one with some arguments fixed.
+ *   rope_style   RN_ROPE_NEOX or RN_ROPE_GPTJ (else RN_ERR_ARG).
+ *   max_pos      0: positions trusted (as qk_norm_rope_fwd); > 0: checked as
+ *                qk_norm_rope_fwd_checked, flagging into *d_err_flag.
+ *   schedule, wait_timeout_ns, debug_flags: as qk_norm_rope_fwd_sched. */
+int qk_norm_rope_fwd_ex(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
+                        const float *cos_sin, const int64_t *positions, int64_t T,
+                        int Hq, int Hkv, int D, int rotary_dim, float eps,
+                        int rope_style, int64_t max_pos, int *d_err_flag,
+                        int schedule, uint64_t wait_timeout_ns, int debug_flags,
+                        rn_stream_t stream);
 
 /* The schedule (RN_QK_*) that qk_norm_rope_fwd picks for T tokens (RN_ERR_SHAPE
  * if T < 0).  When it picks RN_QK_BULK for a layout the ring cannot hold

@@ -6,7 +6,7 @@ tensors into it.  Importing this package does not load the library; the first
 call does, and fails loudly if it is not built.
 """
 from .binding import (  # noqa: F401
-    RN_QK_AUTO, RN_QK_BULK, RN_QK_FOUR_HEADS, RN_QK_HEAD_PER_WARP, RN_QK_PERSISTENT, RN_QK_TWO_HEADS,
+    RN_QK_AUTO, RN_QK_BULK, RN_ROPE_GPTJ, RN_ROPE_NEOX, RN_QK_FOUR_HEADS, RN_QK_HEAD_PER_WARP, RN_QK_PERSISTENT, RN_QK_TWO_HEADS,
     RN_SCHED_AUTO, RN_SCHED_CTA_ROW, RN_SCHED_PERSIST_BULK, RN_SCHED_WARP_ROW,
     RN_STATUS_BAD_POSITION, RN_STATUS_WAIT_TIMEOUT, RowNormError, add_rmsnorm_fwd, device_status, error_string,
-    layernorm_fwd, qk_norm_rope_fwd, qk_norm_rope_fwd_checked, rmsnorm_fwd, rope_cos_sin_table, version)
+    l2norm_fwd, layernorm_fwd, qk_norm_rope_fwd, qk_norm_rope_fwd_checked, qk_norm_rope_fwd_ex, rmsnorm_fwd, rope_cos_sin_table, version)

@@ -42,6 +42,9 @@ RN_QK_FOUR_HEADS = 4
 RN_QK_PERSISTENT = 8
 RN_QK_BULK = 16
 
+RN_ROPE_NEOX = 0
+RN_ROPE_GPTJ = 1
+
 
 class RowNormError(RuntimeError):
     def __init__(self, name: str, code: int):
@@ -80,12 +83,19 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qk_norm_rope_fwd_checked.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
                                                i64, vp, vp]
         L.qk_norm_rope_fwd_checked.restype = i32
+        L.qk_norm_rope_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, i32,
+                                          i64, vp, i32, u64, i32, vp]
+        L.qk_norm_rope_fwd_ex.restype = i32
         L.rope_cos_sin_table.argtypes = [f64, i64, i32, vp, vp]
         L.rope_cos_sin_table.restype = i32
         L.add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
         L.add_rmsnorm_fwd.restype = i32
         L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
         L.add_rmsnorm_fwd_sched.restype = i32
+        L.l2norm_fwd.argtypes = [vp, f32, i64, i64, vp, vp]
+        L.l2norm_fwd.restype = i32
+        L.l2norm_fwd_sched.argtypes = [vp, f32, i64, i64, vp, i32, u64, i32, vp]
+        L.l2norm_fwd_sched.restype = i32
         L.layernorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp]
         L.layernorm_fwd.restype = i32
         L.layernorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, i32, u64, i32, vp]
@@ -160,6 +170,28 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
         rc = L.rmsnorm_fwd_sched(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
                                  schedule, wait_timeout_ns, debug_flags, _stream(stream))
     _check(rc, "rmsnorm_fwd")
+    return y
+
+
+def l2norm_fwd(x: torch.Tensor, eps: float, y: torch.Tensor | None = None, *,
+               schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0, debug_flags: int = 0,
+               stream=None) -> torch.Tensor:
+    """y = x / max(||x||_2, eps) per row of bf16 x [M, N]."""
+    _need(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be [M, N]")
+    y = torch.empty_like(x) if y is None else y
+    _need(y, "y", torch.bfloat16)
+    if y.shape != x.shape:
+        raise ValueError("y must have x's shape")
+    M, N = x.shape
+    L = load()
+    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+        rc = L.l2norm_fwd(x.data_ptr(), eps, M, N, y.data_ptr(), _stream(stream))
+    else:
+        rc = L.l2norm_fwd_sched(x.data_ptr(), eps, M, N, y.data_ptr(), schedule,
+                                wait_timeout_ns, debug_flags, _stream(stream))
+    _check(rc, "l2norm_fwd")
     return y
 
 
@@ -266,6 +298,25 @@ def qk_norm_rope_fwd(qkv: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
                                       rotary_dim, eps, schedule, wait_timeout_ns, debug_flags,
                                       _stream(stream))
     _check(rc, "qk_norm_rope_fwd")
+    return qkv
+
+
+def qk_norm_rope_fwd_ex(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim, eps, *,
+                        rope_style: int = RN_ROPE_NEOX, max_pos: int = 0,
+                        err_flag: torch.Tensor | None = None, schedule: int = RN_QK_AUTO,
+                        wait_timeout_ns: int = 0, debug_flags: int = 0, stream=None):
+    """The general QK entry: rope_style (neox / GPT-J), optional position checks
+    (max_pos > 0 with an int32 CUDA err_flag), schedule and test flags."""
+    T = _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim)
+    ep = None
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32)
+        ep = err_flag.data_ptr()
+    rc = load().qk_norm_rope_fwd_ex(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                    cos_sin.data_ptr(), positions.data_ptr(), T, Hq, Hkv, D,
+                                    rotary_dim, eps, rope_style, int(max_pos), ep, schedule,
+                                    wait_timeout_ns, debug_flags, _stream(stream))
+    _check(rc, "qk_norm_rope_fwd_ex")
     return qkv
 
 

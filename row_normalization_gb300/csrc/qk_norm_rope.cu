@@ -150,7 +150,10 @@ struct QkArgs {
     int *err;         // checked mode: RN_STATUS_BAD_POSITION is OR-ed in here
 };
 
-template <int D, int R, int LPH>
+// STYLE 0: neox pairs (i, i + r/2).  STYLE 1: GPT-J pairs (2i, 2i + 1): the
+// lane's rotary slice is then 2A contiguous elements, de-interleaved into the
+// same (first, second) arrays so the arithmetic is shared.
+template <int D, int R, int LPH, int STYLE>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
     constexpr int H2 = R / 2;
     constexpr int A = H2 / LPH;
@@ -185,8 +188,18 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
 
         float x1[A], x2[A], x3[B > 0 ? B : 1];
         if (ok) {
-            load_bf<A>(head + sub * A, x1);
-            load_bf<A>(head + H2 + sub * A, x2);
+            if constexpr (STYLE == 0) {
+                load_bf<A>(head + sub * A, x1);
+                load_bf<A>(head + H2 + sub * A, x2);
+            } else {
+                float xr[2 * A];
+                load_bf<2 * A>(head + sub * 2 * A, xr);
+#pragma unroll
+                for (int i = 0; i < A; ++i) {
+                    x1[i] = xr[2 * i];
+                    x2[i] = xr[2 * i + 1];
+                }
+            }
             if constexpr (B > 0) load_bf<B>(head + R + sub * B, x3);
         } else {
 #pragma unroll
@@ -211,8 +224,18 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
 
         const uint16_t *wp = (h < static_cast<uint32_t>(a.Hq)) ? a.wq : a.wk;
         float w1[A], w2[A];
-        load_bf<A>(wp + sub * A, w1);
-        load_bf<A>(wp + H2 + sub * A, w2);
+        if constexpr (STYLE == 0) {
+            load_bf<A>(wp + sub * A, w1);
+            load_bf<A>(wp + H2 + sub * A, w2);
+        } else {
+            float wr[2 * A];
+            load_bf<2 * A>(wp + sub * 2 * A, wr);
+#pragma unroll
+            for (int i = 0; i < A; ++i) {
+                w1[i] = wr[2 * i];
+                w2[i] = wr[2 * i + 1];
+            }
+        }
 
         float o1[A], o2[A];
 #pragma unroll
@@ -223,8 +246,18 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
             o2[i] = n2 * c[i] + n1 * s[i];
         }
         if (ok) {
-            store_bf<A>(head + sub * A, o1);
-            store_bf<A>(head + H2 + sub * A, o2);
+            if constexpr (STYLE == 0) {
+                store_bf<A>(head + sub * A, o1);
+                store_bf<A>(head + H2 + sub * A, o2);
+            } else {
+                float orr[2 * A];
+#pragma unroll
+                for (int i = 0; i < A; ++i) {
+                    orr[2 * i] = o1[i];
+                    orr[2 * i + 1] = o2[i];
+                }
+                store_bf<2 * A>(head + sub * 2 * A, orr);
+            }
         }
         if constexpr (B > 0) {
             float w3[B];
@@ -353,7 +386,53 @@ __device__ __forceinline__ void qk_rotate_slice(const uint32_t (&x1)[A2], const 
     }
 }
 
-template <int D, int R>
+// GPT-J slice: the lane's 2A contiguous rotary elements arrive as two arrays of
+// A/2 words (x1 then x2); every word is one pair (2j, 2j + 1) and rotates by
+// (c_j, s_j): (e, o) -> (e c - o s, o c + e s).  Same signature as
+// qk_rotate_slice, so the caller picks by style.
+__device__ __forceinline__ uint32_t gptj_pair(uint32_t x, uint32_t w, float2 r2, float c, float s) {
+    const float2 n = __fmul2_rn(__fmul2_rn(bf2f(x), r2), bf2f(w));
+    const float2 t = __fmul2_rn(n, make_float2(c, c));
+    return pack_f2(__ffma2_rn(make_float2(n.y, n.x), make_float2(-s, s), t));
+}
+
+template <int A2, int B2, bool TAIL>
+__device__ __forceinline__ void qk_rotate_slice_gptj(const uint32_t (&x1)[A2],
+                                                     const uint32_t (&x2)[A2],
+                                                     const uint32_t (&x3)[B2],
+                                                     const uint32_t (&w1)[A2],
+                                                     const uint32_t (&w2)[A2],
+                                                     const uint32_t (&w3)[B2],
+                                                     const float (&c)[2 * A2],
+                                                     const float (&sn)[2 * A2], float rstd,
+                                                     uint32_t (&o1)[A2], uint32_t (&o2)[A2],
+                                                     uint32_t (&o3)[B2]) {
+    const float2 r2 = make_float2(rstd, rstd);
+#pragma unroll
+    for (int i = 0; i < A2; ++i) {
+        o1[i] = gptj_pair(x1[i], w1[i], r2, c[i], sn[i]);
+        o2[i] = gptj_pair(x2[i], w2[i], r2, c[A2 + i], sn[A2 + i]);
+    }
+    if constexpr (TAIL) {
+#pragma unroll
+        for (int i = 0; i < B2; ++i) o3[i] = pack_f2(__fmul2_rn(__fmul2_rn(bf2f(x3[i]), r2), bf2f(w3[i])));
+    }
+}
+
+template <int STYLE, int A2, int B2, bool TAIL>
+__device__ __forceinline__ void qk_rotate(const uint32_t (&x1)[A2], const uint32_t (&x2)[A2],
+                                          const uint32_t (&x3)[B2], const uint32_t (&w1)[A2],
+                                          const uint32_t (&w2)[A2], const uint32_t (&w3)[B2],
+                                          const float (&c)[2 * A2], const float (&sn)[2 * A2],
+                                          float rstd, uint32_t (&o1)[A2], uint32_t (&o2)[A2],
+                                          uint32_t (&o3)[B2]) {
+    if constexpr (STYLE == 0)
+        qk_rotate_slice<A2, B2, TAIL>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
+    else
+        qk_rotate_slice_gptj<A2, B2, TAIL>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
+}
+
+template <int D, int R, int STYLE>
 __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
     qk_persistent_bulk_kernel(const QkBulkArgs args) {
     constexpr int LPH = 8;
@@ -478,11 +557,15 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
     // ---- consumer warps ----
     const int sub = lane % LPH;
     const int grp = lane / LPH;
+    // Element offsets of the lane's two rotary pieces: neox takes A elements
+    // from each half, GPT-J 2A contiguous elements (split in two A-runs).
+    const int off1 = STYLE == 0 ? sub * A : sub * 2 * A;
+    const int off2 = STYLE == 0 ? H2 + sub * A : sub * 2 * A + A;
     uint32_t wq1[A2], wq2[A2], wq3[B2], wk1[A2], wk2[A2], wk3[B2];
-    load_words<A>(a.wq + sub * A, wq1);
-    load_words<A>(a.wq + H2 + sub * A, wq2);
-    load_words<A>(a.wk + sub * A, wk1);
-    load_words<A>(a.wk + H2 + sub * A, wk2);
+    load_words<A>(a.wq + off1, wq1);
+    load_words<A>(a.wq + off2, wq2);
+    load_words<A>(a.wk + off1, wk1);
+    load_words<A>(a.wk + off2, wk2);
     if constexpr (B > 0) {
         load_words<B>(a.wq + R + sub * B, wq3);
         load_words<B>(a.wk + R + sub * B, wk3);
@@ -518,8 +601,8 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
             const uint16_t *xs =
                 reinterpret_cast<const uint16_t *>(st + ts * tok_bytes) + static_cast<size_t>(h) * D;
             uint32_t x1[A2], x2[A2], x3[B2];
-            load_words<A>(xs + sub * A, x1);
-            load_words<A>(xs + H2 + sub * A, x2);
+            load_words<A>(xs + off1, x1);
+            load_words<A>(xs + off2, x2);
             if constexpr (B > 0) load_words<B>(xs + R + sub * B, x3);
             const float *cs = cs_base + ts * R;
             float c[A], sn[A];
@@ -553,9 +636,9 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
             // The quad's heads are usually all query or all key heads: pick the
             // weights once for the warp instead of element by element.
             if (__all_sync(0xffffffffu, isq || !act)) {
-                qk_rotate_slice<A2, B2, (B > 0)>(x1, x2, x3, wq1, wq2, wq3, c, sn, rstd, o1, o2, o3);
+                qk_rotate<STYLE, A2, B2, (B > 0)>(x1, x2, x3, wq1, wq2, wq3, c, sn, rstd, o1, o2, o3);
             } else if (__all_sync(0xffffffffu, !isq || !act)) {
-                qk_rotate_slice<A2, B2, (B > 0)>(x1, x2, x3, wk1, wk2, wk3, c, sn, rstd, o1, o2, o3);
+                qk_rotate<STYLE, A2, B2, (B > 0)>(x1, x2, x3, wk1, wk2, wk3, c, sn, rstd, o1, o2, o3);
             } else {
                 uint32_t w1[A2], w2[A2], w3[B2];
 #pragma unroll
@@ -565,12 +648,12 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < B2; ++i) w3[i] = isq ? wq3[i] : wk3[i];
-                qk_rotate_slice<A2, B2, (B > 0)>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
+                qk_rotate<STYLE, A2, B2, (B > 0)>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
             }
             if (good) {
                 uint16_t *head = a.qkv + (r0 + ts) * W + static_cast<int64_t>(h) * D;
-                store_words<A>(head + sub * A, o1);
-                store_words<A>(head + H2 + sub * A, o2);
+                store_words<A>(head + off1, o1);
+                store_words<A>(head + off2, o2);
                 if constexpr (B > 0) store_words<B>(head + R + sub * B, o3);
             }
         }
@@ -600,7 +683,7 @@ __global__ void rope_table_kernel(double theta, int64_t max_pos, int r, float *o
 
 // ---- host side ----------------------------------------------------------------------
 
-template <int D, int R, int LPH>
+template <int D, int R, int LPH, int STYLE>
 static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const DeviceInfo &dev) {
     constexpr int HPW = 32 / LPH;
     constexpr int kThreads = 256;
@@ -612,29 +695,29 @@ static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const De
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7fffffffULL) blocks = 0x7fffffffULL;
-    qk_norm_rope_kernel<D, R, LPH><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a);
+    qk_norm_rope_kernel<D, R, LPH, STYLE><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a);
     return launch_status();
 }
 
 // Largest lanes-per-head <= the request that tiles both rotary halves and
 // the tail of this (D, rotary_dim); 8 always does.
-template <int D, int R>
+template <int D, int R, int STYLE>
 static int launch_qk_lph(const QkArgs &a, int lph, bool persistent, cudaStream_t st,
                          const DeviceInfo &dev) {
     constexpr int H2 = R / 2;
     if constexpr (H2 % 32 == 0 && (D - R) % 32 == 0) {
-        if (lph >= 32) return launch_qk<D, R, 32>(a, persistent, st, dev);
+        if (lph >= 32) return launch_qk<D, R, 32, STYLE>(a, persistent, st, dev);
     }
     if constexpr (H2 % 16 == 0 && (D - R) % 16 == 0) {
-        if (lph >= 16) return launch_qk<D, R, 16>(a, persistent, st, dev);
+        if (lph >= 16) return launch_qk<D, R, 16, STYLE>(a, persistent, st, dev);
     }
     if constexpr (H2 % 8 == 0 && (D - R) % 8 == 0) {
-        return launch_qk<D, R, 8>(a, persistent, st, dev);
+        return launch_qk<D, R, 8, STYLE>(a, persistent, st, dev);
     }
     return RN_ERR_SHAPE;
 }
 
-template <int D, int R>
+template <int D, int R, int STYLE>
 static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &dev,
                           uint64_t timeout_ns, int debug_flags) {
     static std::atomic<int> attr_done[kMaxDevices];
@@ -655,7 +738,7 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     const int dev_idx = current_device_index();
     if (dev_idx < 0 || dev_idx >= kMaxDevices) return RN_ERR_DEVICE;
     if (!attr_done[dev_idx].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(qk_persistent_bulk_kernel<D, R>,
+        if (cudaFuncSetAttribute(qk_persistent_bulk_kernel<D, R, STYLE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_cap) != cudaSuccess) {
             cudaGetLastError();
@@ -667,7 +750,7 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     if (grid > a.T) grid = a.T;
     const uint64_t inv_h = ((1ull << 32) + H - 1) / H;
     QkBulkArgs b{a, tps, stages, debug_flags & 1, inv_h, timeout_ns ? timeout_ns : 2000000000ull};
-    qk_persistent_bulk_kernel<D, R>
+    qk_persistent_bulk_kernel<D, R, STYLE>
         <<<static_cast<unsigned>(grid), qk_bulk_consumers<D>() + 32, smem, st>>>(b);
     return launch_status();
 }
@@ -683,10 +766,38 @@ static int auto_qk_schedule(int64_t T) {
     return RN_QK_BULK;
 }
 
+template <int STYLE>
+static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic, int lph,
+                     bool persistent, cudaStream_t st, const DeviceInfo &dev,
+                     uint64_t timeout_ns, int debug_flags) {
+    if (schedule == RN_QK_BULK) {
+        int rc = RN_ERR_SHAPE;
+#define RN_QK_BULK_GO(D_, R_)                                                           \
+    if (D == (D_) && r == (R_))                                                         \
+        rc = launch_qk_bulk<D_, R_, STYLE>(a, st, dev, timeout_ns, debug_flags);
+        // (64, 16) leaves one element per lane per half: the warp schedules serve it.
+        RN_QK_BULK_GO(64, 64) RN_QK_BULK_GO(64, 32)
+        RN_QK_BULK_GO(128, 128) RN_QK_BULK_GO(128, 64) RN_QK_BULK_GO(128, 32)
+        RN_QK_BULK_GO(256, 256) RN_QK_BULK_GO(256, 128) RN_QK_BULK_GO(256, 64)
+#undef RN_QK_BULK_GO
+        if (rc != RN_ERR_SHAPE || !automatic) return rc;
+        persistent = true;  // a token too wide for the ring: the warp grid serves it
+    }
+#define RN_QK_GO(D_, R_)                                                               \
+    if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_, STYLE>(a, lph, persistent, st, dev);
+    RN_QK_GO(64, 64) RN_QK_GO(64, 32) RN_QK_GO(64, 16)
+    RN_QK_GO(128, 128) RN_QK_GO(128, 64) RN_QK_GO(128, 32)
+    RN_QK_GO(256, 256) RN_QK_GO(256, 128) RN_QK_GO(256, 64)
+#undef RN_QK_GO
+    return RN_ERR_SHAPE;
+}
+
 static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                        const float *cos_sin, const int64_t *positions, int64_t T, int Hq,
                        int Hkv, int D, int rotary_dim, float eps, int64_t max_pos, int *err,
-                       int schedule, uint64_t timeout_ns, int debug_flags, rn_stream_t stream) {
+                       int schedule, uint64_t timeout_ns, int debug_flags, rn_stream_t stream,
+                       int style = RN_ROPE_NEOX) {
+    if (style != RN_ROPE_NEOX && style != RN_ROPE_GPTJ) return RN_ERR_ARG;
     if (T < 0 || Hq < 0 || Hkv < 0) return RN_ERR_SHAPE;
     if (D != 64 && D != 128 && D != 256) return RN_ERR_SHAPE;
     if (rotary_dim != D && rotary_dim != D / 2 && rotary_dim != D / 4) return RN_ERR_SHAPE;
@@ -719,26 +830,11 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
     QkArgs a{reinterpret_cast<uint16_t *>(qkv), wq, wk, cos_sin, positions, T, Hq, Hkv,
              eps, max_pos, err};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int r = rotary_dim;
-    if (schedule == RN_QK_BULK) {
-        int rc = RN_ERR_SHAPE;
-#define RN_QK_BULK_GO(D_, R_) \
-    if (D == (D_) && r == (R_)) rc = launch_qk_bulk<D_, R_>(a, st, *dev, timeout_ns, debug_flags);
-        // (64, 16) leaves one element per lane per half: the warp schedules serve it.
-        RN_QK_BULK_GO(64, 64) RN_QK_BULK_GO(64, 32)
-        RN_QK_BULK_GO(128, 128) RN_QK_BULK_GO(128, 64) RN_QK_BULK_GO(128, 32)
-        RN_QK_BULK_GO(256, 256) RN_QK_BULK_GO(256, 128) RN_QK_BULK_GO(256, 64)
-#undef RN_QK_BULK_GO
-        if (rc != RN_ERR_SHAPE || !automatic) return rc;
-        persistent = true;  // a token too wide for the ring: the warp grid serves it
-    }
-#define RN_QK_GO(D_, R_)                                                               \
-    if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_>(a, lph, persistent, st, *dev);
-    RN_QK_GO(64, 64) RN_QK_GO(64, 32) RN_QK_GO(64, 16)
-    RN_QK_GO(128, 128) RN_QK_GO(128, 64) RN_QK_GO(128, 32)
-    RN_QK_GO(256, 256) RN_QK_GO(256, 128) RN_QK_GO(256, 64)
-#undef RN_QK_GO
-    return RN_ERR_SHAPE;
+    if (style == RN_ROPE_GPTJ)
+        return qk_launch<1>(a, D, rotary_dim, schedule, automatic, lph, persistent, st, *dev,
+                            timeout_ns, debug_flags);
+    return qk_launch<0>(a, D, rotary_dim, schedule, automatic, lph, persistent, st, *dev,
+                        timeout_ns, debug_flags);
 }
 
 int qk_status(unsigned int *out, int clear) {
@@ -785,6 +881,18 @@ int qk_norm_rope_fwd_checked(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
     if (!d_err_flag && T > 0 && Hq + Hkv > 0) return RN_ERR_NULL;
     return rn::qk_dispatch(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
                            max_pos, d_err_flag, RN_QK_AUTO, 0, 0, stream);
+}
+
+int qk_norm_rope_fwd_ex(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
+                        const float *cos_sin, const int64_t *positions, int64_t T, int Hq,
+                        int Hkv, int D, int rotary_dim, float eps, int rope_style,
+                        int64_t max_pos, int *d_err_flag, int schedule,
+                        uint64_t wait_timeout_ns, int debug_flags, rn_stream_t stream) {
+    if (max_pos < 0) return RN_ERR_SHAPE;
+    if (max_pos > 0 && !d_err_flag && T > 0 && Hq + Hkv > 0) return RN_ERR_NULL;
+    return rn::qk_dispatch(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
+                           max_pos, d_err_flag, schedule, wait_timeout_ns, debug_flags, stream,
+                           rope_style);
 }
 
 int qk_norm_rope_select_schedule(int64_t T) {

@@ -104,6 +104,18 @@ __device__ __forceinline__ float row_rstd(float ss, int N, float eps) {
     return __frsqrt_rn(ss / static_cast<float>(N) + eps);
 }
 
+// Per-row scale: RMSNorm's 1/sqrt(ss/N + eps), or with `l2` the L2Norm's
+// 1/max(sqrt(ss), eps) (a correctly rounded rsqrt when the norm exceeds eps).
+__device__ __forceinline__ float row_scale(float ss, int N, float eps, int l2) {
+    if (!l2) return row_rstd(ss, N, eps);
+    return sqrtf(ss) > eps ? __frsqrt_rn(ss) : 1.0f / eps;
+}
+
+// Weight chunk, or eight ones (bf16 1.0 = 0x3F80) when there is no weight.
+__device__ __forceinline__ uint4 weight16(const uint16_t *w, int c) {
+    return w ? ld_ro16(w + 8 * c) : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+}
+
 // ---------------------------------------------------------------------------
 // warp_rows: one warp per row; lane l holds 16-byte chunks l, l+32, ...
 // ---------------------------------------------------------------------------
@@ -114,7 +126,8 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
                                                             uint16_t *y, const uint16_t *r,
-                                                            uint16_t *h_out, const uint16_t *b) {
+                                                            uint16_t *h_out, const uint16_t *b,
+                                                            int l2) {
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int cpr = N >> 3;
@@ -158,11 +171,11 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
 #pragma unroll
             for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
             ss = warp_sum(ss);
-            const float rstd = row_rstd(ss, N, eps);
+            const float rstd = row_scale(ss, N, eps, l2);
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
-                if (c < cpr) st16(yr + 8 * c, scale8(v[i], ld_ro16(w + 8 * c), rstd));
+                if (c < cpr) st16(yr + 8 * c, scale8(v[i], weight16(w, c), rstd));
             }
         }
     }
@@ -176,7 +189,8 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
                                                             uint16_t *y, const uint16_t *r,
-                                                            uint16_t *h_out, const uint16_t *b) {
+                                                            uint16_t *h_out, const uint16_t *b,
+                                                            int l2) {
     __shared__ float red[2][32];
     __shared__ float red2[2][32];  // LayerNorm's second reduction
     const int tid = threadIdx.x;
@@ -241,14 +255,14 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
         __syncthreads();
         float tot = 0.f;
         for (int k = 0; k < nw; ++k) tot += red[par][k];
-        const float rstd = row_rstd(tot, N, eps);
+        const float rstd = row_scale(tot, N, eps, l2);
         if constexpr (MAXT < 1024) {
             // issue every weight load before the first store
             uint4 wv[VPT];
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
-                if (c < cpr) wv[i] = ld_ro16(w + 8 * c);
+                if (c < cpr) wv[i] = weight16(w, c);
             }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
@@ -260,7 +274,7 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
-                if (c < cpr) st16(yr + 8 * c, scale8(v[i], ld_ro16(w + 8 * c), rstd));
+                if (c < cpr) st16(yr + 8 * c, scale8(v[i], weight16(w, c), rstd));
             }
         }
         // red[par] is rewritten two rows later, after the next barrier: safe.
@@ -277,6 +291,7 @@ struct BulkArgs {
     const uint16_t *r;  // residual (fused add) or nullptr
     uint16_t *h;        // x + r output (fused add) or nullptr
     const uint16_t *b;  // LayerNorm bias or nullptr
+    int l2;             // L2Norm scale instead of RMSNorm's (w may then be null)
     int64_t M;
     int N;
     float eps;
@@ -382,7 +397,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
     const int tid = threadIdx.x;
     uint4 wv[VPR];
 #pragma unroll
-    for (int j = 0; j < VPR; ++j) wv[j] = ld_ro16(a.w + 8 * (tid + j * NT));
+    for (int j = 0; j < VPR; ++j) wv[j] = weight16(a.w, tid + j * NT);
     uint4 bv[LN ? VPR : 1];  // LayerNorm bias, held like the weights
     if constexpr (LN) {
 #pragma unroll
@@ -521,7 +536,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
             if (rr < rows) {
                 float tot = 0.f;
                 for (int q = 0; q < NW; ++q) tot += rb[rr * 32 + q];
-                const float rstd = row_rstd(tot, N, a.eps);
+                const float rstd = row_scale(tot, N, a.eps, a.l2);
                 uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
@@ -547,6 +562,7 @@ struct RowJob {
     const uint16_t *r;
     uint16_t *h;
     const uint16_t *b;  // LayerNorm bias (may be null)
+    int l2;             // L2Norm instead of RMSNorm (w may be null: unit weights)
 };
 
 template <bool ADD, bool LN>
@@ -558,7 +574,7 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
 #define RN_WARP(V) \
     rms_warp_rows_kernel<V, ADD, LN><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, \
-                                                                 j.h, j.b)
+                                                                 j.h, j.b, j.l2)
     if (cpr <= 32)
         RN_WARP(1);
     else if (cpr <= 64)
@@ -586,7 +602,7 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
     };
 #define RN_CTA(V, T)                                                                      \
     rms_cta_rows_kernel<V, T, ADD, LN><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
-                                                                     j.y, j.r, j.h, j.b)
+                                                                     j.y, j.r, j.h, j.b, j.l2)
     if (cpr <= 512)
         RN_CTA(1, 512);
     else if (cpr <= 1024)
@@ -696,7 +712,7 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN);
     int64_t grid = static_cast<int64_t>(dev.sm_count) * ctas_per_sm;
     if (grid > j.M) grid = j.M;
-    BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.M, N, j.eps, stages, debug_flags & 1,
+    BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.l2, j.M, N, j.eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
     const int g = static_cast<int>(grid);
     switch (N) {
@@ -755,7 +771,19 @@ static int rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, float eps, int64
     if (M == 0) return RN_OK;
     if (!x || !w || !y) return RN_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return RN_ERR_ALIGN;
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, nullptr};
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, nullptr, 0};
+    return rows_dispatch<false, false>(j, schedule, timeout_ns, debug_flags, stream);
+}
+
+static int l2norm_dispatch(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
+                           int schedule, uint64_t timeout_ns, int debug_flags,
+                           rn_stream_t stream) {
+    const int rc = check_rows(M, N);
+    if (rc != RN_OK) return rc;
+    if (M == 0) return RN_OK;
+    if (!x || !y) return RN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(y)) return RN_ERR_ALIGN;
+    const RowJob j{x, nullptr, eps, M, static_cast<int>(N), y, nullptr, nullptr, nullptr, 1};
     return rows_dispatch<false, false>(j, schedule, timeout_ns, debug_flags, stream);
 }
 
@@ -769,7 +797,7 @@ static int add_rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *res, const rn_b
     if (!aligned16(x) || !aligned16(res) || !aligned16(w) || !aligned16(h) || !aligned16(y))
         return RN_ERR_ALIGN;
     if (h == y) return RN_ERR_ARG;  // two different outputs
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, res, h, nullptr};
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, res, h, nullptr, 0};
     return rows_dispatch<true, false>(j, schedule, timeout_ns, debug_flags, stream);
 }
 
@@ -782,7 +810,7 @@ static int layernorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 
     if (!x || !w || !y) return RN_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (b && !aligned16(b)))
         return RN_ERR_ALIGN;
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, b};
+    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, b, 0};
     return rows_dispatch<false, true>(j, schedule, timeout_ns, debug_flags, stream);
 }
 
@@ -807,6 +835,17 @@ int rmsnorm_select_schedule(int64_t M, int64_t N) {
     const rn::DeviceInfo *dev = rn::current_device_info();
     if (!dev) return RN_ERR_DEVICE;
     return rn::auto_schedule(M, static_cast<int>(N), false, false, *dev);
+}
+
+int l2norm_fwd(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
+               rn_stream_t stream) {
+    return rn::l2norm_dispatch(x, eps, M, N, y, RN_SCHED_AUTO, 0, 0, stream);
+}
+
+int l2norm_fwd_sched(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
+                     int schedule, uint64_t wait_timeout_ns, int debug_flags,
+                     rn_stream_t stream) {
+    return rn::l2norm_dispatch(x, eps, M, N, y, schedule, wait_timeout_ns, debug_flags, stream);
 }
 
 int layernorm_fwd(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps, int64_t M,

@@ -124,6 +124,13 @@ def test_layernorm_checks(lib):
     assert lib.layernorm_fwd_sched(P, P, None, 1e-5, 4, 64, P, 7, 0, 0, None) == binding.RN_ERR_ARG
 
 
+def test_qk_ex_checks(lib):
+    # unknown rope style, negative max_pos, checked mode without a flag pointer
+    assert lib.qk_norm_rope_fwd_ex(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 2, 0, None, 0, 0, 0, None) == binding.RN_ERR_ARG
+    assert lib.qk_norm_rope_fwd_ex(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 1, -1, None, 0, 0, 0, None) == binding.RN_ERR_SHAPE
+    assert lib.qk_norm_rope_fwd_ex(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 1, 16, None, 0, 0, 0, None) == binding.RN_ERR_NULL
+
+
 def test_table_checks(lib):
     assert lib.rope_cos_sin_table(1e6, 16, 7, P, None) == binding.RN_ERR_SHAPE
     assert lib.rope_cos_sin_table(-1.0, 16, 8, P, None) == binding.RN_ERR_SHAPE

@@ -31,18 +31,25 @@ def _gpu():
 
 
 def run_case(T, Hq, Hkv, D, r, *, positions="arange", max_pos=None, theta=1e6, eps=1e-6,
-             schedule=binding.RN_QK_AUTO, device_inputs=False, seed=0, debug_flags=0):
+             schedule=binding.RN_QK_AUTO, device_inputs=False, seed=0, debug_flags=0,
+             style=binding.RN_ROPE_NEOX):
     max_pos = max_pos or max(T, 1)
     qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions=positions, max_pos=max_pos,
                                   device="cuda" if device_inputs else "cpu", seed=seed)
     table = oracle_table(theta, max_pos, r)
     want = oracle.qk_norm_rope(bf16_bits(qkv), bf16_bits(wq), bf16_bits(wk), table,
-                               pos.cpu().numpy(), Hq, Hkv, D, r, eps)
+                               pos.cpu().numpy(), Hq, Hkv, D, r, eps, style=style)
     pad = 128
     buf, q = padded_empty(tuple(qkv.shape), torch.bfloat16, pad, 0x7FC3)
     q.copy_(qkv)
-    binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(), pos.cuda(),
-                             Hq, Hkv, D, r, eps, schedule=schedule, debug_flags=debug_flags)
+    if style == binding.RN_ROPE_NEOX:
+        binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(),
+                                 pos.cuda(), Hq, Hkv, D, r, eps, schedule=schedule,
+                                 debug_flags=debug_flags)
+    else:
+        binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(),
+                                    pos.cuda(), Hq, Hkv, D, r, eps, rope_style=style,
+                                    schedule=schedule, debug_flags=debug_flags)
     torch.cuda.synchronize()
     got = bf16_bits(q)
     assert canary_intact(buf, pad, 0x7FC3), "write outside qkv"
@@ -206,3 +213,51 @@ def test_positions_view_at_8_byte_offset(schedule):
     binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(), pos_view,
                              Hq, Hkv, D, r, 1e-6, schedule=schedule)
     assert_parity(bf16_bits(q), want, f"offset positions sched={schedule}")
+
+
+# ---------------------------------------------------------------------------
+# GPT-J (interleaved) rotary pairing
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("schedule", QK_SCHEDULES)
+@pytest.mark.parametrize("D,r", LAYOUTS)
+def test_gptj_layouts_every_schedule(D, r, schedule):
+    if schedule == binding.RN_QK_BULK and (D, r) == (64, 16):
+        return  # the ring does not take this layout (warp schedules do)
+    got, want = run_case(5, 4, 2, D, r, positions="uniform", max_pos=97, schedule=schedule,
+                         seed=D + r + 1, style=binding.RN_ROPE_GPTJ)
+    assert_parity(got, want, f"gptj D={D} r={r} sched={schedule}")
+
+
+@pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_FOUR_HEADS,
+                                      binding.RN_QK_BULK])
+@pytest.mark.parametrize("r", [128, 64])
+def test_gptj_many_tokens_full_compare(r, schedule):
+    got, want = run_case(4096, 32, 8, 128, r, positions="uniform", max_pos=131072,
+                         device_inputs=True, seed=3, schedule=schedule,
+                         style=binding.RN_ROPE_GPTJ)
+    assert_parity(got, want, f"gptj T=4096 r={r} sched={schedule}")
+
+
+def test_gptj_checked_positions():
+    T, Hq, Hkv, D, r = 3000, 4, 2, 128, 64
+    max_pos = 64
+    qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions="uniform", max_pos=max_pos, seed=12)
+    pos[5] = -3
+    pos[2222] = max_pos
+    table = oracle_table(1e6, max_pos, r)
+    good = pos.clone()
+    good[[5, 2222]] = 0
+    want = oracle.qk_norm_rope(bf16_bits(qkv), bf16_bits(wq), bf16_bits(wk), table,
+                               good.numpy(), Hq, Hkv, D, r, 1e-6, style=1).reshape(T, -1)
+    q = qkv.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(),
+                                pos.cuda(), Hq, Hkv, D, r, 1e-6, rope_style=binding.RN_ROPE_GPTJ,
+                                max_pos=max_pos, err_flag=err)
+    got = bf16_bits(q).reshape(T, -1)
+    assert int(err.item()) & binding.RN_STATUS_BAD_POSITION
+    src = bf16_bits(qkv).reshape(T, -1)
+    assert np.array_equal(got[[5, 2222]], src[[5, 2222]])
+    ok_rows = [t for t in range(T) if t not in (5, 2222)]
+    assert_parity(got[ok_rows], want[ok_rows], "gptj checked")
