@@ -311,8 +311,16 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, i
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
+// NT <= 0 is the generic form: the consumer count comes from the launch
+// (blockDim.x - 32, a multiple of 32; at most 256 for NT == 0, 512 for
+// NT == -1) and chunks past the end of a row (any N % 8 == 0) are masked.
+template <int VPR, int R, int NT>
+constexpr int bulk_max_threads() { return NT > 0 ? NT + 32 : (NT == 0 ? 288 : 544); }
+
 template <int VPR, int R, int NT, bool ADD, bool LN>
-__global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const BulkArgs a) {
+__global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
+    rms_persistent_bulk_kernel(const BulkArgs a) {
+    constexpr bool GENERIC = NT <= 0;
     static_assert(!(ADD && LN), "the fused add is an RMSNorm prologue");
     constexpr int NIN = ADD ? 2 : 1;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -329,7 +337,11 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
     // polled inside waits so nobody waits out a full timeout needlessly.
     volatile int *flags = reinterpret_cast<volatile int *>(red + 4 * R * 32);
 
-    constexpr int NW = NT / 32;
+    const int nt = GENERIC ? static_cast<int>(blockDim.x) - 32 : NT;
+    const int NW = nt / 32;
+    const int cpr = N >> 3;
+    // chunk j of this thread lies inside the row (always, for exact covers)
+    auto live = [&](int tid_, int j) { return !GENERIC || tid_ + j * nt < cpr; };
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -397,11 +409,13 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
     const int tid = threadIdx.x;
     uint4 wv[VPR];
 #pragma unroll
-    for (int j = 0; j < VPR; ++j) wv[j] = weight16(a.w, tid + j * NT);
+    for (int j = 0; j < VPR; ++j)
+        wv[j] = live(tid, j) ? weight16(a.w, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
     uint4 bv[LN ? VPR : 1];  // LayerNorm bias, held like the weights
     if constexpr (LN) {
 #pragma unroll
-        for (int j = 0; j < VPR; ++j) bv[j] = bias16(a.b, tid + j * NT);
+        for (int j = 0; j < VPR; ++j)
+            bv[j] = live(tid, j) ? bias16(a.b, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
     }
 
     for (int64_t k = 0; k < n_units; ++k) {
@@ -429,8 +443,9 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
         for (int rr = 0; rr < R; ++rr)
 #pragma unroll
             for (int j = 0; j < VPR; ++j)
-                xv[rr][j] = ok ? ld_shared16(st + rr * row_bytes + 16u * (tid + j * NT))
-                               : make_uint4(0u, 0u, 0u, 0u);
+                xv[rr][j] = (ok && live(tid, j))
+                                ? ld_shared16(st + rr * row_bytes + 16u * (tid + j * nt))
+                                : make_uint4(0u, 0u, 0u, 0u);
         if constexpr (ADD) {
             // h = x + r, stored at once; the rest of the row works on h
 #pragma unroll
@@ -438,15 +453,16 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
                     xv[rr][j] = add8(xv[rr][j],
-                                     ok ? ld_shared16(st + (R + rr) * row_bytes + 16u * (tid + j * NT))
-                                        : make_uint4(0u, 0u, 0u, 0u));
+                                     (ok && live(tid, j))
+                                         ? ld_shared16(st + (R + rr) * row_bytes + 16u * (tid + j * nt))
+                                         : make_uint4(0u, 0u, 0u, 0u));
             if (ok) {
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr)
                     if (rr < rows)
 #pragma unroll
                         for (int j = 0; j < VPR; ++j)
-                            st16(a.h + (r0 + rr) * N + 8 * (tid + j * NT), xv[rr][j]);
+                            if (live(tid, j)) st16(a.h + (r0 + rr) * N + 8 * (tid + j * nt), xv[rr][j]);
             }
         }
         __syncwarp();
@@ -476,7 +492,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr) rb1[rr * 32 + warp] = s1[rr];
             }
-            named_bar_sync(1, NT);
+            named_bar_sync(1, nt);
             if (flags[k & 1]) break;  // same decision in every consumer warp
             float mean[R];
 #pragma unroll
@@ -486,14 +502,15 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
                 mean[rr] = t / static_cast<float>(N);
                 float acc = 0.f;
 #pragma unroll
-                for (int j = 0; j < VPR; ++j) acc += sqdev8(xv[rr][j], mean[rr]);
+                for (int j = 0; j < VPR; ++j)
+                    if (live(tid, j)) acc += sqdev8(xv[rr][j], mean[rr]);
                 s1[rr] = warp_sum(acc);
             }
             if (lane == 0) {
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr) rb2[rr * 32 + warp] = s1[rr];
             }
-            named_bar_sync(1, NT);
+            named_bar_sync(1, nt);
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
                 if (rr < rows) {
@@ -503,8 +520,8 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
                     uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
-                        st16(yr + 8 * (tid + j * NT),
-                             ln8(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
+                        if (live(tid, j))
+                            st16(yr + 8 * (tid + j * nt), ln8(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
                 }
             }
             continue;
@@ -529,7 +546,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) rb[rr * 32 + warp] = ss[rr];
         }
-        named_bar_sync(1, NT);
+        named_bar_sync(1, nt);
         if (flags[k & 1]) break;  // same decision in every consumer warp
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
@@ -540,7 +557,7 @@ __global__ void __launch_bounds__(NT + 32, 1) rms_persistent_bulk_kernel(const B
                 uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
-                    st16(yr + 8 * (tid + j * NT), scale8(xv[rr][j], wv[j], rstd));
+                    if (live(tid, j)) st16(yr + 8 * (tid + j * nt), scale8(xv[rr][j], wv[j], rstd));
             }
         }
     }
@@ -632,41 +649,71 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
 // not fit two such stages and take the CTA-per-row schedule.
 struct BulkGeometry {
     int nt, vpr, R, stages, ctas;
+    bool generic;  // masked instantiation with a run-time consumer count
 };
+
+// Rows that are not a power-of-two width (any N % 8 == 0 from 512 to 32768)
+// run the generic instantiation: the fewest chunks per thread (1, 2, 4 or 8)
+// that keep the consumers at 256 threads or fewer (N <= 16384), else 8 chunks
+// and up to 512 threads (plain RMSNorm only: the fused forms would spill);
+// R = 8 / VPR rows a stage.
+static bool bulk_geometry_generic(int N, bool add, bool ln, BulkGeometry *g) {
+    if (N < 512 || N > 32768 || N % 8 != 0) return false;
+    const int cpr = N >> 3;
+    // Plain RMSNorm / L2Norm fit up to 512 consumers without spilling and want
+    // the warps; the fused forms carry more per thread and stay at 256.
+    const int cap = (add || ln) ? 256 : 512;
+    int vpr = 1;
+    while (vpr < 8 && (cpr + vpr - 1) / vpr > cap) vpr *= 2;
+    const int per = (cpr + vpr - 1) / vpr;
+    if (per > cap) return false;
+    const int nt = ((per + 31) / 32) * 32;
+    const int R = 8 / vpr;
+    const size_t stage = static_cast<size_t>(add ? 2 : 1) * R * N * 2;
+    if (2 * stage > 200 * 1024) return false;  // two stages must fit with room to spare
+    // About 64 KiB in flight per SM, as the tuned power-of-two layouts have:
+    // small stages get a deeper ring (2 to 4 stages).
+    int stages = static_cast<int>((65536 + stage - 1) / stage);
+    if (stages < 2) stages = 2;
+    if (stages > 4) stages = 4;
+    *g = {nt, vpr, R, stages, 1, true};
+    return true;
+}
 
 static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) {
     const bool few_rows = M <= 8192;
+    if ((N & (N - 1)) != 0 || N < 1024) return bulk_geometry_generic(N, add, ln, g);
     if (ln) {
         // LayerNorm keeps its mean and the bias loads live too: 4-row stages at
         // 4096 and no ring at 32768 (both spill otherwise).
         switch (N) {
-            case 1024: *g = {128, 1, 8, 2, 1}; break;
-            case 2048: *g = {256, 1, 8, 2, 1}; break;
-            case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1}; break;
-            case 8192: *g = {256, 4, 2, 2, 1}; break;
-            case 16384: *g = {512, 4, 1, 2, 1}; break;
+            case 1024: *g = {128, 1, 8, 2, 1, false}; break;
+            case 2048: *g = {256, 1, 8, 2, 1, false}; break;
+            case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1, false}; break;
+            case 8192: *g = {256, 4, 2, 2, 1, false}; break;
+            case 16384: *g = {512, 4, 1, 2, 1, false}; break;
             default: return false;
         }
         return true;
     }
     if (add) {
         switch (N) {
-            case 1024: *g = {128, 1, 8, 2, 1}; break;
-            case 2048: *g = {256, 1, 8, 2, 1}; break;
-            case 4096: *g = {256, 2, 4, 2, 1}; break;
-            case 8192: *g = {256, 4, 2, 2, 1}; break;
-            case 16384: *g = {512, 4, 1, 2, 1}; break;
+            case 1024: *g = {128, 1, 8, 2, 1, false}; break;
+            case 2048: *g = {256, 1, 8, 2, 1, false}; break;
+            case 4096: *g = {256, 2, 4, 2, 1, false}; break;
+            case 8192: *g = {256, 4, 2, 2, 1, false}; break;
+            case 16384: *g = {512, 4, 1, 2, 1, false}; break;
             default: return false;
         }
         return true;
     }
     switch (N) {
-        case 1024: *g = {128, 1, 8, 2, 1}; break;
-        case 2048: *g = {256, 1, 8, 2, 1}; break;
-        case 4096: *g = few_rows ? BulkGeometry{256, 2, 4, 2, 2} : BulkGeometry{256, 2, 8, 2, 1}; break;
-        case 8192: *g = {256, 4, 2, 2, 1}; break;
-        case 16384: *g = {512, 4, 1, 2, 1}; break;
-        case 32768: *g = {512, 8, 1, 2, 1}; break;
+        case 1024: *g = {128, 1, 8, 2, 1, false}; break;
+        case 2048: *g = {256, 1, 8, 2, 1, false}; break;
+        case 4096: *g = few_rows ? BulkGeometry{256, 2, 4, 2, 2, false} : BulkGeometry{256, 2, 8, 2, 1, false}; break;
+        case 8192: *g = {256, 4, 2, 2, 1, false}; break;
+        case 16384: *g = {512, 4, 1, 2, 1, false}; break;
+        case 32768: *g = {512, 8, 1, 2, 1, false}; break;
         default: return false;
     }
     return true;
@@ -674,7 +721,7 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
 
 template <int VPR, int R, int NT, bool ADD, bool LN>
 static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_cap,
-                            cudaStream_t st) {
+                            cudaStream_t st, int nt = NT) {
     static std::atomic<int> attr_done[kMaxDevices];
     const int dev = current_device_index();
     if (dev < 0 || dev >= kMaxDevices) return RN_ERR_DEVICE;
@@ -687,7 +734,7 @@ static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_c
         }
         attr_done[dev].store(1, std::memory_order_release);
     }
-    rms_persistent_bulk_kernel<VPR, R, NT, ADD, LN><<<grid, NT + 32, smem, st>>>(a);
+    rms_persistent_bulk_kernel<VPR, R, NT, ADD, LN><<<grid, nt + 32, smem, st>>>(a);
     return launch_status();
 }
 
@@ -715,6 +762,24 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.l2, j.M, N, j.eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
     const int g = static_cast<int>(grid);
+    if (geo.generic) {
+        if constexpr (ADD || LN) {  // at most 256 consumers
+            switch (geo.vpr) {
+                case 1: return launch_bulk_inst<1, 8, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 2: return launch_bulk_inst<2, 4, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 4: return launch_bulk_inst<4, 2, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 8: return launch_bulk_inst<8, 1, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+            }
+        } else {  // up to 512 consumers
+            switch (geo.vpr) {
+                case 1: return launch_bulk_inst<1, 8, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 2: return launch_bulk_inst<2, 4, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 4: return launch_bulk_inst<4, 2, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 8: return launch_bulk_inst<8, 1, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+            }
+        }
+        return RN_ERR_SHAPE;
+    }
     switch (N) {
         case 1024: return launch_bulk_inst<1, 8, 128, ADD, LN>(a, g, smem, smem_cap, st);
         case 2048: return launch_bulk_inst<1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
@@ -736,7 +801,11 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
 static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &dev) {
     BulkGeometry geo;
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    if (bulk_geometry(M, N, add, ln, &geo) && M >= 4LL * dev.sm_count) return RN_SCHED_PERSIST_BULK;
+    // The generic (non-power-of-two) ring measured behind the CTA-per-row
+    // schedule below 4096-wide rows; from 4096 up it is ahead.
+    if (bulk_geometry(M, N, add, ln, &geo) && M >= 4LL * dev.sm_count &&
+        (!geo.generic || N >= 4096))
+        return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
     return RN_SCHED_CTA_ROW;
 }

@@ -38,3 +38,25 @@ def padded_empty(shape, dtype, pad: int, fill_bits: int):
 def canary_intact(buf: torch.Tensor, pad: int, fill_bits: int) -> bool:
     b = bf16_bits(buf.view(torch.bfloat16))
     return bool(np.all(b[:pad] == fill_bits) and np.all(b[-pad:] == fill_bits))
+
+
+def bulk_eligible(N: int, mode: str = "rms") -> bool:
+    """Whether the persistent bulk-copy schedule serves row width N for
+    mode "rms" (RMSNorm, L2Norm), "add" (fused residual add) or "ln"
+    (LayerNorm): power-of-two widths 1024..32768 (the fused forms up to
+    16384), and any other N % 8 == 0 from 512 up whose generic layout fits."""
+    if N % 8 or N < 512 or N > 32768:
+        return False
+    if N >= 1024 and (N & (N - 1)) == 0:
+        return N <= 16384 if mode in ("add", "ln") else True
+    cpr = N // 8
+    cap = 256 if mode in ("add", "ln") else 512
+    vpr = 1
+    while vpr < 8 and -(-cpr // vpr) > cap:
+        vpr *= 2
+    per = -(-cpr // vpr)
+    if per > cap:
+        return False
+    rows = 8 // vpr
+    stage = (2 if mode == "add" else 1) * rows * N * 2
+    return 2 * stage <= 200 * 1024

@@ -15,7 +15,7 @@ import torch
 import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, rmsnorm_inputs
-from tests.gpu_util import canary_intact, padded_empty, require_gpu
+from tests.gpu_util import bulk_eligible, canary_intact, padded_empty, require_gpu
 from tests.parity import assert_parity
 
 pytestmark = pytest.mark.gpu
@@ -28,7 +28,7 @@ def eligible(schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
         return N <= 2048
     if schedule == binding.RN_SCHED_PERSIST_BULK:
-        return N in (1024, 2048, 4096, 8192, 16384)
+        return bulk_eligible(N, "add")
     return True
 
 
@@ -124,3 +124,14 @@ def test_full_size_sampled_rows(M, N):
     assert_parity(bf16_bits(y.index_select(0, idx)), y_want, f"sampled M={M} N={N}")
     # every row: h equals torch's own bf16 addition (the correctly rounded sum)
     assert torch.equal(h.view(torch.int16), (x + r).view(torch.int16))
+
+
+@pytest.mark.parametrize("N", [3072, 5120, 12288, 1000])
+def test_non_power_of_two_widths_on_the_ring(N):
+    M = 2001
+    x, r, w = inputs(M, N, seed=N)
+    h_want, y_want = oracle.add_rmsnorm(bf16_bits(x), bf16_bits(r), bf16_bits(w), 1e-6)
+    h, y = binding.add_rmsnorm_fwd(x.cuda(), r.cuda(), w.cuda(), 1e-6,
+                                   schedule=binding.RN_SCHED_PERSIST_BULK)
+    assert np.array_equal(bf16_bits(h), h_want)
+    assert_parity(bf16_bits(y), y_want, f"add ring N={N}")

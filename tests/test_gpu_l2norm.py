@@ -12,7 +12,7 @@ import torch
 import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, rmsnorm_inputs
-from tests.gpu_util import canary_intact, padded_empty, require_gpu
+from tests.gpu_util import bulk_eligible, canary_intact, padded_empty, require_gpu
 from tests.parity import assert_parity
 
 pytestmark = pytest.mark.gpu
@@ -25,7 +25,7 @@ def eligible(schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
         return N <= 2048
     if schedule == binding.RN_SCHED_PERSIST_BULK:
-        return N in (1024, 2048, 4096, 8192, 16384, 32768)
+        return bulk_eligible(N, "rms")
     return True
 
 

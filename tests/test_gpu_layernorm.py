@@ -16,7 +16,7 @@ import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, norm_bias, rmsnorm_inputs
 from tests.exact import bits_to_f64
-from tests.gpu_util import canary_intact, padded_empty, require_gpu
+from tests.gpu_util import bulk_eligible, canary_intact, padded_empty, require_gpu
 from tests.parity import assert_parity
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ def eligible(schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
         return N <= 2048
     if schedule == binding.RN_SCHED_PERSIST_BULK:
-        return N in (1024, 2048, 4096, 8192, 16384)
+        return bulk_eligible(N, "ln")
     return True
 
 
@@ -120,3 +120,14 @@ def test_full_size_sampled_rows(M, N):
     idx = torch.from_numpy(rows).cuda()
     want = oracle.layernorm(bf16_bits(x.index_select(0, idx)), bf16_bits(w), bf16_bits(b), 1e-5)
     assert_parity(bf16_bits(y.index_select(0, idx)), want, f"ln sampled M={M} N={N}")
+
+
+@pytest.mark.parametrize("N", [3072, 5120, 12288, 1000])
+def test_non_power_of_two_widths_on_the_ring(N):
+    M = 2001
+    x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=N + 1)
+    b = norm_bias(N, seed=N + 2)
+    want = oracle.layernorm(bf16_bits(x), bf16_bits(w), bf16_bits(b), 1e-5)
+    y = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), 1e-5,
+                              schedule=binding.RN_SCHED_PERSIST_BULK)
+    assert_parity(bf16_bits(y), want, f"ln ring N={N}")

@@ -16,7 +16,7 @@ import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, rmsnorm_inputs
 from tests.exact import ulp_distance_bf16
-from tests.gpu_util import canary_intact, padded_empty, require_gpu
+from tests.gpu_util import bulk_eligible, canary_intact, padded_empty, require_gpu
 from tests.parity import assert_parity
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ def eligible(schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
         return N <= 2048
     if schedule == binding.RN_SCHED_PERSIST_BULK:
-        return N in (1024, 2048, 4096, 8192, 16384, 32768)
+        return bulk_eligible(N, "rms")
     return True
 
 
@@ -180,3 +180,17 @@ def test_sweep_full_size(M, N):
 @pytest.mark.parametrize("M", [1024, 4096, 8192])
 def test_wide_rows_full_size(M):
     _check_full_size(M, 32768, 1e-5, 0.0)
+
+
+@pytest.mark.parametrize("N", [3072, 5120, 6656, 12288, 20480, 4104, 1000])
+def test_non_power_of_two_widths_on_the_ring(N):
+    # common hidden sizes that are not powers of two: the masked generic ring
+    M = 3001
+    x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=N)
+    want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6)
+    pad = 64
+    buf, y = padded_empty((M, N), torch.bfloat16, pad, 0x7FC1)
+    binding.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6, y, schedule=binding.RN_SCHED_PERSIST_BULK)
+    torch.cuda.synchronize()
+    assert_parity(bf16_bits(y), want, f"ring N={N}")
+    assert canary_intact(buf, pad, 0x7FC1)
