@@ -494,12 +494,17 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             }
             named_bar_sync(1, nt);
             if (flags[k & 1]) break;  // same decision in every consumer warp
+            // lane rr finishes row rr's mean once; a shuffle hands it out
+            float my_mean = 0.f;
+            if (lane < R) {
+                float t = 0.f;
+                for (int q = 0; q < NW; ++q) t += rb1[lane * 32 + q];
+                my_mean = t / static_cast<float>(N);
+            }
             float mean[R];
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
-                float t = 0.f;
-                for (int q = 0; q < NW; ++q) t += rb1[rr * 32 + q];
-                mean[rr] = t / static_cast<float>(N);
+                mean[rr] = __shfl_sync(0xffffffffu, my_mean, rr);
                 float acc = 0.f;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
@@ -511,12 +516,16 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
                 for (int rr = 0; rr < R; ++rr) rb2[rr * 32 + warp] = s1[rr];
             }
             named_bar_sync(1, nt);
+            float my_rstd = 0.f;
+            if (lane < R) {
+                float t = 0.f;
+                for (int q = 0; q < NW; ++q) t += rb2[lane * 32 + q];
+                my_rstd = row_rstd(t, N, a.eps);
+            }
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
+                const float rstd = __shfl_sync(0xffffffffu, my_rstd, rr);
                 if (rr < rows) {
-                    float t = 0.f;
-                    for (int q = 0; q < NW; ++q) t += rb2[rr * 32 + q];
-                    const float rstd = row_rstd(t, N, a.eps);
                     uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
@@ -548,12 +557,18 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         }
         named_bar_sync(1, nt);
         if (flags[k & 1]) break;  // same decision in every consumer warp
+        // Lane rr finishes row rr's sum and scale once; a shuffle hands it to
+        // the warp (instead of every thread redoing all R rows).
+        float my_scale = 0.f;
+        if (lane < R) {
+            float tot = 0.f;
+            for (int q = 0; q < NW; ++q) tot += rb[lane * 32 + q];
+            my_scale = row_scale(tot, N, a.eps, a.l2);
+        }
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
+            const float rstd = __shfl_sync(0xffffffffu, my_scale, rr);
             if (rr < rows) {
-                float tot = 0.f;
-                for (int q = 0; q < NW; ++q) tot += rb[rr * 32 + q];
-                const float rstd = row_scale(tot, N, a.eps, a.l2);
                 uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
