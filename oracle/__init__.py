@@ -76,6 +76,22 @@ def _load():
         lib.rn_oracle_rmsnorm.argtypes = [u16p, u16p, ctypes.c_float,
                                           ctypes.c_int64, ctypes.c_int64, u16p]
         lib.rn_oracle_rmsnorm.restype = ctypes.c_int
+        lib.rn_oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.rn_oracle_f16_to_double.restype = ctypes.c_double
+        lib.rn_oracle_double_to_f16.argtypes = [ctypes.c_double]
+        lib.rn_oracle_double_to_f16.restype = ctypes.c_uint16
+        i32 = ctypes.c_int
+        lib.rn_oracle_rmsnorm_fmt.argtypes = lib.rn_oracle_rmsnorm.argtypes + [i32]
+        lib.rn_oracle_rmsnorm_fmt.restype = i32
+        lib.rn_oracle_l2norm_fmt.argtypes = [u16p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+                                             u16p, i32]
+        lib.rn_oracle_l2norm_fmt.restype = i32
+        lib.rn_oracle_add_rmsnorm_fmt.argtypes = [u16p, u16p, u16p, ctypes.c_float, ctypes.c_int64,
+                                                  ctypes.c_int64, u16p, u16p, i32]
+        lib.rn_oracle_add_rmsnorm_fmt.restype = i32
+        lib.rn_oracle_layernorm_fmt.argtypes = [u16p, u16p, u16p, ctypes.c_float, ctypes.c_int64,
+                                                ctypes.c_int64, u16p, i32]
+        lib.rn_oracle_layernorm_fmt.restype = i32
         lib.rn_oracle_rms_rstd.argtypes = [u16p, ctypes.c_float, ctypes.c_int64,
                                            ctypes.c_int64, f64p]
         lib.rn_oracle_rms_rstd.restype = ctypes.c_int
@@ -131,19 +147,29 @@ def double_to_bf16(v: float) -> int:
     return int(_load().rn_oracle_double_to_bf16(float(v)))
 
 
+def f16_to_double(bits: int) -> float:
+    return float(_load().rn_oracle_f16_to_double(int(bits) & 0xFFFF))
+
+
+def double_to_f16(v: float) -> int:
+    """Round one double to the nearest IEEE binary16 (ties to even); returns the bits."""
+    return int(_load().rn_oracle_double_to_f16(float(v)))
+
+
 # ---- array entry points -----------------------------------------------------
 
-def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
-    """y = bf16(x * 1/sqrt(mean(x^2) + eps) * w) row by row; x is [M, N] uint16."""
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float, f16: bool = False) -> np.ndarray:
+    """y = round(x * 1/sqrt(mean(x^2) + eps) * w) row by row; x is [M, N] uint16
+    bit patterns of bf16 (or IEEE fp16 with f16=True)."""
     x = _u16(x)
     w = _u16(w)
     if x.ndim != 2 or w.shape != (x.shape[1],):
         raise ValueError("x must be [M, N] and w [N]")
     M, N = x.shape
     y = np.zeros_like(x)
-    _check(_load().rn_oracle_rmsnorm(_ptr(x, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
-                                     ctypes.c_float(eps), M, N,
-                                     _ptr(y, ctypes.c_uint16)), "rmsnorm")
+    _check(_load().rn_oracle_rmsnorm_fmt(_ptr(x, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
+                                         ctypes.c_float(eps), M, N,
+                                         _ptr(y, ctypes.c_uint16), int(f16)), "rmsnorm")
     return y
 
 
@@ -191,18 +217,18 @@ def qk_norm_rope(qkv: np.ndarray, wq: np.ndarray, wk: np.ndarray,
     return out
 
 
-def l2norm(x: np.ndarray, eps: float) -> np.ndarray:
-    """y = bf16(x / max(||x||_2, eps)) row by row."""
+def l2norm(x: np.ndarray, eps: float, f16: bool = False) -> np.ndarray:
+    """y = round(x / max(||x||_2, eps)) row by row (bf16, or fp16 with f16=True)."""
     x = _u16(x)
     M, N = x.shape
     y = np.zeros_like(x)
-    _check(_load().rn_oracle_l2norm(_ptr(x, ctypes.c_uint16), ctypes.c_float(eps), M, N,
-                                    _ptr(y, ctypes.c_uint16)), "l2norm")
+    _check(_load().rn_oracle_l2norm_fmt(_ptr(x, ctypes.c_uint16), ctypes.c_float(eps), M, N,
+                                        _ptr(y, ctypes.c_uint16), int(f16)), "l2norm")
     return y
 
 
-def add_rmsnorm(x: np.ndarray, res: np.ndarray, w: np.ndarray, eps: float):
-    """(h, y): h = bf16(x + res), y = rmsnorm(h) row by row."""
+def add_rmsnorm(x: np.ndarray, res: np.ndarray, w: np.ndarray, eps: float, f16: bool = False):
+    """(h, y): h = round(x + res), y = rmsnorm(h) row by row (bf16, or fp16)."""
     x = _u16(x)
     res = _u16(res)
     w = _u16(w)
@@ -211,21 +237,23 @@ def add_rmsnorm(x: np.ndarray, res: np.ndarray, w: np.ndarray, eps: float):
     M, N = x.shape
     h = np.zeros_like(x)
     y = np.zeros_like(x)
-    _check(_load().rn_oracle_add_rmsnorm(_ptr(x, ctypes.c_uint16), _ptr(res, ctypes.c_uint16),
-                                         _ptr(w, ctypes.c_uint16), ctypes.c_float(eps), M, N,
-                                         _ptr(h, ctypes.c_uint16), _ptr(y, ctypes.c_uint16)),
-           "add_rmsnorm")
+    _check(_load().rn_oracle_add_rmsnorm_fmt(_ptr(x, ctypes.c_uint16), _ptr(res, ctypes.c_uint16),
+                                             _ptr(w, ctypes.c_uint16), ctypes.c_float(eps), M, N,
+                                             _ptr(h, ctypes.c_uint16), _ptr(y, ctypes.c_uint16),
+                                             int(f16)), "add_rmsnorm")
     return h, y
 
 
-def layernorm(x: np.ndarray, w: np.ndarray, b: np.ndarray | None, eps: float) -> np.ndarray:
-    """y = bf16((x - mean) / sqrt(var + eps) * w + b) row by row (biased variance)."""
+def layernorm(x: np.ndarray, w: np.ndarray, b: np.ndarray | None, eps: float,
+              f16: bool = False) -> np.ndarray:
+    """y = round((x - mean) / sqrt(var + eps) * w + b) row by row (biased
+    variance; bf16, or fp16 with f16=True)."""
     x = _u16(x)
     w = _u16(w)
     M, N = x.shape
     y = np.zeros_like(x)
     bp = None if b is None else _ptr(_u16(b), ctypes.c_uint16)
-    _check(_load().rn_oracle_layernorm(_ptr(x, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
-                                       bp, ctypes.c_float(eps), M, N,
-                                       _ptr(y, ctypes.c_uint16)), "layernorm")
+    _check(_load().rn_oracle_layernorm_fmt(_ptr(x, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
+                                           bp, ctypes.c_float(eps), M, N,
+                                           _ptr(y, ctypes.c_uint16), int(f16)), "layernorm")
     return y

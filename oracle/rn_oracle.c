@@ -24,7 +24,8 @@
  *     Gluon", section 3.2.
  *
  * Arithmetic: every value is widened to double, computed in double, and
- * rounded ONCE to bf16 with round-to-nearest-even at the end.  Sums run in
+ * rounded ONCE to bf16 (or, for the *_fmt forms with f16 = 1, IEEE fp16)
+ * with round-to-nearest-even at the end.  Sums run in
  * plain index order.  Compile without -ffast-math and with -ffp-contract=off
  * so the result is the same on every host.
  *
@@ -80,13 +81,70 @@ uint16_t rn_oracle_double_to_bf16(double v)
     return (uint16_t)(u >> 16);
 }
 
+/* ---- fp16 (IEEE binary16) <-> double ------------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 mantissa bits. */
+double rn_oracle_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                  /* zero and subnormals */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest binary16 (ties to even), in one step:
+ * 11 significant bits, quantum 2^(e-11) for |v| in [2^(e-1), 2^e), fixed
+ * subnormal quantum 2^-24, and everything that rounds to 2^16 or beyond is
+ * infinity (the largest finite value is 65504). */
+uint16_t rn_oracle_double_to_f16(double v)
+{
+    if (isnan(v)) return 0x7E00u;
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7C00u;
+    int e;
+    (void)frexp(a, &e);                              /* a in [2^(e-1), 2^e) */
+    int qexp = e - 11;
+    if (qexp < -24) qexp = -24;
+    double q = ldexp(1.0, qexp);
+    double r = nearbyint(a / q) * q;                 /* ties to even */
+    if (r >= 65536.0) return sign | 0x7C00u;
+    if (r < ldexp(1.0, -14))                         /* subnormal (or zero) */
+        return sign | (uint16_t)(r / ldexp(1.0, -24));
+    int ex;
+    double m = frexp(r, &ex);                        /* r = m * 2^ex, m in [0.5, 1) */
+    int E = ex - 1;                                  /* r = (2m) * 2^E */
+    uint16_t mant = (uint16_t)((2.0 * m - 1.0) * 1024.0);
+    return sign | (uint16_t)((E + 15) << 10) | mant;
+}
+
+/* Element format of the row operations: 0 = bf16, 1 = fp16. */
+static double widen(uint16_t b, int f16)
+{
+    return f16 ? rn_oracle_f16_to_double(b) : rn_oracle_bf16_to_double(b);
+}
+
+static uint16_t narrow(double v, int f16)
+{
+    return f16 ? rn_oracle_double_to_f16(v) : rn_oracle_double_to_bf16(v);
+}
+
 /* ---- RMSNorm ------------------------------------------------------------ */
 
-/* y[r, j] = bf16( x[r, j] * 1/sqrt( (sum_k x[r, k]^2) / N + eps ) * w[j] )
- * for a row-major x[M, N], one row at a time.  eps is the caller's binary32
- * value widened exactly.  Follows "[Inductor] Codegen Gluon", section 3.1. */
-int rn_oracle_rmsnorm(const uint16_t *x, const uint16_t *w, float eps,
-                      int64_t M, int64_t N, uint16_t *y)
+/* y[r, j] = round( x[r, j] * 1/sqrt( (sum_k x[r, k]^2) / N + eps ) * w[j] )
+ * for a row-major x[M, N], one row at a time, in bf16 (f16 = 0) or fp16
+ * (f16 = 1).  eps is the caller's binary32 value widened exactly.  Follows
+ * "[Inductor] Codegen Gluon", section 3.1 (section 3.2 widens it to fp16). */
+int rn_oracle_rmsnorm_fmt(const uint16_t *x, const uint16_t *w, float eps,
+                          int64_t M, int64_t N, uint16_t *y, int f16)
 {
     if (M < 0 || N <= 0) return -3;
     if (M == 0) return 0;
@@ -97,18 +155,24 @@ int rn_oracle_rmsnorm(const uint16_t *x, const uint16_t *w, float eps,
         uint16_t *yr = y + r * N;
         double ss = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            double v = rn_oracle_bf16_to_double(xr[j]);
+            double v = widen(xr[j], f16);
             ss += v * v;
         }
         double ms = ss / (double)N;
         double rs = 1.0 / sqrt(ms + deps);
         for (int64_t j = 0; j < N; ++j) {
-            double v = rn_oracle_bf16_to_double(xr[j]);
-            double g = rn_oracle_bf16_to_double(w[j]);
-            yr[j] = rn_oracle_double_to_bf16(v * rs * g);
+            double v = widen(xr[j], f16);
+            double g = widen(w[j], f16);
+            yr[j] = narrow(v * rs * g, f16);
         }
     }
     return 0;
+}
+
+int rn_oracle_rmsnorm(const uint16_t *x, const uint16_t *w, float eps,
+                      int64_t M, int64_t N, uint16_t *y)
+{
+    return rn_oracle_rmsnorm_fmt(x, w, eps, M, N, y, 0);
 }
 
 /* The row statistic alone: rstd[r] = 1/sqrt(mean(x[r,:]^2) + eps), in
@@ -240,7 +304,8 @@ int rn_oracle_qk_norm_rope(uint16_t *qkv, const uint16_t *wq,
 /* y[r, j] = bf16( x[r, j] / max(||x[r, :]||_2, eps) ): one reduction, then a
  * scale by the inverse norm ("[Inductor] Codegen Gluon", section 3.2).  The
  * norm is sqrt(sum_j x^2) in double; eps guards rows whose norm is below it. */
-int rn_oracle_l2norm(const uint16_t *x, float eps, int64_t M, int64_t N, uint16_t *y)
+int rn_oracle_l2norm_fmt(const uint16_t *x, float eps, int64_t M, int64_t N, uint16_t *y,
+                         int f16)
 {
     if (M < 0 || N <= 0) return -3;
     if (M == 0) return 0;
@@ -248,15 +313,20 @@ int rn_oracle_l2norm(const uint16_t *x, float eps, int64_t M, int64_t N, uint16_
     for (int64_t r = 0; r < M; ++r) {
         double ss = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            double v = rn_oracle_bf16_to_double(x[r * N + j]);
+            double v = widen(x[r * N + j], f16);
             ss += v * v;
         }
         double nrm = sqrt(ss);
         double d = nrm > (double)eps ? nrm : (double)eps;
         for (int64_t j = 0; j < N; ++j)
-            y[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) / d);
+            y[r * N + j] = narrow(widen(x[r * N + j], f16) / d, f16);
     }
     return 0;
+}
+
+int rn_oracle_l2norm(const uint16_t *x, float eps, int64_t M, int64_t N, uint16_t *y)
+{
+    return rn_oracle_l2norm_fmt(x, eps, M, N, y, 0);
 }
 
 /* ---- fused residual add + RMSNorm ---------------------------------------- */
@@ -267,18 +337,24 @@ int rn_oracle_l2norm(const uint16_t *x, float eps, int64_t M, int64_t N, uint16_
  * and changes nothing else ("TorchInductor: from ATen IR to Triton kernel",
  * sections 14.3 and 14.27: the norm / residual-add chain fused into one
  * kernel). */
-int rn_oracle_add_rmsnorm(const uint16_t *x, const uint16_t *res, const uint16_t *w,
-                          float eps, int64_t M, int64_t N, uint16_t *h, uint16_t *y)
+int rn_oracle_add_rmsnorm_fmt(const uint16_t *x, const uint16_t *res, const uint16_t *w,
+                              float eps, int64_t M, int64_t N, uint16_t *h, uint16_t *y,
+                              int f16)
 {
     if (M < 0 || N <= 0) return -3;
     if (M == 0) return 0;
     if (!x || !res || !w || !h || !y) return -1;
     for (int64_t r = 0; r < M; ++r) {
         for (int64_t j = 0; j < N; ++j)
-            h[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) +
-                                                    rn_oracle_bf16_to_double(res[r * N + j]));
+            h[r * N + j] = narrow(widen(x[r * N + j], f16) + widen(res[r * N + j], f16), f16);
     }
-    return rn_oracle_rmsnorm(h, w, eps, M, N, y);
+    return rn_oracle_rmsnorm_fmt(h, w, eps, M, N, y, f16);
+}
+
+int rn_oracle_add_rmsnorm(const uint16_t *x, const uint16_t *res, const uint16_t *w,
+                          float eps, int64_t M, int64_t N, uint16_t *h, uint16_t *y)
+{
+    return rn_oracle_add_rmsnorm_fmt(x, res, w, eps, M, N, h, y, 0);
 }
 
 /* ---- LayerNorm ---------------------------------------------------------- */
@@ -290,8 +366,8 @@ int rn_oracle_add_rmsnorm(const uint16_t *x, const uint16_t *res, const uint16_t
  * 14.12.2, spells out.  The variance is the plain two-pass definition here;
  * the one-pass Welford update of that section reaches the same value up to
  * rounding.  b may be NULL (no bias). */
-int rn_oracle_layernorm(const uint16_t *x, const uint16_t *w, const uint16_t *b,
-                        float eps, int64_t M, int64_t N, uint16_t *y)
+int rn_oracle_layernorm_fmt(const uint16_t *x, const uint16_t *w, const uint16_t *b,
+                            float eps, int64_t M, int64_t N, uint16_t *y, int f16)
 {
     if (M < 0 || N <= 0) return -3;
     if (M == 0) return 0;
@@ -300,20 +376,25 @@ int rn_oracle_layernorm(const uint16_t *x, const uint16_t *w, const uint16_t *b,
         const uint16_t *xr = x + r * N;
         uint16_t *yr = y + r * N;
         double sum = 0.0;
-        for (int64_t j = 0; j < N; ++j) sum += rn_oracle_bf16_to_double(xr[j]);
+        for (int64_t j = 0; j < N; ++j) sum += widen(xr[j], f16);
         double mean = sum / (double)N;
         double m2 = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            double d = rn_oracle_bf16_to_double(xr[j]) - mean;
+            double d = widen(xr[j], f16) - mean;
             m2 += d * d;
         }
         double rs = 1.0 / sqrt(m2 / (double)N + (double)eps);
         for (int64_t j = 0; j < N; ++j) {
-            double v = (rn_oracle_bf16_to_double(xr[j]) - mean) * rs *
-                       rn_oracle_bf16_to_double(w[j]);
-            if (b) v += rn_oracle_bf16_to_double(b[j]);
-            yr[j] = rn_oracle_double_to_bf16(v);
+            double v = (widen(xr[j], f16) - mean) * rs * widen(w[j], f16);
+            if (b) v += widen(b[j], f16);
+            yr[j] = narrow(v, f16);
         }
     }
     return 0;
+}
+
+int rn_oracle_layernorm(const uint16_t *x, const uint16_t *w, const uint16_t *b, float eps,
+                        int64_t M, int64_t N, uint16_t *y)
+{
+    return rn_oracle_layernorm_fmt(x, w, b, eps, M, N, y, 0);
 }

@@ -146,3 +146,32 @@ def bits_to_f64(bits):
     import numpy as np
     u32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return u32.view(np.float32).astype(np.float64)
+
+
+_F16_OVERFLOW = Fraction(65520)  # 65504 + half a quantum: ties to 2^16 (even) -> inf
+
+
+def round_f16(q) -> int:
+    """Exact rational -> nearest IEEE binary16 bit pattern, ties to even."""
+    q = Fraction(q)
+    if q == 0:
+        return 0
+    sign = 0x8000 if q < 0 else 0
+    a = -q if q < 0 else q
+    if a >= _F16_OVERFLOW:
+        return sign | 0x7C00
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** (e - 1) > a:
+        e -= 1
+    while Fraction(2) ** e <= a:
+        e += 1
+    qexp = max(e - 11, -24)
+    n = _round_half_even(a / Fraction(2) ** qexp)
+    r = n * Fraction(2) ** qexp
+    import numpy as np
+    return sign | int(np.array([float(r)], dtype=np.float16).view(np.uint16)[0])
+
+
+def f16_bits_to_f64(bits):
+    import numpy as np
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)

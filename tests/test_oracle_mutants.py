@@ -22,7 +22,7 @@ MUTANTS = {
     "eps_on_sum": ("double ms = ss / (double)N;\n        double rs = 1.0 / sqrt(ms + deps);",
                    "double ms = ss / (double)N;\n        double rs = 1.0 / sqrt((ss + deps) / (double)N);"),
     "eps_outside_sqrt": ("double rs = 1.0 / sqrt(ms + deps);", "double rs = 1.0 / (sqrt(ms) + deps);"),
-    "no_weight": ("yr[j] = rn_oracle_double_to_bf16(v * rs * g);", "yr[j] = rn_oracle_double_to_bf16(v * rs + 0.0 * g);"),
+    "no_weight": ("yr[j] = narrow(v * rs * g, f16);", "yr[j] = narrow(v * rs + 0.0 * g, f16);"),
     "round_via_float": ("double n = nearbyint(v / q);", "double n = nearbyint((double)(float)v / q);"),
     "ties_away": ("double n = nearbyint(v / q);", "double n = round(v / q);"),
     "rope_sign_first": ("o[a] = n[a] * c - n[b] * s;", "o[a] = n[a] * c + n[b] * s;"),
@@ -44,12 +44,16 @@ MUTANTS = {
     "gptj_cos_index": ("int a = style ? 2 * i : i;", "int a = style ? 2 * i + 1 : i;"),
     "l2_norm_squared": ("double nrm = sqrt(ss);", "double nrm = ss;"),
     "l2_eps_added": ("double d = nrm > (double)eps ? nrm : (double)eps;", "double d = nrm + (double)eps;"),
-    "add_sum_not_rounded": ("h[r * N + j] = rn_oracle_double_to_bf16(rn_oracle_bf16_to_double(x[r * N + j]) +",
-                            "h[r * N + j] = rn_oracle_double_to_bf16(0.999 * rn_oracle_bf16_to_double(x[r * N + j]) +"),
-    "add_norm_of_x_only": ("return rn_oracle_rmsnorm(h, w, eps, M, N, y);", "return rn_oracle_rmsnorm(x, w, eps, M, N, y);"),
+    "add_sum_not_rounded": ("h[r * N + j] = narrow(widen(x[r * N + j], f16) + widen(res[r * N + j], f16), f16);",
+                            "h[r * N + j] = narrow(0.999 * widen(x[r * N + j], f16) + widen(res[r * N + j], f16), f16);"),
+    "add_norm_of_x_only": ("return rn_oracle_rmsnorm_fmt(h, w, eps, M, N, y, f16);", "return rn_oracle_rmsnorm_fmt(x, w, eps, M, N, y, f16);"),
     "layernorm_unbiased": ("double rs = 1.0 / sqrt(m2 / (double)N + (double)eps);",
                            "double rs = 1.0 / sqrt(m2 / (double)(N - 1) + (double)eps);"),
-    "layernorm_bias_dropped": ("if (b) v += rn_oracle_bf16_to_double(b[j]);", "(void)b;"),
+    "layernorm_bias_dropped": ("if (b) v += widen(b[j], f16);", "(void)b;"),
+    "f16_round_via_float": ("double r = nearbyint(a / q) * q;                 /* ties to even */",
+                            "double r = nearbyint((double)(float)a / q) * q;"),
+    "f16_exponent_bias": ("return sign | (uint16_t)((E + 15) << 10) | mant;", "return sign | (uint16_t)((E + 14) << 10) | mant;"),
+    "f16_subnormal_quantum": ("if (qexp < -24) qexp = -24;", "if (qexp < -25) qexp = -25;"),
 }
 
 

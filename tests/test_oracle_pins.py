@@ -647,3 +647,94 @@ def test_gptj_exact_brute_force_and_position_zero():
     a = oracle.qk_norm_rope(qkv, wq, wk, table, np.array([0]), 2, 1, 16, 16, 1e-6, style=1)
     b = oracle.qk_norm_rope(qkv, wq, wk, table, np.array([0]), 2, 1, 16, 16, 1e-6, style=0)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# IEEE fp16 element format
+# ---------------------------------------------------------------------------
+
+from tests.exact import f16_bits_to_f64, round_f16  # noqa: E402
+
+
+class TestF16Rounding:
+    def test_edges(self):
+        assert oracle.double_to_f16(1 + 2**-11) == 0x3C00          # tie -> even
+        assert oracle.double_to_f16(1 + 3 * 2**-11) == 0x3C02      # tie -> even
+        assert oracle.double_to_f16(1 + 2**-11 + 2**-40) == 0x3C01  # single rounding
+        assert oracle.double_to_f16(2.0**-24) == 0x0001            # smallest subnormal
+        assert oracle.double_to_f16(2.0**-25) == 0x0000            # tie -> even (0)
+        assert oracle.double_to_f16(1.5 * 2.0**-24) == 0x0002      # tie -> even (2)
+        assert oracle.double_to_f16(2.0**-14) == 0x0400            # smallest normal
+        assert oracle.double_to_f16(65504.0) == 0x7BFF
+        assert oracle.double_to_f16(65519.99) == 0x7BFF
+        assert oracle.double_to_f16(65520.0) == 0x7C00             # tie -> 2^16 -> inf
+        assert oracle.double_to_f16(-1e9) == 0xFC00
+        assert oracle.double_to_f16(-0.0) == 0x8000
+
+    def test_decode_every_pattern_matches_numpy(self):
+        bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+        ref = bits.view(np.float16).astype(np.float64)
+        ours = np.array([oracle.f16_to_double(int(b)) for b in bits])
+        same = (ours == ref) | (np.isnan(ours) & np.isnan(ref))
+        assert same.all()
+
+    def test_binary32_values_match_torch(self):
+        rng = np.random.default_rng(101)
+        f = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 12, 20000))).astype(np.float32)
+        lib = torch.from_numpy(f).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+        ours = np.array([oracle.double_to_f16(float(v)) for v in f], dtype=np.uint16)
+        assert np.array_equal(ours, lib)
+
+    def test_doubles_match_exact_rationals(self):
+        rng = np.random.default_rng(103)
+        vals = rng.standard_normal(3000) * np.exp(rng.uniform(-18, 11, 3000))
+        for v in vals:
+            assert oracle.double_to_f16(float(v)) == round_f16(Fraction(float(v)))
+
+
+def rand_f16(rng, shape, scale=1.0) -> np.ndarray:
+    return (rng.standard_normal(shape) * scale).astype(np.float16).view(np.uint16)
+
+
+def test_f16_row_ops_exact_brute_force():
+    rng = np.random.default_rng(107)
+    for N in (1, 3, 8, 13):
+        x = rand_f16(rng, (2, N), 2.0)
+        r = rand_f16(rng, (2, N), 0.5)
+        w = rand_f16(rng, (N,))
+        b = rand_f16(rng, (N,), 0.1)
+        eps = 1e-6
+        y = oracle.rmsnorm(x, w, eps, f16=True)
+        h, ya = oracle.add_rmsnorm(x, r, w, eps, f16=True)
+        yl = oracle.layernorm(x, w, b, eps, f16=True)
+        y2 = oracle.l2norm(x, 1e-12, f16=True)
+        for i in range(2):
+            xs = [Fraction(float(v)) for v in x[i].view(np.float16)]
+            ws = [Fraction(float(v)) for v in w.view(np.float16)]
+            bs = [Fraction(float(v)) for v in b.view(np.float16)]
+            den = dsqrt(sum(v * v for v in xs) / N + f32_to_fraction(eps))
+            assert list(y[i]) == [round_f16(to_dec(xs[j] * ws[j]) / den) for j in range(N)]
+            hs = [round_f16(xs[j] + Fraction(float(r[i].view(np.float16)[j]))) for j in range(N)]
+            assert list(h[i]) == hs
+            mean = sum(xs) / N
+            var = sum((v - mean) ** 2 for v in xs) / N
+            dl = dsqrt(var + f32_to_fraction(eps))
+            assert list(yl[i]) == [round_f16(to_dec((xs[j] - mean) * ws[j]) / dl + to_dec(bs[j]))
+                                   for j in range(N)]
+            n2 = dsqrt(sum(v * v for v in xs))
+            assert list(y2[i]) == [round_f16(to_dec(xs[j]) / n2) for j in range(N)]
+        assert np.array_equal(ya, oracle.rmsnorm(h, w, eps, f16=True))
+
+
+def test_f16_constant_row_closed_form():
+    N = 40
+    for c in (1.0, -3.5, 1e-3):
+        cb = np.array([c], dtype=np.float16).view(np.uint16)[0]
+        x = np.full((1, N), cb, dtype=np.uint16)
+        w = np.array(np.linspace(0.5, 2, N), dtype=np.float16).view(np.uint16)
+        y = oracle.rmsnorm(x, w, 1e-6, f16=True)[0]
+        cq = Fraction(float(np.uint16(cb).view(np.float16)))
+        den = dsqrt(cq * cq + f32_to_fraction(1e-6))
+        want = [round_f16(to_dec(cq * Fraction(float(np.uint16(wj).view(np.float16)))) / den)
+                for wj in w]
+        assert list(y) == want
