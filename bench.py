@@ -202,7 +202,7 @@ def traffic_per_launch(kernel: str, workload: str):
     when no capture matches or the kernel source changed since."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     src = os.path.join(ROOT, "row_normalization_gb300", "csrc",
-                       "rmsnorm.cu" if kernel.startswith("rms") else "qk_norm_rope.cu")
+                       "row_kernels.cuh" if kernel.startswith("rms") else "qk_norm_rope.cu")
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         with open(path) as fh:

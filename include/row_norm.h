@@ -1,5 +1,6 @@
 /*
- * row_norm.h -- C ABI of the GB300 (sm_103a) bf16 row-normalization library.
+ * row_norm.h -- C ABI of the GB300 (sm_103a) row-normalization library
+ * (bf16, and IEEE fp16 for the row norms).
  *
  * Operations
  *   rmsnorm_fwd       y = x * 1/sqrt(mean(x^2) + eps) * w, row by row.
@@ -42,6 +43,11 @@
  *   - Arithmetic: bf16 inputs are widened to fp32 at the point of use, all
  *     sums and products run in fp32, and each output is rounded once to
  *     bf16 (round to nearest even).
+ *   - The row norms also take IEEE fp16 tensors (rn_f16; the *_f16 entry
+ *     points and row_norm_fwd_ex): the same fp32 arithmetic, one rounding
+ *     to fp16 at the store (overflow to infinity, subnormals kept).
+ *     "[Inductor] Codegen Gluon", section 3.2, widens the eligible inputs
+ *     of the fused norm to fp16.
  */
 #ifndef ROW_NORM_H
 #define ROW_NORM_H
@@ -54,6 +60,9 @@ extern "C" {
 
 /* Raw bf16 bit pattern (sign, 8-bit exponent, 7-bit mantissa). */
 typedef uint16_t rn_bf16;
+
+/* Raw IEEE binary16 bit pattern (sign, 5-bit exponent, 10-bit mantissa). */
+typedef uint16_t rn_f16;
 
 /* ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *rn_stream_t;
@@ -193,6 +202,47 @@ int add_rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *residual,
                           rn_bf16 *h_out, rn_bf16 *y, int schedule,
                           uint64_t wait_timeout_ns, int debug_flags,
                           rn_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* fp16 row norms, and one entry point for every row norm and format          */
+/* ------------------------------------------------------------------------ */
+
+/* Element formats and operations of row_norm_fwd_ex. */
+enum { RN_DTYPE_BF16 = 0, RN_DTYPE_F16 = 1 };
+enum {
+    RN_OP_RMSNORM = 0,      /* rmsnorm_fwd:     x, w            -> y      */
+    RN_OP_L2NORM = 1,       /* l2norm_fwd:      x               -> y      */
+    RN_OP_ADD_RMSNORM = 2,  /* add_rmsnorm_fwd: x, residual, w  -> h, y   */
+    RN_OP_LAYERNORM = 3     /* layernorm_fwd:   x, w, b (or NULL) -> y    */
+};
+
+/* The four row norms on fp16 tensors: the same contracts, sizes, checks and
+ * errors as their bf16 namesakes above, every tensor rn_f16. */
+int rmsnorm_fwd_f16(const rn_f16 *x, const rn_f16 *w, float eps, int64_t M,
+                    int64_t N, rn_f16 *y, rn_stream_t stream);
+int l2norm_fwd_f16(const rn_f16 *x, float eps, int64_t M, int64_t N, rn_f16 *y,
+                   rn_stream_t stream);
+int add_rmsnorm_fwd_f16(const rn_f16 *x, const rn_f16 *residual, const rn_f16 *w,
+                        float eps, int64_t M, int64_t N, rn_f16 *h_out, rn_f16 *y,
+                        rn_stream_t stream);
+int layernorm_fwd_f16(const rn_f16 *x, const rn_f16 *w, const rn_f16 *b,
+                      float eps, int64_t M, int64_t N, rn_f16 *y,
+                      rn_stream_t stream);
+
+/* Any row norm (op = RN_OP_*) in either format (dtype = RN_DTYPE_*), with an
+ * explicit schedule, wait limit and test flags as rmsnorm_fwd_sched.  Every
+ * tensor is a DEVICE pointer to 16-bit patterns of `dtype`; the pointers an
+ * op does not use (residual and h_out outside RN_OP_ADD_RMSNORM, w for
+ * RN_OP_L2NORM, b outside RN_OP_LAYERNORM) are ignored and may be NULL.
+ * Errors as the op's own entry point; an unknown op or dtype is RN_ERR_ARG. */
+int row_norm_fwd_ex(int op, int dtype, const void *x, const void *residual,
+                    const void *w, const void *b, float eps, int64_t M, int64_t N,
+                    void *h_out, void *y, int schedule, uint64_t wait_timeout_ns,
+                    int debug_flags, rn_stream_t stream);
+
+/* The schedule (RN_SCHED_*) row_norm_fwd_ex picks under RN_SCHED_AUTO for op
+ * and (M, N) on the current device; the same for both formats. */
+int row_norm_select_schedule(int op, int64_t M, int64_t N);
 
 /* ------------------------------------------------------------------------ */
 /* Fused Q/K RMSNorm + neox RoPE                                              */

@@ -45,6 +45,16 @@ RN_QK_BULK = 16
 RN_ROPE_NEOX = 0
 RN_ROPE_GPTJ = 1
 
+RN_DTYPE_BF16 = 0
+RN_DTYPE_F16 = 1
+
+RN_OP_RMSNORM = 0
+RN_OP_L2NORM = 1
+RN_OP_ADD_RMSNORM = 2
+RN_OP_LAYERNORM = 3
+
+_ROW_DTYPES = {torch.bfloat16: RN_DTYPE_BF16, torch.float16: RN_DTYPE_F16}
+
 
 class RowNormError(RuntimeError):
     def __init__(self, name: str, code: int):
@@ -108,6 +118,19 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.rmsnorm_select_schedule.restype = i32
         L.qk_norm_rope_select_schedule.argtypes = [i64]
         L.qk_norm_rope_select_schedule.restype = i32
+        L.rmsnorm_fwd_f16.argtypes = [vp, vp, f32, i64, i64, vp, vp]
+        L.rmsnorm_fwd_f16.restype = i32
+        L.l2norm_fwd_f16.argtypes = [vp, f32, i64, i64, vp, vp]
+        L.l2norm_fwd_f16.restype = i32
+        L.add_rmsnorm_fwd_f16.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
+        L.add_rmsnorm_fwd_f16.restype = i32
+        L.layernorm_fwd_f16.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp]
+        L.layernorm_fwd_f16.restype = i32
+        L.row_norm_fwd_ex.argtypes = [i32, i32, vp, vp, vp, vp, f32, i64, i64, vp, vp, i32, u64,
+                                      i32, vp]
+        L.row_norm_fwd_ex.restype = i32
+        L.row_norm_select_schedule.argtypes = [i32, i64, i64]
+        L.row_norm_select_schedule.restype = i32
         L.rn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.rn_device_status.restype = i32
         _lib = L
@@ -135,6 +158,27 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _row_dtype(x: torch.Tensor) -> torch.dtype:
+    """The element format of a row-norm call: x's dtype, bf16 or fp16."""
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("x must be a torch.Tensor")
+    if x.dtype not in _ROW_DTYPES:
+        raise TypeError(f"x must be torch.bfloat16 or torch.float16, got {x.dtype}")
+    return x.dtype
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _row_ex(name, op, dt, x, r, w, b, eps, M, N, h, y, schedule, wait_timeout_ns, debug_flags,
+            stream):
+    rc = load().row_norm_fwd_ex(op, _ROW_DTYPES[dt], _ptr(x), _ptr(r), _ptr(w), _ptr(b), eps, M,
+                                N, _ptr(h), _ptr(y), schedule, wait_timeout_ns, debug_flags,
+                                _stream(stream))
+    _check(rc, name)
+
+
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -151,20 +195,31 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
 def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | None = None,
                 *, schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0,
                 debug_flags: int = 0, stream=None) -> torch.Tensor:
-    """y = x * rsqrt(mean(x^2, -1) + eps) * w for bf16 x [M, N]; returns y."""
-    _need(x, "x", torch.bfloat16)
-    _need(w, "w", torch.bfloat16)
+    """y = x * rsqrt(mean(x^2, -1) + eps) * w for x [M, N] in bf16 or fp16
+    (w and y in x's dtype); returns y."""
+    dt = _row_dtype(x)
+    _need(x, "x", dt)
+    _need(w, "w", dt)
     if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1]:
         raise ValueError("x must be [M, N] and w [N]")
     if y is None:
         y = torch.empty_like(x)
     else:
-        _need(y, "y", torch.bfloat16)
+        _need(y, "y", dt)
         if y.shape != x.shape:
             raise ValueError("y must have x's shape")
     M, N = x.shape
     L = load()
-    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+    plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if dt == torch.float16:
+        if plain:
+            _check(L.rmsnorm_fwd_f16(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
+                                     _stream(stream)), "rmsnorm_fwd_f16")
+        else:
+            _row_ex("row_norm_fwd_ex", RN_OP_RMSNORM, dt, x, None, w, None, eps, M, N, None, y,
+                    schedule, wait_timeout_ns, debug_flags, stream)
+        return y
+    if plain:
         rc = L.rmsnorm_fwd(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(), _stream(stream))
     else:
         rc = L.rmsnorm_fwd_sched(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
@@ -176,17 +231,27 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
 def l2norm_fwd(x: torch.Tensor, eps: float, y: torch.Tensor | None = None, *,
                schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0, debug_flags: int = 0,
                stream=None) -> torch.Tensor:
-    """y = x / max(||x||_2, eps) per row of bf16 x [M, N]."""
-    _need(x, "x", torch.bfloat16)
+    """y = x / max(||x||_2, eps) per row of x [M, N] (bf16 or fp16)."""
+    dt = _row_dtype(x)
+    _need(x, "x", dt)
     if x.dim() != 2:
         raise ValueError("x must be [M, N]")
     y = torch.empty_like(x) if y is None else y
-    _need(y, "y", torch.bfloat16)
+    _need(y, "y", dt)
     if y.shape != x.shape:
         raise ValueError("y must have x's shape")
     M, N = x.shape
     L = load()
-    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+    plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if dt == torch.float16:
+        if plain:
+            _check(L.l2norm_fwd_f16(x.data_ptr(), eps, M, N, y.data_ptr(), _stream(stream)),
+                   "l2norm_fwd_f16")
+        else:
+            _row_ex("row_norm_fwd_ex", RN_OP_L2NORM, dt, x, None, None, None, eps, M, N, None, y,
+                    schedule, wait_timeout_ns, debug_flags, stream)
+        return y
+    if plain:
         rc = L.l2norm_fwd(x.data_ptr(), eps, M, N, y.data_ptr(), _stream(stream))
     else:
         rc = L.l2norm_fwd_sched(x.data_ptr(), eps, M, N, y.data_ptr(), schedule,
@@ -198,23 +263,34 @@ def l2norm_fwd(x: torch.Tensor, eps: float, y: torch.Tensor | None = None, *,
 def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None, eps: float,
                   y: torch.Tensor | None = None, *, schedule: int = RN_SCHED_AUTO,
                   wait_timeout_ns: int = 0, debug_flags: int = 0, stream=None) -> torch.Tensor:
-    """y = (x - mean) / sqrt(var + eps) * w + b per row (biased variance); b may be None."""
-    _need(x, "x", torch.bfloat16)
-    _need(w, "w", torch.bfloat16)
+    """y = (x - mean) / sqrt(var + eps) * w + b per row (biased variance); b may
+    be None.  bf16 or fp16, every tensor in x's dtype."""
+    dt = _row_dtype(x)
+    _need(x, "x", dt)
+    _need(w, "w", dt)
     if b is not None:
-        _need(b, "b", torch.bfloat16)
+        _need(b, "b", dt)
         if b.shape != w.shape:
             raise ValueError("b must have w's shape")
     if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1]:
         raise ValueError("x must be [M, N] and w [N]")
     y = torch.empty_like(x) if y is None else y
-    _need(y, "y", torch.bfloat16)
+    _need(y, "y", dt)
     if y.shape != x.shape:
         raise ValueError("y must have x's shape")
     M, N = x.shape
     bp = None if b is None else b.data_ptr()
     L = load()
-    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+    plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if dt == torch.float16:
+        if plain:
+            _check(L.layernorm_fwd_f16(x.data_ptr(), w.data_ptr(), bp, eps, M, N, y.data_ptr(),
+                                       _stream(stream)), "layernorm_fwd_f16")
+        else:
+            _row_ex("row_norm_fwd_ex", RN_OP_LAYERNORM, dt, x, None, w, b, eps, M, N, None, y,
+                    schedule, wait_timeout_ns, debug_flags, stream)
+        return y
+    if plain:
         rc = L.layernorm_fwd(x.data_ptr(), w.data_ptr(), bp, eps, M, N, y.data_ptr(),
                              _stream(stream))
     else:
@@ -222,6 +298,15 @@ def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None, eps:
                                    schedule, wait_timeout_ns, debug_flags, _stream(stream))
     _check(rc, "layernorm_fwd")
     return y
+
+
+def row_norm_select_schedule(op: int, M: int, N: int) -> int:
+    """The RN_SCHED_* schedule a row norm (RN_OP_*) picks for (M, N); the same
+    for both element formats."""
+    rc = int(load().row_norm_select_schedule(int(op), int(M), int(N)))
+    if rc < 0:
+        raise RowNormError("row_norm_select_schedule", rc)
+    return rc
 
 
 def layernorm_select_schedule(M: int, N: int) -> int:
@@ -236,22 +321,33 @@ def add_rmsnorm_fwd(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, ep
                     h: torch.Tensor | None = None, y: torch.Tensor | None = None, *,
                     schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0,
                     debug_flags: int = 0, stream=None):
-    """h = x + residual (bf16), y = rmsnorm(h); returns (h, y).  Pass
-    h=residual for an in-place residual update."""
-    _need(x, "x", torch.bfloat16)
-    _need(residual, "residual", torch.bfloat16)
-    _need(w, "w", torch.bfloat16)
+    """h = x + residual, y = rmsnorm(h); returns (h, y).  bf16 or fp16, every
+    tensor in x's dtype.  Pass h=residual for an in-place residual update."""
+    dt = _row_dtype(x)
+    _need(x, "x", dt)
+    _need(residual, "residual", dt)
+    _need(w, "w", dt)
     if x.dim() != 2 or residual.shape != x.shape or w.dim() != 1 or w.shape[0] != x.shape[1]:
         raise ValueError("x and residual must be [M, N] and w [N]")
     h = torch.empty_like(x) if h is None else h
     y = torch.empty_like(x) if y is None else y
-    _need(h, "h", torch.bfloat16)
-    _need(y, "y", torch.bfloat16)
+    _need(h, "h", dt)
+    _need(y, "y", dt)
     if h.shape != x.shape or y.shape != x.shape:
         raise ValueError("h and y must have x's shape")
     M, N = x.shape
     L = load()
-    if schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
+    plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if dt == torch.float16:
+        if plain:
+            _check(L.add_rmsnorm_fwd_f16(x.data_ptr(), residual.data_ptr(), w.data_ptr(), eps, M,
+                                         N, h.data_ptr(), y.data_ptr(), _stream(stream)),
+                   "add_rmsnorm_fwd_f16")
+        else:
+            _row_ex("row_norm_fwd_ex", RN_OP_ADD_RMSNORM, dt, x, residual, w, None, eps, M, N, h,
+                    y, schedule, wait_timeout_ns, debug_flags, stream)
+        return h, y
+    if plain:
         rc = L.add_rmsnorm_fwd(x.data_ptr(), residual.data_ptr(), w.data_ptr(), eps, M, N,
                                h.data_ptr(), y.data_ptr(), _stream(stream))
     else:

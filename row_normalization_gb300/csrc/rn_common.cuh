@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,6 +28,32 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+
+// ---- element formats -----------------------------------------------------------
+// A 16-bit element format: widen the two halves of a packed word to fp32
+// (exact) and narrow two fp32 back with one round-to-nearest-even.
+
+struct Bf16 {
+    static constexpr uint32_t kOne2 = 0x3F803F80u;  // two 1.0
+    __device__ static __forceinline__ float lo(uint32_t u) { return bf_lo(u); }
+    __device__ static __forceinline__ float hi(uint32_t u) { return bf_hi(u); }
+    __device__ static __forceinline__ uint32_t pack(float a, float b) { return pack_bf2(a, b); }
+};
+
+// IEEE binary16: overflow rounds to infinity, subnormals are kept.
+struct F16 {
+    static constexpr uint32_t kOne2 = 0x3C003C00u;  // two 1.0
+    __device__ static __forceinline__ float lo(uint32_t u) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xFFFFu)));
+    }
+    __device__ static __forceinline__ float hi(uint32_t u) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16)));
+    }
+    __device__ static __forceinline__ uint32_t pack(float a, float b) {
+        __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+};
 
 // ---- global memory ----------------------------------------------------------
 

@@ -57,6 +57,32 @@ inline int current_device_index() {
 // Reads (and optionally clears) the status word of the QK translation unit.
 int qk_status(unsigned int *out, int clear);
 
+// One row-normalization call, independent of the element format.
+enum RowOp { ROW_RMS = 0, ROW_L2 = 1, ROW_ADD_RMS = 2, ROW_LN = 3 };
+
+struct RowCall {
+    int op;                // RowOp
+    const uint16_t *x;     // [M, N]
+    const uint16_t *r;     // residual [M, N] (ROW_ADD_RMS)
+    const uint16_t *w;     // weight [N] (all but ROW_L2)
+    const uint16_t *b;     // bias [N] or null (ROW_LN)
+    float eps;
+    int64_t M, N;
+    uint16_t *h;           // x + r out [M, N] (ROW_ADD_RMS)
+    uint16_t *y;           // [M, N]
+    int schedule;
+    uint64_t timeout_ns;
+    int debug_flags;
+    rn_stream_t stream;
+};
+
+// Row kernels instantiated per element format (rows_bf16.cu, rows_f16.cu).
+int rows_run_bf16(const RowCall &c);
+int rows_run_f16(const RowCall &c);
+int rows_status_bf16(unsigned int *out, int clear);
+int rows_status_f16(unsigned int *out, int clear);
+int rows_select_schedule(int op, int64_t M, int64_t N);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int launch_status() {

@@ -1,12 +1,18 @@
-// rmsnorm.cu -- bf16 RMSNorm forward for sm_103a, and the library's status word.
+// row_kernels.cuh -- the row-normalization kernels for sm_103a, written once
+// over a 16-bit element format (bf16 or IEEE fp16; the fp32 arithmetic is the
+// same for both) and instantiated by one translation unit per format.
 //
-// y[r, :] = bf16( x[r, :] * 1/sqrt(sum_j x[r, j]^2 / N + eps) * w[:] )
+//   RMSNorm    y[r, :] = round( x[r, :] * 1/sqrt(sum_j x[r, j]^2 / N + eps) * w[:] )
+//   L2Norm     y[r, :] = round( x[r, :] / max(||x[r, :]||_2, eps) )
+//   add+RMS    h = round(x + res), y = RMSNorm(h)
+//   LayerNorm  y[r, :] = round( (x[r, :] - mean) / sqrt(var + eps) * w[:] + b[:] )
 //
 // "[Inductor] Codegen Gluon", section 3.1: x feeds both the x*x reduction and
 // the x * rstd * weight pass.  Every schedule here reads each element of x
-// from HBM exactly once, keeps it (bf16) in registers or shared memory
+// from HBM exactly once, keeps it (16-bit) in registers or shared memory
 // between the two passes, widens to fp32 at the point of use, and writes each
-// output once with a single bf16 rounding.
+// output once with a single rounding.  Section 3.2 of the same page widens
+// the eligible inputs to fp16 and to rows that are not a power of two wide.
 //
 // Schedules:
 //   warp_rows        one warp per row, the row in registers (N <= 2048).
@@ -18,6 +24,11 @@
 //                    mbarrier); consumer warps pull each unit into registers
 //                    once, release the stage, reduce, and store y.  The
 //                    weight stays in registers for the CTA's whole life.
+//
+// Each including translation unit gets its own status word (g_status) and
+// reads it back through rows_status_word().
+#pragma once
+
 #include "rn_common.cuh"
 #include "rn_host.h"
 
@@ -27,71 +38,82 @@ static __device__ unsigned int g_status = 0u;
 
 __device__ __forceinline__ void raise_status(unsigned int bits) { atomicOr(&g_status, bits); }
 
-// Sum of squares of the 8 bf16 in a 16-byte vector, in fp32 (pairwise).
+// Sum of squares of the 8 elements in a 16-byte vector, in fp32 (pairwise).
+template <class E>
 __device__ __forceinline__ float sumsq8(uint4 v) {
-    float a = bf_lo(v.x) * bf_lo(v.x);
-    a = fmaf(bf_hi(v.x), bf_hi(v.x), a);
-    float b = bf_lo(v.y) * bf_lo(v.y);
-    b = fmaf(bf_hi(v.y), bf_hi(v.y), b);
-    float c = bf_lo(v.z) * bf_lo(v.z);
-    c = fmaf(bf_hi(v.z), bf_hi(v.z), c);
-    float d = bf_lo(v.w) * bf_lo(v.w);
-    d = fmaf(bf_hi(v.w), bf_hi(v.w), d);
+    float a = E::lo(v.x) * E::lo(v.x);
+    a = fmaf(E::hi(v.x), E::hi(v.x), a);
+    float b = E::lo(v.y) * E::lo(v.y);
+    b = fmaf(E::hi(v.y), E::hi(v.y), b);
+    float c = E::lo(v.z) * E::lo(v.z);
+    c = fmaf(E::hi(v.z), E::hi(v.z), c);
+    float d = E::lo(v.w) * E::lo(v.w);
+    d = fmaf(E::hi(v.w), E::hi(v.w), d);
     return (a + b) + (c + d);
 }
 
-// y = bf16((x * rstd) * w) for 8 packed elements.
+// y = round((x * rstd) * w) for 8 packed elements.
+template <class E>
 __device__ __forceinline__ uint4 scale8(uint4 xv, uint4 wv, float rstd) {
     uint4 o;
-    o.x = pack_bf2(bf_lo(xv.x) * rstd * bf_lo(wv.x), bf_hi(xv.x) * rstd * bf_hi(wv.x));
-    o.y = pack_bf2(bf_lo(xv.y) * rstd * bf_lo(wv.y), bf_hi(xv.y) * rstd * bf_hi(wv.y));
-    o.z = pack_bf2(bf_lo(xv.z) * rstd * bf_lo(wv.z), bf_hi(xv.z) * rstd * bf_hi(wv.z));
-    o.w = pack_bf2(bf_lo(xv.w) * rstd * bf_lo(wv.w), bf_hi(xv.w) * rstd * bf_hi(wv.w));
+    o.x = E::pack(E::lo(xv.x) * rstd * E::lo(wv.x), E::hi(xv.x) * rstd * E::hi(wv.x));
+    o.y = E::pack(E::lo(xv.y) * rstd * E::lo(wv.y), E::hi(xv.y) * rstd * E::hi(wv.y));
+    o.z = E::pack(E::lo(xv.z) * rstd * E::lo(wv.z), E::hi(xv.z) * rstd * E::hi(wv.z));
+    o.w = E::pack(E::lo(xv.w) * rstd * E::lo(wv.w), E::hi(xv.w) * rstd * E::hi(wv.w));
     return o;
 }
 
-// h = bf16(x + r) for 8 packed elements.  Each sum of two bf16 is formed in
-// fp32 and rounded once: either the fp32 sum is exact (exponents within 16 of
-// each other) or the smaller addend is below 2^-16 of the larger, too small to
-// reach a bf16 rounding midpoint.  So h is the correctly rounded exact sum.
+// h = round(x + r) for 8 packed elements.  Each sum is formed in fp32 and
+// rounded once, which gives the correctly rounded exact sum in both formats.
+// bf16: the fp32 sum is exact when the exponents are within 16 of each other;
+// otherwise the smaller addend is below 2^-16 of the larger, too small to
+// reach a rounding midpoint.  fp16: both addends are multiples of 2^-24 below
+// 2^16, so the fp32 sum is exact unless the exponents differ by 14 or more,
+// and then the smaller addend stays under a quarter of the larger's half-step
+// (the fp32 result stays on the larger addend's side of every midpoint).
+template <class E>
 __device__ __forceinline__ uint4 add8(uint4 a, uint4 b) {
     uint4 o;
-    o.x = pack_bf2(bf_lo(a.x) + bf_lo(b.x), bf_hi(a.x) + bf_hi(b.x));
-    o.y = pack_bf2(bf_lo(a.y) + bf_lo(b.y), bf_hi(a.y) + bf_hi(b.y));
-    o.z = pack_bf2(bf_lo(a.z) + bf_lo(b.z), bf_hi(a.z) + bf_hi(b.z));
-    o.w = pack_bf2(bf_lo(a.w) + bf_lo(b.w), bf_hi(a.w) + bf_hi(b.w));
+    o.x = E::pack(E::lo(a.x) + E::lo(b.x), E::hi(a.x) + E::hi(b.x));
+    o.y = E::pack(E::lo(a.y) + E::lo(b.y), E::hi(a.y) + E::hi(b.y));
+    o.z = E::pack(E::lo(a.z) + E::lo(b.z), E::hi(a.z) + E::hi(b.z));
+    o.w = E::pack(E::lo(a.w) + E::lo(b.w), E::hi(a.w) + E::hi(b.w));
     return o;
 }
 
 // LayerNorm pieces: sum of 8, sum of squared deviations from `mean`, and
 // y = (x - mean) * rstd * w (+ b) rounded once.
+template <class E>
 __device__ __forceinline__ float sum8(uint4 v) {
-    return ((bf_lo(v.x) + bf_hi(v.x)) + (bf_lo(v.y) + bf_hi(v.y))) +
-           ((bf_lo(v.z) + bf_hi(v.z)) + (bf_lo(v.w) + bf_hi(v.w)));
+    return ((E::lo(v.x) + E::hi(v.x)) + (E::lo(v.y) + E::hi(v.y))) +
+           ((E::lo(v.z) + E::hi(v.z)) + (E::lo(v.w) + E::hi(v.w)));
 }
 
+template <class E>
 __device__ __forceinline__ float sqdev8(uint4 v, float m) {
-    float a = bf_lo(v.x) - m, b = bf_hi(v.x) - m, c = bf_lo(v.y) - m, d = bf_hi(v.y) - m;
-    float e = bf_lo(v.z) - m, f = bf_hi(v.z) - m, g = bf_lo(v.w) - m, h = bf_hi(v.w) - m;
+    float a = E::lo(v.x) - m, b = E::hi(v.x) - m, c = E::lo(v.y) - m, d = E::hi(v.y) - m;
+    float e = E::lo(v.z) - m, f = E::hi(v.z) - m, g = E::lo(v.w) - m, h = E::hi(v.w) - m;
     return ((a * a + b * b) + (c * c + d * d)) + ((e * e + f * f) + (g * g + h * h));
 }
 
 // Same, on fp32 pairs (Blackwell FADD2/FMUL2/FFMA2): per pair one subtract,
 // one multiply by rstd, one fused multiply-add with (w, b).
+template <class E>
 __device__ __forceinline__ uint32_t ln2w(uint32_t x, uint32_t w, uint32_t b, float2 nm, float2 r) {
-    const float2 d = __fmul2_rn(__fadd2_rn(make_float2(bf_lo(x), bf_hi(x)), nm), r);
-    const float2 y = __ffma2_rn(d, make_float2(bf_lo(w), bf_hi(w)), make_float2(bf_lo(b), bf_hi(b)));
-    return pack_bf2(y.x, y.y);
+    const float2 d = __fmul2_rn(__fadd2_rn(make_float2(E::lo(x), E::hi(x)), nm), r);
+    const float2 y = __ffma2_rn(d, make_float2(E::lo(w), E::hi(w)), make_float2(E::lo(b), E::hi(b)));
+    return E::pack(y.x, y.y);
 }
 
+template <class E>
 __device__ __forceinline__ uint4 ln8(uint4 xv, uint4 wv, uint4 bv, float m, float rstd) {
     const float2 nm = make_float2(-m, -m);
     const float2 r = make_float2(rstd, rstd);
     uint4 o;
-    o.x = ln2w(xv.x, wv.x, bv.x, nm, r);
-    o.y = ln2w(xv.y, wv.y, bv.y, nm, r);
-    o.z = ln2w(xv.z, wv.z, bv.z, nm, r);
-    o.w = ln2w(xv.w, wv.w, bv.w, nm, r);
+    o.x = ln2w<E>(xv.x, wv.x, bv.x, nm, r);
+    o.y = ln2w<E>(xv.y, wv.y, bv.y, nm, r);
+    o.z = ln2w<E>(xv.z, wv.z, bv.z, nm, r);
+    o.w = ln2w<E>(xv.w, wv.w, bv.w, nm, r);
     return o;
 }
 
@@ -111,17 +133,18 @@ __device__ __forceinline__ float row_scale(float ss, int N, float eps, int l2) {
     return sqrtf(ss) > eps ? __frsqrt_rn(ss) : 1.0f / eps;
 }
 
-// Weight chunk, or eight ones (bf16 1.0 = 0x3F80) when there is no weight.
+// Weight chunk, or eight ones in the element format when there is no weight.
+template <class E>
 __device__ __forceinline__ uint4 weight16(const uint16_t *w, int c) {
-    return w ? ld_ro16(w + 8 * c) : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    return w ? ld_ro16(w + 8 * c) : make_uint4(E::kOne2, E::kOne2, E::kOne2, E::kOne2);
 }
 
 // ---------------------------------------------------------------------------
 // warp_rows: one warp per row; lane l holds 16-byte chunks l, l+32, ...
 // ---------------------------------------------------------------------------
-// With ADD, the row is h = bf16(x + r) (stored to h_out) and y = rmsnorm(h).
+// With ADD, the row is h = round(x + r) (stored to h_out) and y = rmsnorm(h).
 // With LN, y = layernorm(x) = (x - mean) * rstd * w + b (b may be null).
-template <int VPT, bool ADD, bool LN>
+template <class E, int VPT, bool ADD, bool LN>
 __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
@@ -145,7 +168,7 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
                 if (c < cpr) {
-                    v[i] = add8(v[i], ld_stream16(r + row * N + 8 * c));
+                    v[i] = add8<E>(v[i], ld_stream16(r + row * N + 8 * c));
                     st16(h_out + row * N + 8 * c, v[i]);
                 }
             }
@@ -154,28 +177,28 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
         if constexpr (LN) {
             float s1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) s1 += sum8(v[i]);  // absent chunks are zero
+            for (int i = 0; i < VPT; ++i) s1 += sum8<E>(v[i]);  // absent chunks are zero
             const float mean = warp_sum(s1) / static_cast<float>(N);
             float s2 = 0.f;
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
-                if (lane + 32 * i < cpr) s2 += sqdev8(v[i], mean);
+                if (lane + 32 * i < cpr) s2 += sqdev8<E>(v[i], mean);
             const float rstd = row_rstd(warp_sum(s2), N, eps);
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
-                if (c < cpr) st16(yr + 8 * c, ln8(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
+                if (c < cpr) st16(yr + 8 * c, ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
             }
         } else {
             float ss = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
+            for (int i = 0; i < VPT; ++i) ss += sumsq8<E>(v[i]);
             ss = warp_sum(ss);
             const float rstd = row_scale(ss, N, eps, l2);
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
-                if (c < cpr) st16(yr + 8 * c, scale8(v[i], weight16(w, c), rstd));
+                if (c < cpr) st16(yr + 8 * c, scale8<E>(v[i], weight16<E>(w, c), rstd));
             }
         }
     }
@@ -184,7 +207,7 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
 // ---------------------------------------------------------------------------
 // cta_rows: one CTA per row; thread t holds chunks t, t+nt, ...
 // ---------------------------------------------------------------------------
-template <int VPT, int MAXT, bool ADD, bool LN>
+template <class E, int VPT, int MAXT, bool ADD, bool LN>
 __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                                                             const uint16_t *__restrict__ w,
                                                             float eps, int64_t M, int N,
@@ -211,7 +234,7 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
                 if (c < cpr) {
-                    v[i] = add8(v[i], ld_stream16(r + row * N + 8 * c));
+                    v[i] = add8<E>(v[i], ld_stream16(r + row * N + 8 * c));
                     st16(h_out + row * N + 8 * c, v[i]);
                 }
             }
@@ -222,7 +245,7 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             // over the register-resident row, two CTA reductions.
             float s1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) s1 += sum8(v[i]);  // absent chunks are zero
+            for (int i = 0; i < VPT; ++i) s1 += sum8<E>(v[i]);  // absent chunks are zero
             s1 = warp_sum(s1);
             if ((tid & 31) == 0) red[par][tid >> 5] = s1;
             __syncthreads();
@@ -232,7 +255,7 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             float s2 = 0.f;
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
-                if (tid + nt * i < cpr) s2 += sqdev8(v[i], mean);
+                if (tid + nt * i < cpr) s2 += sqdev8<E>(v[i], mean);
             s2 = warp_sum(s2);
             if ((tid & 31) == 0) red2[par][tid >> 5] = s2;
             __syncthreads();
@@ -243,13 +266,13 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
                 if (c < cpr)
-                    st16(yr + 8 * c, ln8(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
+                    st16(yr + 8 * c, ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
             }
             continue;
         }
         float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) ss += sumsq8(v[i]);
+        for (int i = 0; i < VPT; ++i) ss += sumsq8<E>(v[i]);
         ss = warp_sum(ss);
         if ((tid & 31) == 0) red[par][tid >> 5] = ss;
         __syncthreads();
@@ -262,19 +285,19 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
-                if (c < cpr) wv[i] = weight16(w, c);
+                if (c < cpr) wv[i] = weight16<E>(w, c);
             }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
-                if (c < cpr) st16(yr + 8 * c, scale8(v[i], wv[i], rstd));
+                if (c < cpr) st16(yr + 8 * c, scale8<E>(v[i], wv[i], rstd));
             }
         } else {
             // 64 registers a thread at 1024 threads: stream the weights
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
-                if (c < cpr) st16(yr + 8 * c, scale8(v[i], weight16(w, c), rstd));
+                if (c < cpr) st16(yr + 8 * c, scale8<E>(v[i], weight16<E>(w, c), rstd));
             }
         }
         // red[par] is rewritten two rows later, after the next barrier: safe.
@@ -317,7 +340,7 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, i
 template <int VPR, int R, int NT>
 constexpr int bulk_max_threads() { return NT > 0 ? NT + 32 : (NT == 0 ? 288 : 544); }
 
-template <int VPR, int R, int NT, bool ADD, bool LN>
+template <class E, int VPR, int R, int NT, bool ADD, bool LN>
 __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
     rms_persistent_bulk_kernel(const BulkArgs a) {
     constexpr bool GENERIC = NT <= 0;
@@ -410,7 +433,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
     uint4 wv[VPR];
 #pragma unroll
     for (int j = 0; j < VPR; ++j)
-        wv[j] = live(tid, j) ? weight16(a.w, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
+        wv[j] = live(tid, j) ? weight16<E>(a.w, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
     uint4 bv[LN ? VPR : 1];  // LayerNorm bias, held like the weights
     if constexpr (LN) {
 #pragma unroll
@@ -422,7 +445,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         int64_t r0;
         int rows;
         sched.unit(bid, k, &r0, &rows);
-        // Keep the weights packed (bf16) across rows: without this the
+        // Keep the weights packed (16-bit) across rows: without this the
         // compiler hoists their fp32 widening out of the loop and doubles
         // the register footprint.
 #pragma unroll
@@ -452,7 +475,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             for (int rr = 0; rr < R; ++rr)
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
-                    xv[rr][j] = add8(xv[rr][j],
+                    xv[rr][j] = add8<E>(xv[rr][j],
                                      (ok && live(tid, j))
                                          ? ld_shared16(st + (R + rr) * row_bytes + 16u * (tid + j * nt))
                                          : make_uint4(0u, 0u, 0u, 0u));
@@ -483,7 +506,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             for (int rr = 0; rr < R; ++rr) {
                 float acc = 0.f;
 #pragma unroll
-                for (int j = 0; j < VPR; ++j) acc += sum8(xv[rr][j]);
+                for (int j = 0; j < VPR; ++j) acc += sum8<E>(xv[rr][j]);
                 s1[rr] = warp_sum(acc);
             }
             float *rb1 = red + (k & 1) * R * 32;
@@ -508,7 +531,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
                 float acc = 0.f;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
-                    if (live(tid, j)) acc += sqdev8(xv[rr][j], mean[rr]);
+                    if (live(tid, j)) acc += sqdev8<E>(xv[rr][j], mean[rr]);
                 s1[rr] = warp_sum(acc);
             }
             if (lane == 0) {
@@ -530,7 +553,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
                         if (live(tid, j))
-                            st16(yr + 8 * (tid + j * nt), ln8(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
+                            st16(yr + 8 * (tid + j * nt), ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
                 }
             }
             continue;
@@ -540,7 +563,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         for (int rr = 0; rr < R; ++rr) {
             float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < VPR; ++j) acc += sumsq8(xv[rr][j]);
+            for (int j = 0; j < VPR; ++j) acc += sumsq8<E>(xv[rr][j]);
             ss[rr] = warp_sum(acc);
         }
         // Same for x: hold it packed across the barrier, widen again after.
@@ -572,7 +595,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
                 uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
-                    if (live(tid, j)) st16(yr + 8 * (tid + j * nt), scale8(xv[rr][j], wv[j], rstd));
+                    if (live(tid, j)) st16(yr + 8 * (tid + j * nt), scale8<E>(xv[rr][j], wv[j], rstd));
             }
         }
     }
@@ -597,7 +620,7 @@ struct RowJob {
     int l2;             // L2Norm instead of RMSNorm (w may be null: unit weights)
 };
 
-template <bool ADD, bool LN>
+template <class E, bool ADD, bool LN>
 static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &dev) {
     const int cpr = j.N >> 3;
     const int wpb = 8;
@@ -605,7 +628,7 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 64;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
 #define RN_WARP(V) \
-    rms_warp_rows_kernel<V, ADD, LN><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, \
+    rms_warp_rows_kernel<E, V, ADD, LN><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, \
                                                                  j.h, j.b, j.l2)
     if (cpr <= 32)
         RN_WARP(1);
@@ -621,7 +644,7 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     return launch_status();
 }
 
-template <bool ADD, bool LN>
+template <class E, bool ADD, bool LN>
 static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &dev) {
     const int cpr = j.N >> 3;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 2048;
@@ -633,7 +656,7 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
         return ((t + 31) / 32) * 32;
     };
 #define RN_CTA(V, T)                                                                      \
-    rms_cta_rows_kernel<V, T, ADD, LN><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
+    rms_cta_rows_kernel<E, V, T, ADD, LN><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
                                                                      j.y, j.r, j.h, j.b, j.l2)
     if (cpr <= 512)
         RN_CTA(1, 512);
@@ -734,14 +757,14 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
     return true;
 }
 
-template <int VPR, int R, int NT, bool ADD, bool LN>
+template <class E, int VPR, int R, int NT, bool ADD, bool LN>
 static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_cap,
                             cudaStream_t st, int nt = NT) {
     static std::atomic<int> attr_done[kMaxDevices];
     const int dev = current_device_index();
     if (dev < 0 || dev >= kMaxDevices) return RN_ERR_DEVICE;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<VPR, R, NT, ADD, LN>,
+        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_cap) != cudaSuccess) {
             cudaGetLastError();
@@ -749,11 +772,11 @@ static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_c
         }
         attr_done[dev].store(1, std::memory_order_release);
     }
-    rms_persistent_bulk_kernel<VPR, R, NT, ADD, LN><<<grid, nt + 32, smem, st>>>(a);
+    rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN><<<grid, nt + 32, smem, st>>>(a);
     return launch_status();
 }
 
-template <bool ADD, bool LN>
+template <class E, bool ADD, bool LN>
 static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const DeviceInfo &dev,
                                   uint64_t timeout_ns, int debug_flags) {
     constexpr int NIN = ADD ? 2 : 1;
@@ -780,34 +803,34 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     if (geo.generic) {
         if constexpr (ADD || LN) {  // at most 256 consumers
             switch (geo.vpr) {
-                case 1: return launch_bulk_inst<1, 8, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 2: return launch_bulk_inst<2, 4, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 4: return launch_bulk_inst<4, 2, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 8: return launch_bulk_inst<8, 1, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 1: return launch_bulk_inst<E, 1, 8, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 2: return launch_bulk_inst<E, 2, 4, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 4: return launch_bulk_inst<E, 4, 2, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 8: return launch_bulk_inst<E, 8, 1, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
             }
         } else {  // up to 512 consumers
             switch (geo.vpr) {
-                case 1: return launch_bulk_inst<1, 8, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 2: return launch_bulk_inst<2, 4, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 4: return launch_bulk_inst<4, 2, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 8: return launch_bulk_inst<8, 1, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 1: return launch_bulk_inst<E, 1, 8, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 2: return launch_bulk_inst<E, 2, 4, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 4: return launch_bulk_inst<E, 4, 2, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 8: return launch_bulk_inst<E, 8, 1, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
             }
         }
         return RN_ERR_SHAPE;
     }
     switch (N) {
-        case 1024: return launch_bulk_inst<1, 8, 128, ADD, LN>(a, g, smem, smem_cap, st);
-        case 2048: return launch_bulk_inst<1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 1024: return launch_bulk_inst<E, 1, 8, 128, ADD, LN>(a, g, smem, smem_cap, st);
+        case 2048: return launch_bulk_inst<E, 1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
         case 4096:
-            if constexpr (ADD || LN) return launch_bulk_inst<2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
+            if constexpr (ADD || LN) return launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
             else
-                return geo.R == 4 ? launch_bulk_inst<2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st)
-                                  : launch_bulk_inst<2, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
-        case 8192: return launch_bulk_inst<4, 2, 256, ADD, LN>(a, g, smem, smem_cap, st);
-        case 16384: return launch_bulk_inst<4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
+                return geo.R == 4 ? launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st)
+                                  : launch_bulk_inst<E, 2, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 8192: return launch_bulk_inst<E, 4, 2, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 16384: return launch_bulk_inst<E, 4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
         case 32768:
             if constexpr (!ADD && !LN)
-                return launch_bulk_inst<8, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
+                return launch_bulk_inst<E, 8, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
             break;
     }
     return RN_ERR_SHAPE;
@@ -830,7 +853,7 @@ static int check_rows(int64_t M, int64_t N) {
     return RN_OK;
 }
 
-template <bool ADD, bool LN>
+template <class E, bool ADD, bool LN>
 static int rows_dispatch(const RowJob &j, int schedule, uint64_t timeout_ns, int debug_flags,
                          rn_stream_t stream) {
     if (schedule < RN_SCHED_AUTO || schedule > RN_SCHED_PERSIST_BULK) return RN_ERR_ARG;
@@ -839,177 +862,68 @@ static int rows_dispatch(const RowJob &j, int schedule, uint64_t timeout_ns, int
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, LN, *dev);
     switch (schedule) {
-        case RN_SCHED_WARP_ROW: return launch_warp_rows<ADD, LN>(j, st, *dev);
-        case RN_SCHED_CTA_ROW: return launch_cta_rows<ADD, LN>(j, st, *dev);
+        case RN_SCHED_WARP_ROW: return launch_warp_rows<E, ADD, LN>(j, st, *dev);
+        case RN_SCHED_CTA_ROW: return launch_cta_rows<E, ADD, LN>(j, st, *dev);
         case RN_SCHED_PERSIST_BULK:
-            return launch_persistent_bulk<ADD, LN>(j, st, *dev, timeout_ns, debug_flags);
+            return launch_persistent_bulk<E, ADD, LN>(j, st, *dev, timeout_ns, debug_flags);
     }
     return RN_ERR_ARG;
 }
 
-static int rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N,
-                            rn_bf16 *y, int schedule, uint64_t timeout_ns, int debug_flags,
-                            rn_stream_t stream) {
-    const int rc = check_rows(M, N);
+// Validates one call and launches it in the element format E.
+template <class E>
+static int rows_run(const RowCall &c) {
+    const int rc = check_rows(c.M, c.N);
     if (rc != RN_OK) return rc;
-    if (M == 0) return RN_OK;
-    if (!x || !w || !y) return RN_ERR_NULL;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return RN_ERR_ALIGN;
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, nullptr, 0};
-    return rows_dispatch<false, false>(j, schedule, timeout_ns, debug_flags, stream);
-}
-
-static int l2norm_dispatch(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
-                           int schedule, uint64_t timeout_ns, int debug_flags,
-                           rn_stream_t stream) {
-    const int rc = check_rows(M, N);
-    if (rc != RN_OK) return rc;
-    if (M == 0) return RN_OK;
-    if (!x || !y) return RN_ERR_NULL;
-    if (!aligned16(x) || !aligned16(y)) return RN_ERR_ALIGN;
-    const RowJob j{x, nullptr, eps, M, static_cast<int>(N), y, nullptr, nullptr, nullptr, 1};
-    return rows_dispatch<false, false>(j, schedule, timeout_ns, debug_flags, stream);
-}
-
-static int add_rmsnorm_dispatch(const rn_bf16 *x, const rn_bf16 *res, const rn_bf16 *w, float eps,
-                                int64_t M, int64_t N, rn_bf16 *h, rn_bf16 *y, int schedule,
-                                uint64_t timeout_ns, int debug_flags, rn_stream_t stream) {
-    const int rc = check_rows(M, N);
-    if (rc != RN_OK) return rc;
-    if (M == 0) return RN_OK;
-    if (!x || !res || !w || !h || !y) return RN_ERR_NULL;
-    if (!aligned16(x) || !aligned16(res) || !aligned16(w) || !aligned16(h) || !aligned16(y))
+    if (c.op < ROW_RMS || c.op > ROW_LN) return RN_ERR_ARG;
+    if (c.M == 0) return RN_OK;
+    const bool need_w = c.op != ROW_L2;
+    const bool add = c.op == ROW_ADD_RMS;
+    if (!c.x || !c.y || (need_w && !c.w) || (add && (!c.r || !c.h))) return RN_ERR_NULL;
+    if (!aligned16(c.x) || !aligned16(c.y) || (c.w && !aligned16(c.w)) ||
+        (add && (!aligned16(c.r) || !aligned16(c.h))) || (c.op == ROW_LN && c.b && !aligned16(c.b)))
         return RN_ERR_ALIGN;
-    if (h == y) return RN_ERR_ARG;  // two different outputs
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, res, h, nullptr, 0};
-    return rows_dispatch<true, false>(j, schedule, timeout_ns, debug_flags, stream);
-}
-
-static int layernorm_dispatch(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps,
-                              int64_t M, int64_t N, rn_bf16 *y, int schedule,
-                              uint64_t timeout_ns, int debug_flags, rn_stream_t stream) {
-    const int rc = check_rows(M, N);
-    if (rc != RN_OK) return rc;
-    if (M == 0) return RN_OK;
-    if (!x || !w || !y) return RN_ERR_NULL;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (b && !aligned16(b)))
-        return RN_ERR_ALIGN;
-    const RowJob j{x, w, eps, M, static_cast<int>(N), y, nullptr, nullptr, b, 0};
-    return rows_dispatch<false, true>(j, schedule, timeout_ns, debug_flags, stream);
-}
-
-}  // namespace rn
-
-extern "C" {
-
-int rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N, rn_bf16 *y,
-                rn_stream_t stream) {
-    return rn::rmsnorm_dispatch(x, w, eps, M, N, y, RN_SCHED_AUTO, 0, 0, stream);
-}
-
-int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N,
-                      rn_bf16 *y, int schedule, uint64_t wait_timeout_ns, int debug_flags,
-                      rn_stream_t stream) {
-    return rn::rmsnorm_dispatch(x, w, eps, M, N, y, schedule, wait_timeout_ns, debug_flags,
-                                stream);
-}
-
-int rmsnorm_select_schedule(int64_t M, int64_t N) {
-    if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
-    const rn::DeviceInfo *dev = rn::current_device_info();
-    if (!dev) return RN_ERR_DEVICE;
-    return rn::auto_schedule(M, static_cast<int>(N), false, false, *dev);
-}
-
-int l2norm_fwd(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
-               rn_stream_t stream) {
-    return rn::l2norm_dispatch(x, eps, M, N, y, RN_SCHED_AUTO, 0, 0, stream);
-}
-
-int l2norm_fwd_sched(const rn_bf16 *x, float eps, int64_t M, int64_t N, rn_bf16 *y,
-                     int schedule, uint64_t wait_timeout_ns, int debug_flags,
-                     rn_stream_t stream) {
-    return rn::l2norm_dispatch(x, eps, M, N, y, schedule, wait_timeout_ns, debug_flags, stream);
-}
-
-int layernorm_fwd(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps, int64_t M,
-                  int64_t N, rn_bf16 *y, rn_stream_t stream) {
-    return rn::layernorm_dispatch(x, w, b, eps, M, N, y, RN_SCHED_AUTO, 0, 0, stream);
-}
-
-int layernorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, const rn_bf16 *b, float eps,
-                        int64_t M, int64_t N, rn_bf16 *y, int schedule, uint64_t wait_timeout_ns,
-                        int debug_flags, rn_stream_t stream) {
-    return rn::layernorm_dispatch(x, w, b, eps, M, N, y, schedule, wait_timeout_ns, debug_flags,
-                                  stream);
-}
-
-int add_rmsnorm_select_schedule(int64_t M, int64_t N) {
-    if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
-    const rn::DeviceInfo *dev = rn::current_device_info();
-    if (!dev) return RN_ERR_DEVICE;
-    return rn::auto_schedule(M, static_cast<int>(N), true, false, *dev);
-}
-
-int layernorm_select_schedule(int64_t M, int64_t N) {
-    if (rn::check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
-    const rn::DeviceInfo *dev = rn::current_device_info();
-    if (!dev) return RN_ERR_DEVICE;
-    return rn::auto_schedule(M, static_cast<int>(N), false, true, *dev);
-}
-
-int add_rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *residual, const rn_bf16 *w, float eps,
-                    int64_t M, int64_t N, rn_bf16 *h_out, rn_bf16 *y, rn_stream_t stream) {
-    return rn::add_rmsnorm_dispatch(x, residual, w, eps, M, N, h_out, y, RN_SCHED_AUTO, 0, 0,
-                                    stream);
-}
-
-int add_rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *residual, const rn_bf16 *w,
-                          float eps, int64_t M, int64_t N, rn_bf16 *h_out, rn_bf16 *y,
-                          int schedule, uint64_t wait_timeout_ns, int debug_flags,
-                          rn_stream_t stream) {
-    return rn::add_rmsnorm_dispatch(x, residual, w, eps, M, N, h_out, y, schedule,
-                                    wait_timeout_ns, debug_flags, stream);
-}
-
-int rn_device_status(unsigned int *out, int clear) {
-    if (!out) return RN_ERR_NULL;
-    if (cudaDeviceSynchronize() != cudaSuccess) {
-        cudaGetLastError();
-        return RN_ERR_DEVICE;
+    if (add && c.h == c.y) return RN_ERR_ARG;  // two different outputs
+    RowJob j{c.x, c.op == ROW_L2 ? nullptr : c.w, c.eps, c.M, static_cast<int>(c.N), c.y,
+             nullptr, nullptr, nullptr, c.op == ROW_L2 ? 1 : 0};
+    if (add) {
+        j.r = c.r;
+        j.h = c.h;
+        return rows_dispatch<E, true, false>(j, c.schedule, c.timeout_ns, c.debug_flags, c.stream);
     }
+    if (c.op == ROW_LN) {
+        j.b = c.b;
+        return rows_dispatch<E, false, true>(j, c.schedule, c.timeout_ns, c.debug_flags, c.stream);
+    }
+    return rows_dispatch<E, false, false>(j, c.schedule, c.timeout_ns, c.debug_flags, c.stream);
+}
+
+// The schedule rows_run picks in RN_SCHED_AUTO (the same for both formats:
+// only the element size enters the geometry).
+static int rows_select(int op, int64_t M, int64_t N) {
+    if (check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
+    const DeviceInfo *dev = current_device_info();
+    if (!dev) return RN_ERR_DEVICE;
+    return auto_schedule(M, static_cast<int>(N), op == ROW_ADD_RMS, op == ROW_LN, *dev);
+}
+
+// Reads (and optionally clears) this translation unit's status word; the
+// caller has synchronised the device.
+static int rows_status_word(unsigned int *out, int clear) {
     unsigned int v = 0;
-    if (cudaMemcpyFromSymbol(&v, rn::g_status, sizeof v) != cudaSuccess) {
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess) {
         cudaGetLastError();
         return RN_ERR_DEVICE;
     }
     if (clear) {
         const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(rn::g_status, &zero, sizeof zero) != cudaSuccess) {
+        if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) {
             cudaGetLastError();
             return RN_ERR_DEVICE;
         }
     }
-    unsigned int q = 0;
-    const int rc = rn::qk_status(&q, clear);
-    if (rc != RN_OK) return rc;
-    *out = v | q;
+    *out = v;
     return RN_OK;
 }
 
-const char *rn_error_string(int code) {
-    switch (code) {
-        case RN_OK: return "ok";
-        case RN_ERR_NULL: return "a required pointer is NULL";
-        case RN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
-        case RN_ERR_SHAPE: return "unsupported or inconsistent sizes";
-        case RN_ERR_LAUNCH: return "CUDA kernel launch failed";
-        case RN_ERR_DEVICE: return "no usable CUDA device";
-        case RN_ERR_ARG: return "invalid argument";
-    }
-    return "unknown status code";
-}
-
-int rn_version(void) { return 100; }
-
-}  // extern "C"
+}  // namespace rn

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for bf16 row normalization.
+"""Seeded synthetic inputs for row normalization (bf16, or fp16 for the row norms).
 
 This module only draws random numbers; it holds none of the normalisation
 or rotary arithmetic.  The same tensors feed the CUDA library and the CPU
@@ -11,8 +11,9 @@ oracle.  Every distribution follows the workloads the pages measure:
   1 + 0.1 * N(0, 1); positions either 0..T-1 or uniform in [0, max_pos).
 
 Seeds: x / qkv = seed, w / wq = seed + 1, outlier rows = seed + 2,
-wk = seed + 3, positions = seed + 4.  fp32 draws are rounded to bf16 with
-round-to-nearest-even (``Tensor.to(torch.bfloat16)``).
+wk = seed + 3, positions = seed + 4.  fp32 draws are rounded to the element
+format (bf16 by default, or ``dtype=torch.float16``) with round-to-nearest-even
+(``Tensor.to``); the fp16 draws are the same fp32 numbers rounded to fp16.
 
 ``device="cuda"`` draws on the GPU (torch's Philox generator), which the
 large workloads need; ``device="cpu"`` draws on the host.  The two devices
@@ -32,29 +33,31 @@ def _gen(device, seed: int) -> torch.Generator:
 
 
 def rmsnorm_inputs(M: int, N: int, *, outlier_frac: float = 0.0, device="cpu",
-                   seed: int = 0):
-    """Return (x [M, N] bf16, w [N] bf16) on ``device``."""
+                   seed: int = 0, dtype: torch.dtype = torch.bfloat16):
+    """Return (x [M, N], w [N]) in ``dtype`` on ``device``."""
     x = torch.randn(M, N, generator=_gen(device, seed), device=device,
                     dtype=torch.float32)
     k = int(round(outlier_frac * M))
     if k > 0:
         rows = torch.randperm(M, generator=_gen("cpu", seed + 2))[:k]
         x[rows.to(x.device)] *= 100.0
-    x = x.to(torch.bfloat16)
-    w = norm_weight(N, device=device, seed=seed + 1)
+    x = x.to(dtype)
+    w = norm_weight(N, device=device, seed=seed + 1, dtype=dtype)
     return x, w
 
 
-def norm_weight(n: int, *, device="cpu", seed: int = 1) -> torch.Tensor:
-    """w = 1 + 0.1 * N(0, 1), rounded to bf16."""
+def norm_weight(n: int, *, device="cpu", seed: int = 1,
+                dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """w = 1 + 0.1 * N(0, 1), rounded to ``dtype``."""
     g = torch.randn(n, generator=_gen(device, seed), device=device, dtype=torch.float32)
-    return (1.0 + 0.1 * g).to(torch.bfloat16)
+    return (1.0 + 0.1 * g).to(dtype)
 
 
-def norm_bias(n: int, *, device="cpu", seed: int = 5) -> torch.Tensor:
-    """b = 0.1 * N(0, 1), rounded to bf16 (LayerNorm's affine shift)."""
+def norm_bias(n: int, *, device="cpu", seed: int = 5,
+              dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """b = 0.1 * N(0, 1), rounded to ``dtype`` (LayerNorm's affine shift)."""
     g = torch.randn(n, generator=_gen(device, seed), device=device, dtype=torch.float32)
-    return (0.1 * g).to(torch.bfloat16)
+    return (0.1 * g).to(dtype)
 
 
 def qkv_inputs(T: int, Hq: int, Hkv: int, D: int, *, positions: str = "arange",
@@ -82,7 +85,7 @@ def qkv_inputs(T: int, Hq: int, Hkv: int, D: int, *, positions: str = "arange",
 
 
 def bf16_bits(t: torch.Tensor):
-    """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
+    """16-bit (bf16 or fp16) tensor -> numpy uint16 bit patterns (host copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
 
 

@@ -1,25 +1,38 @@
-"""Element-by-element parity of CUDA bf16 outputs against the oracle.
+"""Element-by-element parity of CUDA 16-bit outputs against the oracle.
 
-Tolerance (the stated bar for floating-point outputs): every element obeys
+Tolerance for bf16 (the stated bar for floating-point outputs): every element
+obeys
     |gpu - oracle| <= 2^-7 * |oracle| + 1e-6,
 no element is more than one bf16 step (ulp) away from the oracle's rounded
 value unless it is also within 1e-6 of it (values next to zero, where a
 rotation's fp32 cancellation legitimately moves more than one step), and at
 most 0.1% of all elements are exactly one step away.  Steps are counted on
-the sign-magnitude order of bf16 bit patterns, so +0 and -0 are 0 apart.
+the sign-magnitude order of the bit patterns, so +0 and -0 are 0 apart.
+Identical bit patterns (infinities included) always agree.
+
+fp16 outputs carry the same fp32 arithmetic to a format with 3 more
+significand bits.  An output moves by one step only when the kernel's
+relative error eps_k straddles a rounding midpoint; for a value with relative
+step u that happens with probability about 2 * eps_k / u.  bf16 has
+u > 2^-8, so the 0.1% budget allows eps_k up to about 2^-19; fp16 has
+u > 2^-11, so the same eps_k gives 8 times the fraction: the fp16 budget is
+2^-7 (0.78%) one-step elements, and each element within one fp16 step
+(2^-10 relative) of the oracle.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from tests.exact import bits_to_f64, ulp_distance_bf16
+from tests.exact import bits_to_f64, f16_bits_to_f64, ulp_distance_bf16
 
 ABS_FLOOR = 1e-6
 REL_BOUND = 2.0**-7
 MAX_ONE_ULP_FRACTION = 1e-3
+REL_BOUND_F16 = 2.0**-10
+MAX_ONE_ULP_FRACTION_F16 = 2.0**-7
 
 
-def parity_report(gpu_bits, ref_bits, abs_floor=None) -> dict:
+def parity_report(gpu_bits, ref_bits, abs_floor=None, fmt: str = "bf16") -> dict:
     """`abs_floor` (scalar or per-element array) replaces the 1e-6 absolute
     floor where an operation's own fp32 error bound is larger (LayerNorm rows
     with a large mean: the centring x - mean carries |mean| * 2^-24)."""
@@ -28,14 +41,21 @@ def parity_report(gpu_bits, ref_bits, abs_floor=None) -> dict:
     assert gpu_bits.shape == ref_bits.shape
     floor = ABS_FLOOR if abs_floor is None else np.maximum(
         ABS_FLOOR, np.broadcast_to(np.asarray(abs_floor, dtype=np.float64), gpu_bits.shape))
-    g = bits_to_f64(gpu_bits)
-    r = bits_to_f64(ref_bits)
-    diff = np.abs(g - r)
-    ulp = ulp_distance_bf16(gpu_bits, ref_bits)
+    decode = f16_bits_to_f64 if fmt == "f16" else bits_to_f64
+    rel = REL_BOUND_F16 if fmt == "f16" else REL_BOUND
+    g = decode(gpu_bits)
+    r = decode(ref_bits)
+    with np.errstate(invalid="ignore"):
+        diff = np.abs(g - r)
+    ulp = ulp_distance_bf16(gpu_bits, ref_bits)  # sign-magnitude order: any 16-bit float
     finite = np.isfinite(g) & np.isfinite(r)
-    over_bound = ~(diff <= REL_BOUND * np.abs(r) + floor) | ~finite
-    multi_ulp = (ulp > 1) & (diff > floor)
-    bad = over_bound | multi_ulp
+    # the largest finite value and infinity are one step apart: a kernel
+    # result on the other side of the overflow threshold counts as one step
+    edge = ~finite & (ulp == 1) & ~np.isnan(g) & ~np.isnan(r)
+    with np.errstate(invalid="ignore"):
+        over_bound = (~(diff <= rel * np.abs(r) + floor) | ~finite) & ~edge
+    multi_ulp = (ulp > 1) & ~((diff <= floor) & finite)
+    bad = (over_bound | multi_ulp) & (gpu_bits != ref_bits)
     n = max(1, gpu_bits.size)
     return {
         "n": int(gpu_bits.size),
@@ -43,6 +63,7 @@ def parity_report(gpu_bits, ref_bits, abs_floor=None) -> dict:
         "one_ulp": int((ulp == 1).sum()),
         "one_ulp_frac": float((ulp == 1).sum()) / n,
         "near_zero_multi_ulp": int(((ulp > 1) & (diff <= floor)).sum()),
+        "fmt": fmt,
         "exact": int((ulp == 0).sum()),
         "max_ulp": int(ulp.max()) if ulp.size else 0,
         "first_bad": (np.flatnonzero(bad)[:8].tolist()),
@@ -50,9 +71,11 @@ def parity_report(gpu_bits, ref_bits, abs_floor=None) -> dict:
 
 
 def assert_parity(gpu_bits, ref_bits, what: str = "", abs_floor=None,
-                  max_one_ulp_frac: float = MAX_ONE_ULP_FRACTION) -> dict:
-    rep = parity_report(gpu_bits, ref_bits, abs_floor)
+                  max_one_ulp_frac: float | None = None, fmt: str = "bf16") -> dict:
+    if max_one_ulp_frac is None:
+        max_one_ulp_frac = MAX_ONE_ULP_FRACTION_F16 if fmt == "f16" else MAX_ONE_ULP_FRACTION
+    rep = parity_report(gpu_bits, ref_bits, abs_floor, fmt)
     assert rep["bad"] == 0, f"{what}: {rep['bad']} elements outside tolerance: {rep}"
     assert rep["one_ulp_frac"] <= max_one_ulp_frac, \
-        f"{what}: {rep['one_ulp_frac']:.5%} elements one bf16 step off (> {max_one_ulp_frac:.2%}): {rep}"
+        f"{what}: {rep['one_ulp_frac']:.5%} elements one step off (> {max_one_ulp_frac:.2%}): {rep}"
     return rep

@@ -159,3 +159,62 @@ def test_binding_fails_loudly_without_library(tmp_path):
     finally:
         b._lib = saved
         importlib.invalidate_caches()
+
+
+# ---- fp16 row norms and the general row entry point -----------------------
+
+@pytest.mark.parametrize("M,N,expect", [
+    (4, 7, binding.RN_ERR_SHAPE), (4, 65544, binding.RN_ERR_SHAPE), (-1, 64, binding.RN_ERR_SHAPE),
+    (0, 64, binding.RN_OK),
+])
+def test_f16_entry_points_shape_checks(lib, M, N, expect):
+    assert lib.rmsnorm_fwd_f16(P, P, 1e-6, M, N, P, None) == expect
+    assert lib.l2norm_fwd_f16(P, 1e-6, M, N, P, None) == expect
+    assert lib.add_rmsnorm_fwd_f16(P, P, P, 1e-6, M, N, P, P + 4096, None) == expect
+    assert lib.layernorm_fwd_f16(P, P, None, 1e-6, M, N, P, None) == expect
+
+
+def test_f16_entry_points_null_alignment_and_aliasing(lib):
+    assert lib.rmsnorm_fwd_f16(None, P, 1e-6, 4, 64, P, None) == binding.RN_ERR_NULL
+    assert lib.rmsnorm_fwd_f16(P, P, 1e-6, 4, 64, MISALIGNED, None) == binding.RN_ERR_ALIGN
+    assert lib.l2norm_fwd_f16(MISALIGNED, 1e-6, 4, 64, P, None) == binding.RN_ERR_ALIGN
+    assert lib.add_rmsnorm_fwd_f16(P, None, P, 1e-6, 4, 64, P, P, None) == binding.RN_ERR_NULL
+    assert lib.add_rmsnorm_fwd_f16(P, P, P, 1e-6, 4, 64, P, P, None) == binding.RN_ERR_ARG
+    assert lib.layernorm_fwd_f16(P, P, MISALIGNED, 1e-6, 4, 64, P, None) == binding.RN_ERR_ALIGN
+
+
+def test_row_norm_fwd_ex_checks(lib):
+    ex = lib.row_norm_fwd_ex
+    # unknown op or element format
+    assert ex(4, 0, P, None, P, None, 1e-6, 4, 64, None, P, 0, 0, 0, None) == binding.RN_ERR_ARG
+    assert ex(-1, 0, P, None, P, None, 1e-6, 4, 64, None, P, 0, 0, 0, None) == binding.RN_ERR_ARG
+    assert ex(0, 2, P, None, P, None, 1e-6, 4, 64, None, P, 0, 0, 0, None) == binding.RN_ERR_ARG
+    for dt in (binding.RN_DTYPE_BF16, binding.RN_DTYPE_F16):
+        # pointers an op does not use are ignored: a misaligned residual, h and
+        # bias pass the checks of plain RMSNorm, which then stops at the bad
+        # schedule (checked after the pointers)
+        assert ex(binding.RN_OP_RMSNORM, dt, P, MISALIGNED, P, MISALIGNED, 1e-6, 4, 64,
+                  MISALIGNED, P, 9, 0, 0, None) == binding.RN_ERR_ARG
+        # L2Norm takes no weight
+        assert ex(binding.RN_OP_L2NORM, dt, P, None, None, None, 1e-6, 4, 64, None, P, 9, 0, 0,
+                  None) == binding.RN_ERR_ARG
+        # the fused add needs its residual and h, distinct from y
+        assert ex(binding.RN_OP_ADD_RMSNORM, dt, P, None, P, None, 1e-6, 4, 64, P + 4096, P, 0,
+                  0, 0, None) == binding.RN_ERR_NULL
+        assert ex(binding.RN_OP_ADD_RMSNORM, dt, P, P, P, None, 1e-6, 4, 64, P, P, 0, 0, 0,
+                  None) == binding.RN_ERR_ARG
+        assert ex(binding.RN_OP_LAYERNORM, dt, P, None, P, MISALIGNED, 1e-6, 4, 64, None, P, 0,
+                  0, 0, None) == binding.RN_ERR_ALIGN
+        assert ex(binding.RN_OP_LAYERNORM, dt, P, None, P, None, 1e-6, 0, 64, None, P, 0, 0, 0,
+                  None) == binding.RN_OK
+    assert lib.row_norm_select_schedule(7, 8, 64) == binding.RN_ERR_ARG
+    assert lib.row_norm_select_schedule(0, 8, 7) == binding.RN_ERR_SHAPE
+
+
+def test_binding_rejects_mixed_and_unsupported_dtypes():
+    x = torch.zeros(2, 8, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        binding.rmsnorm_fwd(x, torch.zeros(8), 1e-6)
+    with pytest.raises((TypeError, ValueError)):
+        binding.rmsnorm_fwd(torch.zeros(2, 8, dtype=torch.float16),
+                            torch.zeros(8, dtype=torch.bfloat16), 1e-6)
