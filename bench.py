@@ -41,10 +41,13 @@ if ROOT not in sys.path:
 
 METRIC = "achieved HBM GB/s and % of GB300 peak for bf16 RMSNorm / QK-norm+RoPE"
 SPEC_GBS = 7928.0
+L2_BYTES = 126 * 2**20
 
 RMS_SHAPES = [(M, N) for M in (4096, 8192, 16384, 32768) for N in (4096, 8192, 16384)]
 ADD_SHAPES: list = []   # fused residual add + RMSNorm: only with --only add:MxN
 LN_SHAPES: list = []    # LayerNorm (with bias): only with --only ln:MxN
+L2_SHAPES: list = []    # L2Norm: only with --only l2:MxN
+ROW_DTYPE = "bf16"      # element format of the row norms (--row-dtype f16 for fp16)
 RMS_EPS = 1e-6
 QK_T = 16384
 QK_ROT = (128, 64)
@@ -77,18 +80,25 @@ def ln_bytes(M: int, N: int) -> int:
     return 4 * M * N + 4 * N
 
 
+def l2_bytes(M: int, N: int) -> int:
+    """Ideal bytes of L2Norm: read x, write y (no weight)."""
+    return 4 * M * N
+
+
 def step_bytes() -> int:
     return (sum(rms_bytes(M, N) for M, N in RMS_SHAPES) + sum(qk_bytes(QK_T, r) for r in QK_ROT)
             + sum(add_bytes(M, N) for M, N in ADD_SHAPES)
-            + sum(ln_bytes(M, N) for M, N in LN_SHAPES))
+            + sum(ln_bytes(M, N) for M, N in LN_SHAPES)
+            + sum(l2_bytes(M, N) for M, N in L2_SHAPES))
 
 
 def restrict_workload(spec: str) -> None:
     """--only: keep a subset of the step, e.g. "rms:8192x16384,qk:16384:128",
-    or measure the fused residual add with "add:8192x8192".  Used for
-    profiling one launch; the printed line names the reduced workload."""
-    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD, ADD_SHAPES, LN_SHAPES
-    rms, rot, add, ln = [], [], [], []
+    or measure the fused residual add with "add:8192x8192" (likewise "ln:"
+    for LayerNorm, "l2:" for L2Norm).  Used for profiling one launch; the
+    printed line names the reduced workload."""
+    global RMS_SHAPES, QK_ROT, QK_T, WORKLOAD, ADD_SHAPES, LN_SHAPES, L2_SHAPES
+    rms, rot, add, ln, l2 = [], [], [], [], []
     for item in spec.split(","):
         kind, _, rest = item.partition(":")
         if kind == "rms":
@@ -104,9 +114,12 @@ def restrict_workload(spec: str) -> None:
         elif kind == "ln":
             M, N = rest.split("x")
             ln.append((int(M), int(N)))
+        elif kind == "l2":
+            M, N = rest.split("x")
+            l2.append((int(M), int(N)))
         else:
             raise SystemExit(f"bad --only item {item!r}")
-    RMS_SHAPES, QK_ROT, ADD_SHAPES, LN_SHAPES = rms, tuple(rot), add, ln
+    RMS_SHAPES, QK_ROT, ADD_SHAPES, LN_SHAPES, L2_SHAPES = rms, tuple(rot), add, ln, l2
     WORKLOAD = "subset: " + spec
 
 
@@ -228,20 +241,28 @@ QK_KERNELS = {1: "qk_norm_rope_kernel", 2: "qk_norm_rope_kernel", 4: "qk_norm_ro
 
 def build_inputs(torch, binding, inputs, device):
     """All inputs of one step, resident on the device."""
+    dt = torch.float16 if ROW_DTYPE == "f16" else torch.bfloat16
     rms = []
     for i, (M, N) in enumerate(RMS_SHAPES):
-        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=100 * i)
+        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=100 * i,
+                                     dtype=dt)
         y = torch.empty_like(x)
         rms.append({"M": M, "N": N, "x": x, "w": w, "y": y})
     for i, (M, N) in enumerate(ADD_SHAPES):
-        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=500 + i)
-        r, _ = inputs.rmsnorm_inputs(M, N, device=device, seed=550 + i)
+        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=500 + i,
+                                     dtype=dt)
+        r, _ = inputs.rmsnorm_inputs(M, N, device=device, seed=550 + i, dtype=dt)
         rms.append({"M": M, "N": N, "x": x, "w": w, "y": torch.empty_like(x), "r": r,
                     "h": torch.empty_like(x)})
     for i, (M, N) in enumerate(LN_SHAPES):
-        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=700 + i)
+        x, w = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=700 + i,
+                                     dtype=dt)
         rms.append({"M": M, "N": N, "x": x, "w": w, "y": torch.empty_like(x),
-                    "b": inputs.norm_bias(N, device=device, seed=750 + i)})
+                    "b": inputs.norm_bias(N, device=device, seed=750 + i, dtype=dt)})
+    for i, (M, N) in enumerate(L2_SHAPES):
+        x, _ = inputs.rmsnorm_inputs(M, N, outlier_frac=0.01, device=device, seed=900 + i,
+                                     dtype=dt)
+        rms.append({"M": M, "N": N, "x": x, "y": torch.empty_like(x), "l2": True})
     qk = []
     for j, r in enumerate(QK_ROT):
         qkv, wq, wk, pos = inputs.qkv_inputs(QK_T, HQ, HKV, D, positions="uniform",
@@ -254,6 +275,23 @@ def build_inputs(torch, binding, inputs, device):
 FORCE = {"rms": 0, "qk": 0}  # schedule overrides (--rms-schedule / --qk-schedule)
 
 
+def launch_row(binding, c):
+    if "r" in c:
+        binding.add_rmsnorm_fwd(c["x"], c["r"], c["w"], RMS_EPS, c["h"], c["y"],
+                                schedule=FORCE["rms"])
+    elif "b" in c:
+        binding.layernorm_fwd(c["x"], c["w"], c["b"], 1e-5, c["y"], schedule=FORCE["rms"])
+    elif "l2" in c:
+        binding.l2norm_fwd(c["x"], 1e-12, c["y"], schedule=FORCE["rms"])
+    else:
+        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
+
+
+def launch_qk(binding, c):
+    binding.qk_norm_rope_fwd(c["qkv"], c["wq"], c["wk"], c["table"], c["pos"], HQ, HKV, D,
+                             c["r"], QK_EPS, schedule=FORCE["qk"])
+
+
 def launch_step(binding, rms, qk, events=None):
     """Enqueue one step; optionally record an event before every launch."""
     k = 0
@@ -261,20 +299,80 @@ def launch_step(binding, rms, qk, events=None):
         if events is not None:
             events[k].record()
         k += 1
-        if "r" in c:
-            binding.add_rmsnorm_fwd(c["x"], c["r"], c["w"], RMS_EPS, c["h"], c["y"],
-                                    schedule=FORCE["rms"])
-        elif "b" in c:
-            binding.layernorm_fwd(c["x"], c["w"], c["b"], 1e-5, c["y"], schedule=FORCE["rms"])
-        else:
-            binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
+        launch_row(binding, c)
     for c in qk:
         if events is not None:
             events[k].record()
         k += 1
-        binding.qk_norm_rope_fwd(c["qkv"], c["wq"], c["wk"], c["table"], c["pos"], HQ, HKV, D,
-                                 c["r"], QK_EPS, schedule=FORCE["qk"])
+        launch_qk(binding, c)
     return k
+
+
+def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> list:
+    """Each launch of the step measured on its own, in steady state: `reps`
+    back-to-back launches of one shape, alternating between two sets of
+    activations so nothing is reused from L2 (weights and tables shared).
+    A launch then pays for the dirty L2 lines its predecessor (the same
+    shape) left behind and leaves as many itself, so its DRAM traffic equals
+    its algorithmic bytes.  The in-step per-launch times instead also carry
+    the dirty tail of whichever launch ran before (up to the 126 MiB L2).
+    Beside each: torch's copy of the same number of bytes, timed the same
+    way (the ceiling any single-pass kernel of that size meets)."""
+    out = []
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+
+    def copy_frac(nbytes: int) -> float:
+        # torch's own copy of the same bytes (half read, half written), run
+        # the same way: the ceiling a single-pass kernel of this size reaches
+        n = nbytes // 2 // 16 * 16
+        bufs = [(torch.empty(n, dtype=torch.uint8, device="cuda"),
+                 torch.empty(n, dtype=torch.uint8, device="cuda")) for _ in range(2)]
+        ms = timed(bufs, lambda _b, p: p[1].copy_(p[0]))
+        del bufs
+        return round(2 * n / (ms * 1e-3) / 1e9 / hbm_peak, 4)
+
+    def timed(pair, launch):
+        for i in range(4):
+            launch(binding, pair[i & 1])
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(reps):
+            launch(binding, pair[i & 1])
+        end.record()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / reps
+
+    for c in rms:
+        twin = dict(c)
+        for k in ("x", "r"):
+            if k in c:
+                twin[k] = c[k].clone()
+        for k in ("y", "h"):
+            if k in c:
+                twin[k] = torch.empty_like(c[k])
+        ms = timed((c, twin), launch_row)
+        del twin
+        op = ("add_rmsnorm" if "r" in c else "layernorm" if "b" in c else
+              "l2norm" if "l2" in c else "rmsnorm")
+        b = {"add_rmsnorm": add_bytes, "layernorm": ln_bytes, "l2norm": l2_bytes,
+             "rmsnorm": rms_bytes}[op](c["M"], c["N"])
+        gbs = b / (ms * 1e-3) / 1e9
+        out.append({"op": op, "M": c["M"], "N": c["N"], "us": round(ms * 1e3, 2),
+                    "gbs": round(gbs, 1), "frac_of_measured": round(gbs / hbm_peak, 4),
+                    "copy_same_bytes_frac": copy_frac(b)})
+    for c in qk:
+        twin = dict(c)
+        twin["qkv"] = c["qkv"].clone()
+        ms = timed((c, twin), launch_qk)
+        del twin
+        b = qk_bytes(QK_T, c["r"])
+        gbs = b / (ms * 1e-3) / 1e9
+        out.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
+                    "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                    "frac_of_measured": round(gbs / hbm_peak, 4),
+                    "copy_same_bytes_frac": copy_frac(b)})
+    return out
 
 
 def run_ours(args) -> int:
@@ -343,13 +441,16 @@ def run_ours(args) -> int:
 
     per_shape = []
     for k, c in enumerate(rms):
-        op = "add_rmsnorm" if "r" in c else ("layernorm" if "b" in c else "rmsnorm")
+        op = ("add_rmsnorm" if "r" in c else "layernorm" if "b" in c else
+              "l2norm" if "l2" in c else "rmsnorm")
         select = {"add_rmsnorm": binding.add_rmsnorm_select_schedule,
                   "layernorm": binding.layernorm_select_schedule,
+                  "l2norm": binding.rmsnorm_select_schedule,
                   "rmsnorm": binding.rmsnorm_select_schedule}[op]
         sched = FORCE["rms"] or select(c["M"], c["N"])
-        b = {"add_rmsnorm": add_bytes, "layernorm": ln_bytes, "rmsnorm": rms_bytes}[op](c["M"], c["N"])
-        per_shape.append({"op": op, "M": c["M"], "N": c["N"],
+        b = {"add_rmsnorm": add_bytes, "layernorm": ln_bytes, "l2norm": l2_bytes,
+             "rmsnorm": rms_bytes}[op](c["M"], c["N"])
+        per_shape.append({"op": op, "dtype": ROW_DTYPE, "M": c["M"], "N": c["N"],
                           "kernel": RMS_KERNELS.get(sched, str(sched)),
                           "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
                           "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
@@ -373,10 +474,13 @@ def run_ours(args) -> int:
                 "kernel": dom["kernel"], "launch": dom_wl,
                 "algorithmic_bytes_per_launch": dom["bytes"]}
 
-    e2e = (run_e2e(torch, binding, rms, qk, args, dist, device)
-           if args.e2e_steps > 0 and not ADD_SHAPES and not LN_SHAPES else None)
+    steady = steady_per_shape(torch, binding, rms, qk, args.steady_reps, hbm_peak) \
+        if args.steady_reps > 0 else None
+    plain = not ADD_SHAPES and not LN_SHAPES and not L2_SHAPES and ROW_DTYPE == "bf16"
+    e2e = run_e2e(torch, binding, rms, qk, args, dist, device) if args.e2e_steps > 0 and plain \
+        else None
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and plain:
         cpu = cpu_baseline(budget_s=args.cpu_seconds)
 
     rms_ms = sum(per_launch_ms[:len(RMS_SHAPES)])
@@ -384,12 +488,19 @@ def run_ours(args) -> int:
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": (ROW_DTYPE if ROW_DTYPE == "bf16" or not QK_ROT
+                  else f"{ROW_DTYPE} (row norms), bf16 (qk_norm_rope)"),
         "data": "synthetic (seeded torch generators; see DESIGN.md input recipe)",
         "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step,
                    "launches_per_step": n_launch, "parallelism": f"replicas x{world}",
-                   "l2": ("inputs larger than L2: each buffer is touched once per step and a "
-                          f"step moves {bytes_step / 1e9:.2f} GB, >50x the 126 MiB L2")},
+                   "l2": (("inputs larger than L2: each buffer is touched once per step and a "
+                           f"step moves {bytes_step / 1e9:.2f} GB, "
+                           f"{bytes_step / L2_BYTES:.0f}x the 126 MiB L2")
+                          if bytes_step >= 4 * L2_BYTES else
+                          (f"step of {bytes_step / 1e9:.2f} GB is under 4x the 126 MiB L2: "
+                           "in-step numbers may reuse L2; steady_per_shape alternates two "
+                           "buffer sets"))},
         "frac_of_measured_copy": round(value / world / hbm_peak, 4),
         "frac_of_spec_7928": round(value / world / SPEC_GBS, 4),
         "per_op": {"rmsnorm_sweep_gbs": round(sum(rms_bytes(M, N) for M, N in RMS_SHAPES)
@@ -397,6 +508,7 @@ def run_ours(args) -> int:
                    "qk_norm_rope_gbs": round(sum(qk_bytes(QK_T, r) for r in QK_ROT)
                                              / (qk_ms * 1e-3) / 1e9, 1) if qk_ms else None},
         "per_shape": per_shape,
+        "steady_per_shape": steady,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -635,13 +747,19 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--steady-reps", type=int, default=50,
+                    help="back-to-back launches per shape for steady_per_shape (0: skip)")
     ap.add_argument("--only", default="", help="profile a subset, e.g. rms:8192x16384")
+    ap.add_argument("--row-dtype", choices=("bf16", "f16"), default="bf16",
+                    help="element format of the row norms in the step (the QK op stays bf16)")
     ap.add_argument("--rms-schedule", type=int, default=0, help="force an RN_SCHED_* value")
     ap.add_argument("--qk-schedule", type=int, default=0, help="force an RN_QK_* value")
     args = ap.parse_args()
     FORCE["rms"], FORCE["qk"] = args.rms_schedule, args.qk_schedule
     if args.only:
         restrict_workload(args.only)
+    global ROW_DTYPE
+    ROW_DTYPE = args.row_dtype
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3  # never time without at least three warm-up steps
     if args.impl == "reference":

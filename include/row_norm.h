@@ -43,6 +43,9 @@
  *   - Arithmetic: bf16 inputs are widened to fp32 at the point of use, all
  *     sums and products run in fp32, and each output is rounded once to
  *     bf16 (round to nearest even).
+ *   - Row statistics are fp32 sums: a bf16 row whose sum of squares passes
+ *     the fp32 range (about 3.4e38; values near 2^63 / sqrt(N) and above)
+ *     gets a zero scale, and so zero outputs.
  *   - The row norms also take IEEE fp16 tensors (rn_f16; the *_f16 entry
  *     points and row_norm_fwd_ex): the same fp32 arithmetic, one rounding
  *     to fp16 at the store (overflow to infinity, subnormals kept).

@@ -33,11 +33,22 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 // A 16-bit element format: widen the two halves of a packed word to fp32
 // (exact) and narrow two fp32 back with one round-to-nearest-even.
 
+// Besides widening and narrowing, each format offers sq_acc(acc, u) =
+// acc + lo(u)^2 + hi(u)^2 as two mixed-precision fused multiply-adds on the
+// packed halves (16-bit multiplicands, fp32 addend and result; sm_100 and
+// later): each square is exact in fp32 and no widening instruction is spent.
+
 struct Bf16 {
     static constexpr uint32_t kOne2 = 0x3F803F80u;  // two 1.0
     __device__ static __forceinline__ float lo(uint32_t u) { return bf_lo(u); }
     __device__ static __forceinline__ float hi(uint32_t u) { return bf_hi(u); }
     __device__ static __forceinline__ uint32_t pack(float a, float b) { return pack_bf2(a, b); }
+    __device__ static __forceinline__ float sq_acc(float acc, uint32_t u) {
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+            "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
+            : "+f"(acc) : "r"(u));
+        return acc;
+    }
 };
 
 // IEEE binary16: overflow rounds to infinity, subnormals are kept.
@@ -52,6 +63,12 @@ struct F16 {
     __device__ static __forceinline__ uint32_t pack(float a, float b) {
         __half2 v = __floats2half2_rn(a, b);
         return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __device__ static __forceinline__ float sq_acc(float acc, uint32_t u) {
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+            "fma.rn.f32.f16 %0, l, l, %0;\n\tfma.rn.f32.f16 %0, h, h, %0;\n\t}"
+            : "+f"(acc) : "r"(u));
+        return acc;
     }
 };
 

@@ -38,17 +38,14 @@ static __device__ unsigned int g_status = 0u;
 
 __device__ __forceinline__ void raise_status(unsigned int bits) { atomicOr(&g_status, bits); }
 
-// Sum of squares of the 8 elements in a 16-byte vector, in fp32 (pairwise).
+// Sum of squares of the 8 elements in a 16-byte vector, in fp32 (pairwise):
+// each square is exact, formed straight from the packed halves.
 template <class E>
 __device__ __forceinline__ float sumsq8(uint4 v) {
-    float a = E::lo(v.x) * E::lo(v.x);
-    a = fmaf(E::hi(v.x), E::hi(v.x), a);
-    float b = E::lo(v.y) * E::lo(v.y);
-    b = fmaf(E::hi(v.y), E::hi(v.y), b);
-    float c = E::lo(v.z) * E::lo(v.z);
-    c = fmaf(E::hi(v.z), E::hi(v.z), c);
-    float d = E::lo(v.w) * E::lo(v.w);
-    d = fmaf(E::hi(v.w), E::hi(v.w), d);
+    const float a = E::sq_acc(0.f, v.x);
+    const float b = E::sq_acc(0.f, v.y);
+    const float c = E::sq_acc(0.f, v.z);
+    const float d = E::sq_acc(0.f, v.w);
     return (a + b) + (c + d);
 }
 
@@ -674,17 +671,19 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
     return launch_status();
 }
 
-// Geometry of the persistent schedule, measured on GB300: NT consumer threads
-// x VPR 16-byte chunks cover one row exactly, R rows make a stage, `stages`
-// stages per CTA, `ctas` co-resident CTAs per SM.  Two stages in flight per
-// CTA stream best; deeper rings measured slower (more concurrent DRAM streams,
-// no more bandwidth).  Up to M = 8192 rows the 4096-wide rows run two CTAs
-// per SM with 32 KiB stages: more independent pipelines shorten the ramp that
-// dominates such short launches (measured inside the bench step; for 8192-wide
-// rows the second CTA measured slower).  Larger M runs one CTA per SM.  With
-// the fused residual add a stage carries R rows of x and R rows of r, so R is
-// halved where needed to keep a stage at 64 KiB or less; 32768-wide rows do
-// not fit two such stages and take the CTA-per-row schedule.
+// Geometry of the persistent schedule, measured on GB300 (back-to-back
+// launches of one shape, two alternating buffer sets): NT consumer threads x
+// VPR 16-byte chunks cover one row exactly, R rows make a stage, `stages`
+// stages per CTA, `ctas` co-resident CTAs per SM.  About 64 KiB in flight per
+// SM (two 32 KiB stages) streams best at every width from 4096 to 16384:
+// deeper rings and 64 KiB stages measured slower (more concurrent DRAM
+// streams, no more bandwidth).  4096-wide rows run two CTAs per SM up to
+// M = 8192 rows, where more independent pipelines shorten the ramp that
+// dominates such short launches; launches of 4096 rows take a third stage at
+// widths 8192 and 16384 for the same reason.  With the fused residual add a
+// stage carries R rows of x and R rows of r, so R is halved where needed to
+// keep a stage at 64 KiB or less; 32768-wide rows do not fit two such stages
+// and take the CTA-per-row schedule.
 struct BulkGeometry {
     int nt, vpr, R, stages, ctas;
     bool generic;  // masked instantiation with a run-time consumer count
@@ -745,12 +744,15 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
         }
         return true;
     }
+    // A third stage pays only on the shortest launches (4096 rows), where the
+    // ramp is a larger share of the time.
+    const int short_stages = M <= 4096 ? 3 : 2;
     switch (N) {
         case 1024: *g = {128, 1, 8, 2, 1, false}; break;
         case 2048: *g = {256, 1, 8, 2, 1, false}; break;
-        case 4096: *g = few_rows ? BulkGeometry{256, 2, 4, 2, 2, false} : BulkGeometry{256, 2, 8, 2, 1, false}; break;
-        case 8192: *g = {256, 4, 2, 2, 1, false}; break;
-        case 16384: *g = {512, 4, 1, 2, 1, false}; break;
+        case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1, false}; break;
+        case 8192: *g = {256, 4, 2, short_stages, 1, false}; break;
+        case 16384: *g = {512, 4, 1, short_stages, 1, false}; break;
         case 32768: *g = {512, 8, 1, 2, 1, false}; break;
         default: return false;
     }
@@ -821,11 +823,7 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     switch (N) {
         case 1024: return launch_bulk_inst<E, 1, 8, 128, ADD, LN>(a, g, smem, smem_cap, st);
         case 2048: return launch_bulk_inst<E, 1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
-        case 4096:
-            if constexpr (ADD || LN) return launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
-            else
-                return geo.R == 4 ? launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st)
-                                  : launch_bulk_inst<E, 2, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 4096: return launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
         case 8192: return launch_bulk_inst<E, 4, 2, 256, ADD, LN>(a, g, smem, smem_cap, st);
         case 16384: return launch_bulk_inst<E, 4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
         case 32768:

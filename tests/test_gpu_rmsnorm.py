@@ -194,3 +194,25 @@ def test_non_power_of_two_widths_on_the_ring(N):
     torch.cuda.synchronize()
     assert_parity(bf16_bits(y), want, f"ring N={N}")
     assert canary_intact(buf, pad, 0x7FC1)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_rows_with_extreme_scales(schedule):
+    # Rows from 2^-55 to 2^50 in magnitude (with eps = 0 the tiny rows get
+    # scales up to 2^55), and a weight vector holding 2^70: every output must
+    # still agree with the oracle.
+    N, M = 4096, 2000
+    g = torch.Generator().manual_seed(41)
+    x = torch.randn(M, N, generator=g)
+    scale = torch.tensor([1.0, 2.0**50, 2.0**-55, 2.0**35, 2.0**-35, 2.0**45, 2.0**-38, 1.0])
+    x = (x * scale[torch.arange(M) % len(scale)][:, None]).to(torch.bfloat16)
+    w = rmsnorm_inputs(1, N, seed=42)[1]
+    w_big = w.clone()
+    w_big[777] = 2.0**70
+    for ww in (w, w_big):
+        for eps in (0.0, 1e-6):
+            want = oracle.rmsnorm(bf16_bits(x), bf16_bits(ww), eps)
+            if not eligible(schedule, N):
+                continue
+            y = binding.rmsnorm_fwd(x.cuda(), ww.cuda(), eps, schedule=schedule)
+            assert_parity(bf16_bits(y), want, f"extreme rows eps={eps} sched={schedule}")
