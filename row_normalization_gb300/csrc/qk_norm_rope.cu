@@ -160,6 +160,8 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
     constexpr int B = (D - R) / LPH;
     constexpr int HPW = 32 / LPH;
     static_assert(A * LPH == H2 && B * LPH == D - R && A >= 1, "bad lane layout");
+    pdl_trigger();
+    pdl_wait();
 
     const int lane = threadIdx.x & 31;
     const int sub = lane % LPH;
@@ -473,6 +475,8 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    pdl_trigger();
+    pdl_wait();
     __syncthreads();
 
     const UnitSchedule sched(a.T, gridDim.x, TPS);
@@ -666,6 +670,8 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
 
 // fp64 angle and trig, rounded once to fp32.
 __global__ void rope_table_kernel(double theta, int64_t max_pos, int r, float *out) {
+    pdl_trigger();
+    pdl_wait();
     const int h = r / 2;
     const int64_t n = max_pos * h;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
@@ -695,8 +701,8 @@ static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const De
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7fffffffULL) blocks = 0x7fffffffULL;
-    qk_norm_rope_kernel<D, R, LPH, STYLE><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a);
-    return launch_status();
+    return launch_pdl(qk_norm_rope_kernel<D, R, LPH, STYLE>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kThreads), 0, st, a);
 }
 
 // Largest lanes-per-head <= the request that tiles both rotary halves and
@@ -750,9 +756,8 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     if (grid > a.T) grid = a.T;
     const uint64_t inv_h = ((1ull << 32) + H - 1) / H;
     QkBulkArgs b{a, tps, stages, debug_flags & 1, inv_h, timeout_ns ? timeout_ns : 2000000000ull};
-    qk_persistent_bulk_kernel<D, R, STYLE>
-        <<<static_cast<unsigned>(grid), qk_bulk_consumers<D>() + 32, smem, st>>>(b);
-    return launch_status();
+    return launch_pdl(qk_persistent_bulk_kernel<D, R, STYLE>, dim3(static_cast<unsigned>(grid)),
+                      dim3(qk_bulk_consumers<D>() + 32), smem, st, b);
 }
 
 // Schedule by token count (measured on GB300): one head per warp for 1-2
@@ -913,10 +918,9 @@ int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim, float *cos
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = static_cast<int64_t>(dev->sm_count) * 16;
     if (blocks > cap) blocks = cap;
-    rn::rope_table_kernel<<<static_cast<unsigned>(blocks), 256, 0,
-                            reinterpret_cast<cudaStream_t>(stream)>>>(theta, max_pos, rotary_dim,
-                                                                       cos_sin);
-    return rn::launch_status();
+    return rn::launch_pdl(rn::rope_table_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                          reinterpret_cast<cudaStream_t>(stream), theta, max_pos, rotary_dim,
+                          cos_sin);
 }
 
 }  // extern "C"

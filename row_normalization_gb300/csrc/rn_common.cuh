@@ -72,6 +72,42 @@ struct F16 {
     }
 };
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Every kernel here is launched with programmatic stream serialisation: its
+// CTAs may be scheduled while the previous launch in the stream is still
+// finishing, which hides the launch gap between back-to-back kernels.  Each
+// kernel lets its own successor do the same (pdl_trigger) and then waits,
+// before its first global memory access, until the previous launch has
+// completed and its writes are visible (pdl_wait).  Both are no-ops when the
+// neighbouring launch does not take part.
+
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` with programmatic stream serialisation; RN_OK or
+// RN_ERR_LAUNCH.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...) != cudaSuccess) {
+        cudaGetLastError();
+        return RN_ERR_LAUNCH;
+    }
+    return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_LAUNCH;
+}
+
 // ---- global memory ----------------------------------------------------------
 
 // Read-once 16-byte load (streaming: evict first from L1/L2).

@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                                                             uint16_t *y, const uint16_t *r,
                                                             uint16_t *h_out, const uint16_t *b,
                                                             int l2) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int cpr = N >> 3;
@@ -213,6 +215,8 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                                                             int l2) {
     __shared__ float red[2][32];
     __shared__ float red2[2][32];  // LayerNorm's second reduction
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
     const int nw = nt >> 5;
@@ -375,6 +379,8 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         flags[2] = 0;
         fence_mbar_init();
     }
+    pdl_trigger();
+    pdl_wait();
     __syncthreads();
 
     const UnitSchedule sched(a.M, gridDim.x, R);
@@ -624,21 +630,15 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     const int64_t want = (j.M + wpb - 1) / wpb;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 64;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-#define RN_WARP(V) \
-    rms_warp_rows_kernel<E, V, ADD, LN><<<grid, 32 * wpb, 0, st>>>(j.x, j.w, j.eps, j.M, j.N, j.y, j.r, \
-                                                                 j.h, j.b, j.l2)
-    if (cpr <= 32)
-        RN_WARP(1);
-    else if (cpr <= 64)
-        RN_WARP(2);
-    else if (cpr <= 128)
-        RN_WARP(4);
-    else if (cpr <= 256)
-        RN_WARP(8);
-    else
-        return RN_ERR_SHAPE;
+#define RN_WARP(V)                                                                              \
+    return launch_pdl(rms_warp_rows_kernel<E, V, ADD, LN>, dim3(grid), dim3(32 * wpb), 0, st, j.x, \
+                      j.w, j.eps, j.M, j.N, j.y, j.r, j.h, j.b, j.l2)
+    if (cpr <= 32) RN_WARP(1);
+    if (cpr <= 64) RN_WARP(2);
+    if (cpr <= 128) RN_WARP(4);
+    if (cpr <= 256) RN_WARP(8);
 #undef RN_WARP
-    return launch_status();
+    return RN_ERR_SHAPE;
 }
 
 template <class E, bool ADD, bool LN>
@@ -652,23 +652,16 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
         int t = (cpr + vpt - 1) / vpt;
         return ((t + 31) / 32) * 32;
     };
-#define RN_CTA(V, T)                                                                      \
-    rms_cta_rows_kernel<E, V, T, ADD, LN><<<grid, nthreads(V), 0, st>>>(j.x, j.w, j.eps, j.M, j.N, \
-                                                                     j.y, j.r, j.h, j.b, j.l2)
-    if (cpr <= 512)
-        RN_CTA(1, 512);
-    else if (cpr <= 1024)
-        RN_CTA(2, 512);
-    else if (cpr <= 2048)
-        RN_CTA(4, 512);
-    else if (cpr <= 4096)
-        RN_CTA(8, 512);
-    else if (cpr <= 8192)
-        RN_CTA(8, 1024);
-    else
-        return RN_ERR_SHAPE;
+#define RN_CTA(V, T)                                                                           \
+    return launch_pdl(rms_cta_rows_kernel<E, V, T, ADD, LN>, dim3(grid), dim3(nthreads(V)), 0, st, \
+                      j.x, j.w, j.eps, j.M, j.N, j.y, j.r, j.h, j.b, j.l2)
+    if (cpr <= 512) RN_CTA(1, 512);
+    if (cpr <= 1024) RN_CTA(2, 512);
+    if (cpr <= 2048) RN_CTA(4, 512);
+    if (cpr <= 4096) RN_CTA(8, 512);
+    if (cpr <= 8192) RN_CTA(8, 1024);
 #undef RN_CTA
-    return launch_status();
+    return RN_ERR_SHAPE;
 }
 
 // Geometry of the persistent schedule, measured on GB300 (back-to-back
@@ -774,8 +767,8 @@ static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_c
         }
         attr_done[dev].store(1, std::memory_order_release);
     }
-    rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN><<<grid, nt + 32, smem, st>>>(a);
-    return launch_status();
+    return launch_pdl(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>, dim3(grid), dim3(nt + 32),
+                      smem, st, a);
 }
 
 template <class E, bool ADD, bool LN>
