@@ -303,8 +303,10 @@ enum {
 };
 
 /* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*).
- * `wait_timeout_ns` and `debug_flags` (bit 0 only) act on RN_QK_BULK as on
- * rmsnorm_fwd_sched's persistent schedule; 0 and 0 in normal use. */
+ * `wait_timeout_ns` and `debug_flags` act on RN_QK_BULK as on
+ * rmsnorm_fwd_sched's persistent schedule (bit 0: never issue the copies;
+ * bits 8-12: ring stages, 2 or more; bits 16-21: tokens per stage, 1-32;
+ * a shared-memory overflow is RN_ERR_SHAPE); 0 and 0 in normal use. */
 int qk_norm_rope_fwd_sched(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                            const float *cos_sin, const int64_t *positions,
                            int64_t T, int Hq, int Hkv, int D, int rotary_dim,

@@ -314,6 +314,25 @@ __device__ __forceinline__ void bulk_copy_g2s_plain(void *dst_smem, const void *
         : "memory");
 }
 
+// load_f32_smem for the CNT consecutive floats that lane `sub` (of the 8 lanes
+// serving one head) owns at p = base + sub * CNT.  A 16-byte-per-lane shared
+// load is served 8 lanes at a time; with CNT = 8 lanes sub and sub + 4 sit
+// 128 bytes apart, so reading both 16-byte halves in the same order puts two
+// lanes on every bank group.  Lanes 4-7 read their halves in the other order,
+// which gives the 8 lanes 8 distinct bank groups per load.
+template <int CNT>
+__device__ __forceinline__ void load_f32_smem_lanes(const float *p, float (&o)[CNT], int sub) {
+    if constexpr (CNT == 8) {
+        const bool sw = (sub & 4) != 0;
+        const float4 a = *reinterpret_cast<const float4 *>(p + (sw ? 4 : 0));
+        const float4 b = *reinterpret_cast<const float4 *>(p + (sw ? 0 : 4));
+        o[0] = sw ? b.x : a.x; o[1] = sw ? b.y : a.y; o[2] = sw ? b.z : a.z; o[3] = sw ? b.w : a.w;
+        o[4] = sw ? a.x : b.x; o[5] = sw ? a.y : b.y; o[6] = sw ? a.z : b.z; o[7] = sw ? a.w : b.w;
+    } else {
+        load_f32_smem<CNT>(p, o);
+    }
+}
+
 __device__ __forceinline__ float2 bf2f(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
 
 // CNT (even) consecutive bf16 as CNT/2 packed words; same alignment rules as load_bf.
@@ -610,8 +629,8 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
             if constexpr (B > 0) load_words<B>(xs + R + sub * B, x3);
             const float *cs = cs_base + ts * R;
             float c[A], sn[A];
-            load_f32_smem<A>(cs + sub * A, c);
-            load_f32_smem<A>(cs + H2 + sub * A, sn);
+            load_f32_smem_lanes<A>(cs + sub * A, c, sub);
+            load_f32_smem_lanes<A>(cs + H2 + sub * A, sn, sub);
 
             // two independent accumulators: half the dependent FMA chain
             float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
@@ -730,7 +749,12 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     const int H = a.Hq + a.Hkv;
     const int tok_bytes = H * D * 2;
     const int cs_bytes = R * 4;
-    int tps = 32768 / (tok_bytes + cs_bytes);
+    // About 32 KiB a stage; 44 KiB when the rotation spans the whole head,
+    // whose consumers hold a stage longer (more arithmetic per token): 4
+    // tokens a stage instead of 3 at D = 128, measured on GB300.
+    int tps = (R == D ? 45056 : 32768) / (tok_bytes + cs_bytes);
+    const int forced_tps = (debug_flags >> 16) & 0x3F;
+    if (forced_tps > 0) tps = forced_tps;
     if (tps < 1) tps = 1;
     if (tps > 32) tps = 32;
     // Consumers hold a stage while they compute, so four stages keep about
@@ -739,6 +763,9 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     const int forced = (debug_flags >> 8) & 0x1F;
     if (forced >= 2) stages = forced;
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
+    // a forced stage count takes precedence over the stage size
+    while (tps > 1 && qk_bulk_smem_bytes(stages, tps, tok_bytes, cs_bytes) > static_cast<size_t>(smem_cap))
+        --tps;
     const size_t smem = qk_bulk_smem_bytes(stages, tps, tok_bytes, cs_bytes);
     if (smem > static_cast<size_t>(smem_cap)) return RN_ERR_SHAPE;
     const int dev_idx = current_device_index();

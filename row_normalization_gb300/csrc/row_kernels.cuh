@@ -324,14 +324,19 @@ struct BulkArgs {
     uint64_t timeout_ns;
 };
 
+// Per-warp partial sums of row rr sit at [rr * kRedStride + warp]: the lane
+// that finishes row rr reads its row's partials along a run of consecutive
+// words, and the R such lanes fall in different banks (stride 33, not 32).
+constexpr int kRedStride = 33;
+
 // Shared memory: [stages x (R rows of x [+ R rows of r])][full mbarriers]
-//                [empty mbarriers][partial sums 4 x R x 32 floats][flags: 4 ints]
+//                [empty mbarriers][partial sums 4 x R x 33 floats][flags: 4 ints]
 // (two double-buffered sets of partial sums: LayerNorm reduces twice a row)
 // `nin` is the number of row inputs streamed through the ring (1, or 2 with
 // the fused residual add).
 __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1) {
     return static_cast<size_t>(stages) * nin * R * N * 2 + static_cast<size_t>(stages) * 16 +
-           static_cast<size_t>(4) * R * 32 * 4 + 16;
+           static_cast<size_t>(4) * R * kRedStride * 4 + 16;
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
     // flags[0], flags[1]: "consumers give up" for even / odd units (decided
     // before a named barrier, read after it); flags[2]: "someone gave up",
     // polled inside waits so nobody waits out a full timeout needlessly.
-    volatile int *flags = reinterpret_cast<volatile int *>(red + 4 * R * 32);
+    volatile int *flags = reinterpret_cast<volatile int *>(red + 4 * R * kRedStride);
 
     const int nt = GENERIC ? static_cast<int>(blockDim.x) - 32 : NT;
     const int NW = nt / 32;
@@ -512,11 +517,11 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
                 for (int j = 0; j < VPR; ++j) acc += sum8<E>(xv[rr][j]);
                 s1[rr] = warp_sum(acc);
             }
-            float *rb1 = red + (k & 1) * R * 32;
-            float *rb2 = red + (2 + (k & 1)) * R * 32;
+            float *rb1 = red + (k & 1) * R * kRedStride;
+            float *rb2 = red + (2 + (k & 1)) * R * kRedStride;
             if (lane == 0) {
 #pragma unroll
-                for (int rr = 0; rr < R; ++rr) rb1[rr * 32 + warp] = s1[rr];
+                for (int rr = 0; rr < R; ++rr) rb1[rr * kRedStride + warp] = s1[rr];
             }
             named_bar_sync(1, nt);
             if (flags[k & 1]) break;  // same decision in every consumer warp
@@ -524,7 +529,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             float my_mean = 0.f;
             if (lane < R) {
                 float t = 0.f;
-                for (int q = 0; q < NW; ++q) t += rb1[lane * 32 + q];
+                for (int q = 0; q < NW; ++q) t += rb1[lane * kRedStride + q];
                 my_mean = t / static_cast<float>(N);
             }
             float mean[R];
@@ -539,13 +544,13 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             }
             if (lane == 0) {
 #pragma unroll
-                for (int rr = 0; rr < R; ++rr) rb2[rr * 32 + warp] = s1[rr];
+                for (int rr = 0; rr < R; ++rr) rb2[rr * kRedStride + warp] = s1[rr];
             }
             named_bar_sync(1, nt);
             float my_rstd = 0.f;
             if (lane < R) {
                 float t = 0.f;
-                for (int q = 0; q < NW; ++q) t += rb2[lane * 32 + q];
+                for (int q = 0; q < NW; ++q) t += rb2[lane * kRedStride + q];
                 my_rstd = row_rstd(t, N, a.eps);
             }
 #pragma unroll
@@ -576,10 +581,10 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             for (int j = 0; j < VPR; ++j)
                 asm volatile("" : "+r"(xv[rr][j].x), "+r"(xv[rr][j].y), "+r"(xv[rr][j].z),
                              "+r"(xv[rr][j].w));
-        float *rb = red + (k & 1) * R * 32;
+        float *rb = red + (k & 1) * R * kRedStride;
         if (lane == 0) {
 #pragma unroll
-            for (int rr = 0; rr < R; ++rr) rb[rr * 32 + warp] = ss[rr];
+            for (int rr = 0; rr < R; ++rr) rb[rr * kRedStride + warp] = ss[rr];
         }
         named_bar_sync(1, nt);
         if (flags[k & 1]) break;  // same decision in every consumer warp
@@ -588,7 +593,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         float my_scale = 0.f;
         if (lane < R) {
             float tot = 0.f;
-            for (int q = 0; q < NW; ++q) tot += rb[lane * 32 + q];
+            for (int q = 0; q < NW; ++q) tot += rb[lane * kRedStride + q];
             my_scale = row_scale(tot, N, a.eps, a.l2);
         }
 #pragma unroll

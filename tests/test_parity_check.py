@@ -70,3 +70,17 @@ def test_nan_only_matches_itself():
     ref = bits([np.nan, 1.0], "f16")
     assert parity_report(ref, ref, fmt="f16")["bad"] == 0
     assert parity_report(bits([1.0, 1.0], "f16"), ref, fmt="f16")["bad"] == 1
+
+
+def test_midpoint_mode_accepts_ties_and_rejects_other_one_step_errors():
+    from tests.parity import near_midpoint
+    # 1 + 2^-8 is the bf16 midpoint between 1 and 1 + 2^-7
+    exact = np.array([1 + 2.0**-8 + 2.0**-30, 1.25, 1 + 2.0**-8 - 2.0**-26])
+    assert near_midpoint(exact).tolist() == [True, False, True]
+    ref = bits([1.0 + 2.0**-7, 1.25, 1.0], "bf16")        # oracle rounding
+    got = bits([1.0, 1.25 + 2.0**-7, 1.0 + 2.0**-7], "bf16")  # each one step away
+    rep = parity_report(got, ref, exact=exact)
+    assert rep["one_ulp_not_at_midpoint"] == 1              # only the 1.25 element
+    # fp16: 1 + 2^-11 is a midpoint
+    assert near_midpoint(np.array([1 + 2.0**-11]), fmt="f16").tolist() == [True]
+    assert near_midpoint(np.array([1 + 2.0**-12]), fmt="f16").tolist() == [False]
