@@ -33,10 +33,14 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 // A 16-bit element format: widen the two halves of a packed word to fp32
 // (exact) and narrow two fp32 back with one round-to-nearest-even.
 
-// Besides widening and narrowing, each format offers sq_acc(acc, u) =
-// acc + lo(u)^2 + hi(u)^2 as two mixed-precision fused multiply-adds on the
-// packed halves (16-bit multiplicands, fp32 addend and result; sm_100 and
-// later): each square is exact in fp32 and no widening instruction is spent.
+// Besides widening and narrowing, each format offers three operations on the
+// packed halves as mixed-precision instructions (16-bit operand, fp32 other
+// operand and result; sm_100 and later), which fold the widening into the
+// arithmetic and round exactly as widen-then-operate does:
+//   sq_acc(acc, u)  acc + lo(u)^2 + hi(u)^2  (two fused multiply-adds; each
+//                   square is exact in fp32);
+//   pair_sum(u)     lo(u) + hi(u), rounded once;
+//   sub2(u, m)      (lo(u) - m, hi(u) - m), each rounded once.
 
 struct Bf16 {
     static constexpr uint32_t kOne2 = 0x3F803F80u;  // two 1.0
@@ -48,6 +52,19 @@ struct Bf16 {
             "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
             : "+f"(acc) : "r"(u));
         return acc;
+    }    __device__ static __forceinline__ float pair_sum(uint32_t u) {
+        float r;
+        asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 t;\n\tmov.b32 {l, h}, %1;\n\t"
+            "add.rn.f32.bf16 t, l, 0f80000000;\n\tadd.rn.f32.bf16 %0, h, t;\n\t}"
+            : "=f"(r) : "r"(u));
+        return r;
+    }
+    __device__ static __forceinline__ float2 sub2(uint32_t u, float m) {
+        float2 r;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+            : "=f"(r.x), "=f"(r.y) : "r"(u), "f"(m));
+        return r;
     }
 };
 
@@ -69,6 +86,19 @@ struct F16 {
             "fma.rn.f32.f16 %0, l, l, %0;\n\tfma.rn.f32.f16 %0, h, h, %0;\n\t}"
             : "+f"(acc) : "r"(u));
         return acc;
+    }    __device__ static __forceinline__ float pair_sum(uint32_t u) {
+        float r;
+        asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 t;\n\tmov.b32 {l, h}, %1;\n\t"
+            "add.rn.f32.f16 t, l, 0f80000000;\n\tadd.rn.f32.f16 %0, h, t;\n\t}"
+            : "=f"(r) : "r"(u));
+        return r;
+    }
+    __device__ static __forceinline__ float2 sub2(uint32_t u, float m) {
+        float2 r;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "sub.rn.f32.f16 %0, l, %3;\n\tsub.rn.f32.f16 %1, h, %3;\n\t}"
+            : "=f"(r.x), "=f"(r.y) : "r"(u), "f"(m));
+        return r;
     }
 };
 

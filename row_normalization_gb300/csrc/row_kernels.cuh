@@ -79,38 +79,58 @@ __device__ __forceinline__ uint4 add8(uint4 a, uint4 b) {
 }
 
 // LayerNorm pieces: sum of 8, sum of squared deviations from `mean`, and
-// y = (x - mean) * rstd * w (+ b) rounded once.
+// y = (x - mean) * rstd * w (+ b) rounded once.  The widening of x is folded
+// into mixed-precision adds and subtracts (pair_sum, sub2), which round
+// exactly as widen-then-add does.
 template <class E>
 __device__ __forceinline__ float sum8(uint4 v) {
-    return ((E::lo(v.x) + E::hi(v.x)) + (E::lo(v.y) + E::hi(v.y))) +
-           ((E::lo(v.z) + E::hi(v.z)) + (E::lo(v.w) + E::hi(v.w)));
+    return (E::pair_sum(v.x) + E::pair_sum(v.y)) + (E::pair_sum(v.z) + E::pair_sum(v.w));
 }
 
 template <class E>
 __device__ __forceinline__ float sqdev8(uint4 v, float m) {
-    float a = E::lo(v.x) - m, b = E::hi(v.x) - m, c = E::lo(v.y) - m, d = E::hi(v.y) - m;
-    float e = E::lo(v.z) - m, f = E::hi(v.z) - m, g = E::lo(v.w) - m, h = E::hi(v.w) - m;
-    return ((a * a + b * b) + (c * c + d * d)) + ((e * e + f * f) + (g * g + h * h));
+    const float2 p = E::sub2(v.x, m), q = E::sub2(v.y, m), r = E::sub2(v.z, m), t = E::sub2(v.w, m);
+    const float2 a = __ffma2_rn(r, r, __fmul2_rn(p, p));
+    const float2 b = __ffma2_rn(t, t, __fmul2_rn(q, q));
+    const float2 s2 = __fadd2_rn(a, b);
+    return s2.x + s2.y;
 }
 
 // Same, on fp32 pairs (Blackwell FADD2/FMUL2/FFMA2): per pair one subtract,
 // one multiply by rstd, one fused multiply-add with (w, b).
 template <class E>
-__device__ __forceinline__ uint32_t ln2w(uint32_t x, uint32_t w, uint32_t b, float2 nm, float2 r) {
-    const float2 d = __fmul2_rn(__fadd2_rn(make_float2(E::lo(x), E::hi(x)), nm), r);
+__device__ __forceinline__ uint32_t ln2w(uint32_t x, uint32_t w, uint32_t b, float m, float2 r) {
+    const float2 d = __fmul2_rn(E::sub2(x, m), r);
     const float2 y = __ffma2_rn(d, make_float2(E::lo(w), E::hi(w)), make_float2(E::lo(b), E::hi(b)));
     return E::pack(y.x, y.y);
 }
 
 template <class E>
 __device__ __forceinline__ uint4 ln8(uint4 xv, uint4 wv, uint4 bv, float m, float rstd) {
-    const float2 nm = make_float2(-m, -m);
     const float2 r = make_float2(rstd, rstd);
     uint4 o;
-    o.x = ln2w<E>(xv.x, wv.x, bv.x, nm, r);
-    o.y = ln2w<E>(xv.y, wv.y, bv.y, nm, r);
-    o.z = ln2w<E>(xv.z, wv.z, bv.z, nm, r);
-    o.w = ln2w<E>(xv.w, wv.w, bv.w, nm, r);
+    o.x = ln2w<E>(xv.x, wv.x, bv.x, m, r);
+    o.y = ln2w<E>(xv.y, wv.y, bv.y, m, r);
+    o.z = ln2w<E>(xv.z, wv.z, bv.z, m, r);
+    o.w = ln2w<E>(xv.w, wv.w, bv.w, m, r);
+    return o;
+}
+
+// ln8 with the weights already widened to fp32 pairs (w[0..3]).
+template <class E>
+__device__ __forceinline__ uint32_t ln2f(uint32_t x, float2 w, uint32_t b, float m, float2 r) {
+    const float2 y = __ffma2_rn(__fmul2_rn(E::sub2(x, m), r), w, make_float2(E::lo(b), E::hi(b)));
+    return E::pack(y.x, y.y);
+}
+
+template <class E>
+__device__ __forceinline__ uint4 ln8w(uint4 xv, const float2 *w, uint4 bv, float m, float rstd) {
+    const float2 r = make_float2(rstd, rstd);
+    uint4 o;
+    o.x = ln2f<E>(xv.x, w[0], bv.x, m, r);
+    o.y = ln2f<E>(xv.y, w[1], bv.y, m, r);
+    o.z = ln2f<E>(xv.z, w[2], bv.z, m, r);
+    o.w = ln2f<E>(xv.w, w[3], bv.w, m, r);
     return o;
 }
 
@@ -443,10 +463,26 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
     for (int j = 0; j < VPR; ++j)
         wv[j] = live(tid, j) ? weight16<E>(a.w, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
     uint4 bv[LN ? VPR : 1];  // LayerNorm bias, held like the weights
+    // With at most 256 consumers (3 warps a scheduler, up to 170 registers a
+    // thread) LayerNorm keeps its weights widened to fp32 pairs: one fused
+    // multiply-add a pair and no widening of w per row.  The 512-consumer
+    // layout (5 warps on one scheduler: 96 registers) keeps them packed.  The
+    // bias stays packed.
+    constexpr bool WIDE_W = LN && NT <= 256;
+    float2 wf[WIDE_W ? VPR * 4 : 1];
     if constexpr (LN) {
 #pragma unroll
         for (int j = 0; j < VPR; ++j)
             bv[j] = live(tid, j) ? bias16(a.b, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if constexpr (WIDE_W) {
+#pragma unroll
+        for (int j = 0; j < VPR; ++j) {
+            wf[4 * j + 0] = make_float2(E::lo(wv[j].x), E::hi(wv[j].x));
+            wf[4 * j + 1] = make_float2(E::lo(wv[j].y), E::hi(wv[j].y));
+            wf[4 * j + 2] = make_float2(E::lo(wv[j].z), E::hi(wv[j].z));
+            wf[4 * j + 3] = make_float2(E::lo(wv[j].w), E::hi(wv[j].w));
+        }
     }
 
     for (int64_t k = 0; k < n_units; ++k) {
@@ -456,9 +492,11 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         // Keep the weights packed (16-bit) across rows: without this the
         // compiler hoists their fp32 widening out of the loop and doubles
         // the register footprint.
+        if constexpr (!WIDE_W) {
 #pragma unroll
-        for (int j = 0; j < VPR; ++j)
-            asm volatile("" : "+r"(wv[j].x), "+r"(wv[j].y), "+r"(wv[j].z), "+r"(wv[j].w));
+            for (int j = 0; j < VPR; ++j)
+                asm volatile("" : "+r"(wv[j].x), "+r"(wv[j].y), "+r"(wv[j].z), "+r"(wv[j].w));
+        }
         if constexpr (LN) {
 #pragma unroll
             for (int j = 0; j < VPR; ++j)
@@ -561,7 +599,8 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
                         if (live(tid, j))
-                            st16(yr + 8 * (tid + j * nt), ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
+                            st16(yr + 8 * (tid + j * nt), (WIDE_W ? ln8w<E>(xv[rr][j], &wf[4 * j], bv[j], mean[rr], rstd)
+                                          : ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd)));
                 }
             }
             continue;
