@@ -464,11 +464,12 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
         wv[j] = live(tid, j) ? weight16<E>(a.w, tid + j * nt) : make_uint4(0u, 0u, 0u, 0u);
     uint4 bv[LN ? VPR : 1];  // LayerNorm bias, held like the weights
     // With at most 256 consumers (3 warps a scheduler, up to 170 registers a
-    // thread) LayerNorm keeps its weights widened to fp32 pairs: one fused
-    // multiply-add a pair and no widening of w per row.  The 512-consumer
-    // layout (5 warps on one scheduler: 96 registers) keeps them packed.  The
-    // bias stays packed.
-    constexpr bool WIDE_W = LN && NT <= 256;
+    // thread) and at most 4 chunks a thread, LayerNorm keeps its weights
+    // widened to fp32 pairs: one fused multiply-add a pair and no widening of
+    // w per row.  Other layouts keep them packed (512 consumers put 5 warps on
+    // one scheduler: 96 registers; 8 chunks would spill).  The bias stays
+    // packed.
+    constexpr bool WIDE_W = LN && NT <= 256 && VPR <= 4;
     float2 wf[WIDE_W ? VPR * 4 : 1];
     if constexpr (LN) {
 #pragma unroll
@@ -765,7 +766,7 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
             case 2048: *g = {256, 1, 8, 2, 1, false}; break;
             case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1, false}; break;
             case 8192: *g = {256, 4, 2, 2, 1, false}; break;
-            case 16384: *g = {512, 4, 1, 2, 1, false}; break;
+            case 16384: *g = {256, 8, 1, 2, 1, false}; break;  // measured ahead of 512 x 4
             default: return false;
         }
         return true;
@@ -862,7 +863,9 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
         case 2048: return launch_bulk_inst<E, 1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
         case 4096: return launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
         case 8192: return launch_bulk_inst<E, 4, 2, 256, ADD, LN>(a, g, smem, smem_cap, st);
-        case 16384: return launch_bulk_inst<E, 4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
+        case 16384:
+            if constexpr (LN) return launch_bulk_inst<E, 8, 1, 256, ADD, LN>(a, g, smem, smem_cap, st);
+            else return launch_bulk_inst<E, 4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
         case 32768:
             if constexpr (!ADD && !LN)
                 return launch_bulk_inst<E, 8, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
