@@ -787,14 +787,15 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
                       dim3(qk_bulk_consumers<D>() + 32), smem, st, b);
 }
 
-// Schedule by token count (measured on GB300): one head per warp for 1-2
-// tokens, two heads per warp through 256 tokens, four heads per warp on a
-// persistent grid up to 2047 tokens, and the bulk-copy token ring beyond,
+// Schedule by token count (measured on GB300, back-to-back launches): one
+// head per warp for 1-2 tokens, two heads per warp through 256 tokens, four
+// heads per warp on a persistent grid through 4096 tokens (5-15% ahead of the
+// ring there), and the bulk-copy token ring beyond (ahead from 6144 tokens),
 // where its deeper prefetch pays for its longer start-up.
 static int auto_qk_schedule(int64_t T) {
     if (T <= 2) return RN_QK_HEAD_PER_WARP;
     if (T <= 256) return RN_QK_TWO_HEADS;
-    if (T < 2048) return RN_QK_PERSISTENT;
+    if (T <= 4096) return RN_QK_PERSISTENT;
     return RN_QK_BULK;
 }
 
