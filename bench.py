@@ -310,37 +310,56 @@ def launch_step(binding, rms, qk, events=None):
 
 def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> list:
     """Each launch of the step measured on its own, in steady state: `reps`
-    back-to-back launches of one shape, alternating between two sets of
-    activations so nothing is reused from L2 (weights and tables shared).
+    back-to-back launches of one shape, replayed from a CUDA graph, alternating
+    between two sets of activations so nothing is reused from L2 when the
+    shape exceeds it (weights and tables shared).
     A launch then pays for the dirty L2 lines its predecessor (the same
     shape) left behind and leaves as many itself, so its DRAM traffic equals
     its algorithmic bytes.  The in-step per-launch times instead also carry
     the dirty tail of whichever launch ran before (up to the 126 MiB L2).
-    Beside each: torch's copy of the same number of bytes, timed the same
-    way (the ceiling any single-pass kernel of that size meets)."""
+    Beside each: a plain torch streaming kernel over the same number of
+    bytes, timed the same way (the ceiling any single-pass kernel of that
+    size meets)."""
     out = []
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
 
     def copy_frac(nbytes: int) -> float:
-        # torch's own copy of the same bytes (half read, half written), run
-        # the same way: the ceiling a single-pass kernel of this size reaches
-        n = nbytes // 2 // 16 * 16
-        bufs = [(torch.empty(n, dtype=torch.uint8, device="cuda"),
-                 torch.empty(n, dtype=torch.uint8, device="cuda")) for _ in range(2)]
-        ms = timed(bufs, lambda _b, p: p[1].copy_(p[0]))
+        # A plain streaming kernel over the same bytes (half read, half
+        # written), run the same way: torch's elementwise bitwise NOT on int32
+        # words, the ceiling a single-pass kernel of this size reaches.  (Not
+        # copy_: inside a CUDA graph a same-dtype copy becomes a memcpy node
+        # whose engine the driver picks, and it measured 2x slower on some
+        # buffers.)
+        n = nbytes // 2 // 16 * 4
+        bufs = [(torch.empty(n, dtype=torch.int32, device="cuda"),
+                 torch.empty(n, dtype=torch.int32, device="cuda")) for _ in range(2)]
+        ms = timed(bufs, lambda _b, p: torch.bitwise_not(p[0], out=p[1]))
         del bufs
-        return round(2 * n / (ms * 1e-3) / 1e9 / hbm_peak, 4)
+        return round(8 * n / (ms * 1e-3) / 1e9 / hbm_peak, 4)
 
     def timed(pair, launch):
-        for i in range(4):
-            launch(binding, pair[i & 1])
+        # `reps` back-to-back launches captured once in a CUDA graph and
+        # replayed: the GPU time of the launches, without the host's per-call
+        # cost (which exceeds the whole kernel below a few MB).
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(4):
+                launch(binding, pair[i & 1])
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(reps):
+                launch(binding, pair[i & 1])
+        graph.replay()
         torch.cuda.synchronize()
         start.record()
-        for i in range(reps):
-            launch(binding, pair[i & 1])
+        graph.replay()
         end.record()
         torch.cuda.synchronize()
+        del graph
         return start.elapsed_time(end) / reps
 
     for c in rms:
@@ -360,7 +379,7 @@ def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> lis
         gbs = b / (ms * 1e-3) / 1e9
         out.append({"op": op, "M": c["M"], "N": c["N"], "us": round(ms * 1e3, 2),
                     "gbs": round(gbs, 1), "frac_of_measured": round(gbs / hbm_peak, 4),
-                    "copy_same_bytes_frac": copy_frac(b)})
+                    "stream_same_bytes_frac": copy_frac(b)})
     for c in qk:
         twin = dict(c)
         twin["qkv"] = c["qkv"].clone()
@@ -371,7 +390,7 @@ def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> lis
         out.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
                     "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                     "frac_of_measured": round(gbs / hbm_peak, 4),
-                    "copy_same_bytes_frac": copy_frac(b)})
+                    "stream_same_bytes_frac": copy_frac(b)})
     return out
 
 
