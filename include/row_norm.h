@@ -35,7 +35,12 @@
  *   - The caller owns every buffer.  The library allocates no device memory,
  *     never synchronises, and enqueues its kernels on `stream` (NULL = the
  *     legacy default stream).  Results are ready when the stream reaches
- *     that point.
+ *     that point.  The calls can be captured into a CUDA graph.
+ *   - Kernels launch with programmatic dependent launch: a kernel may be
+ *     scheduled while the previous launch on the stream is finishing, but it
+ *     waits for that launch to complete (and its writes to be visible)
+ *     before it reads or writes any tensor, so stream order holds exactly
+ *     as for ordinary launches.
  *   - Every function returns RN_OK (0) or a negative RN_ERR_* code.  Argument
  *     errors are detected on the host before anything is launched; nothing is
  *     written in that case.  RN_ERR_LAUNCH reports a failed launch.
