@@ -308,6 +308,99 @@ def launch_step(binding, rms, qk, events=None):
     return k
 
 
+def graph_ms(torch, launch, reps: int) -> float:
+    """Milliseconds per launch of `launch(i)`, i = 0..reps-1, captured once in
+    a CUDA graph and replayed: the GPU time of back-to-back launches without
+    the host's per-call cost (which exceeds a whole kernel below a few MB)."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(4):
+            launch(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(reps):
+            launch(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    start.record()
+    graph.replay()
+    end.record()
+    torch.cuda.synchronize()
+    del graph
+    return start.elapsed_time(end) / reps
+
+
+def direct_ms(torch, launch, reps: int) -> float:
+    """Milliseconds per launch issued one by one from Python (host-bound for
+    small launches: the figure a caller without graphs sees)."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    for i in range(4):
+        launch(i)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(reps):
+        launch(i)
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / reps
+
+
+def config_points(torch, binding, inputs, hbm_peak: float) -> dict:
+    """The named configurations outside the step, each timed by CUDA-graph
+    replay of back-to-back launches on two alternating buffer sets:
+    RMSNorm 64 x 4096 (latency), the 32768-wide rows (eps 1e-5), QK at
+    T in {1, 2, 16, 64, 256} (rotary 128, positions 0..T-1, latency) and at
+    T in {1024, 4096} (rotary 128 and 64, uniform positions)."""
+    out = {}
+
+    def rms_point(M, N, eps, latency):
+        pair = [inputs.rmsnorm_inputs(M, N, device="cuda", seed=s) for s in (11, 12)]
+        ys = [torch.empty_like(pair[0][0]) for _ in range(2)]
+        fn = lambda i: binding.rmsnorm_fwd(pair[i & 1][0], pair[0][1], eps, ys[i & 1])  # noqa: E731
+        ms = graph_ms(torch, fn, 100 if latency else 20)
+        b = rms_bytes(M, N)
+        pt = {"M": M, "N": N, "eps": eps, "us": round(ms * 1e3, 2),
+              "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+              "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+        if latency:
+            pt["us_direct_launch"] = round(direct_ms(torch, fn, 200) * 1e3, 2)
+        return pt
+
+    def qk_point(T, r, positions, latency):
+        table = binding.rope_cos_sin_table(THETA, MAX_POS, r, device="cuda")
+        bufs = [inputs.qkv_inputs(T, HQ, HKV, D, positions=positions, max_pos=MAX_POS,
+                                  device="cuda", seed=s) for s in (21, 22)]
+
+        def fn(i):
+            q, wq, wk, pos = bufs[i & 1]
+            binding.qk_norm_rope_fwd(q, wq, wk, table, pos, HQ, HKV, D, r, QK_EPS)
+
+        ms = graph_ms(torch, fn, 100 if latency else 20)
+        b = qk_bytes(T, r)
+        pt = {"T": T, "rotary_dim": r, "positions": positions, "us": round(ms * 1e3, 2),
+              "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+              "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+        if latency:
+            pt["us_direct_launch"] = round(direct_ms(torch, fn, 200) * 1e3, 2)
+        return pt
+
+    out["rmsnorm_64x4096_latency"] = rms_point(64, 4096, 1e-6, True)
+    out["rmsnorm_wide_N32768"] = [rms_point(M, 32768, 1e-5, False) for M in (1024, 4096, 8192)]
+    out["qk_small_T_latency"] = [qk_point(T, 128, "arange", True) for T in (1, 2, 16, 64, 256)]
+    out["qk_T1024_T4096"] = [qk_point(T, r, "uniform", False) for T in (1024, 4096)
+                             for r in (128, 64)]
+    out["timing"] = ("CUDA-graph replay of back-to-back launches on two alternating buffer "
+                     "sets (us per launch); us_direct_launch: the same launches issued one "
+                     "by one from Python")
+    return out
+
+
 def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> list:
     """Each launch of the step measured on its own, in steady state: `reps`
     back-to-back launches of one shape, replayed from a CUDA graph, alternating
@@ -321,8 +414,6 @@ def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> lis
     bytes, timed the same way (the ceiling any single-pass kernel of that
     size meets)."""
     out = []
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
 
     def copy_frac(nbytes: int) -> float:
         # A plain streaming kernel over the same bytes (half read, half
@@ -339,28 +430,7 @@ def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> lis
         return round(8 * n / (ms * 1e-3) / 1e9 / hbm_peak, 4)
 
     def timed(pair, launch):
-        # `reps` back-to-back launches captured once in a CUDA graph and
-        # replayed: the GPU time of the launches, without the host's per-call
-        # cost (which exceeds the whole kernel below a few MB).
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for i in range(4):
-                launch(binding, pair[i & 1])
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(reps):
-                launch(binding, pair[i & 1])
-        graph.replay()
-        torch.cuda.synchronize()
-        start.record()
-        graph.replay()
-        end.record()
-        torch.cuda.synchronize()
-        del graph
-        return start.elapsed_time(end) / reps
+        return graph_ms(torch, lambda i: launch(binding, pair[i & 1]), reps)
 
     for c in rms:
         twin = dict(c)
@@ -512,6 +582,8 @@ def run_ours(args) -> int:
     steady = steady_per_shape(torch, binding, rms, qk, args.steady_reps, hbm_peak) \
         if args.steady_reps > 0 else None
     plain = not ADD_SHAPES and not LN_SHAPES and not L2_SHAPES and ROW_DTYPE == "bf16"
+    configs = config_points(torch, binding, inputs, hbm_peak) \
+        if plain and WORKLOAD.startswith("rmsnorm sweep") and args.steady_reps > 0 else None
     e2e = run_e2e(torch, binding, rms, qk, args, dist, device) if args.e2e_steps > 0 and plain \
         else None
     cpu = None
@@ -549,6 +621,7 @@ def run_ours(args) -> int:
                    "before every launch, which serialises the launches"),
         "per_shape": per_shape,
         "steady_per_shape": steady,
+        "configs": configs,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -732,8 +805,20 @@ def cpu_baseline(budget_s: float = 10.0, frac_den: int = 256) -> dict:
             el = time.perf_counter() - t0
             if el >= budget_s:
                 break
+    # one thread on the same sample, for a fraction of the budget
+    single = None
+    with ThreadPoolExecutor(max_workers=1) as pool1:
+        t1 = time.perf_counter()
+        p1 = 0
+        while True:
+            _cpu_pass(pool1, 1, rms, qk, tables)
+            p1 += 1
+            e1 = time.perf_counter() - t1
+            if e1 >= budget_s * 0.3:
+                break
+        single = round(nbytes * p1 / e1 / 1e9, 3)
     return {"value": round(nbytes * passes / el / 1e9, 3), "unit": "GB/s", "cores": threads,
-            "kind": "oracle",
+            "single_thread_value": single, "kind": "oracle",
             "sample": (f"first 1/{frac_den} of the rows of every RMSNorm shape and of the "
                        f"tokens of each QK case ({nbytes / 1e6:.1f} MB ideal traffic per pass), "
                        f"{passes} passes in {el:.1f} s, fp64 C oracle on {threads} threads")}
