@@ -1,7 +1,9 @@
 // rn_common.cuh -- device helpers shared by the row-normalization kernels.
 //
-// bf16 packing, 16-byte global accesses, and thin inline-PTX wrappers for the
-// Hopper/Blackwell asynchronous-copy machinery the persistent schedule uses:
+// The 16-bit element formats (bf16, IEEE fp16) with their mixed-precision
+// operations, 16-byte global accesses, programmatic-dependent-launch hooks
+// and the launch helper, and thin inline-PTX wrappers for the
+// Hopper/Blackwell asynchronous-copy machinery the persistent schedules use:
 // mbarriers (arrive, expect-tx, parity wait) and 1D bulk copies
 // (cp.async.bulk, global -> this CTA's shared memory, completion signalled on
 // an mbarrier).  No tensor maps and no multicast.

@@ -1,5 +1,7 @@
-// rn_host.h -- host-side helpers shared by the entry points: argument checks
-// and a per-device cache of the properties the schedules depend on.
+// rn_host.h -- host-side helpers shared by the entry points: a per-device
+// cache of the properties the schedules depend on, alignment checks, and the
+// format-independent row-norm call that the C entry points hand to the
+// translation unit of each element format.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -85,9 +87,5 @@ int rows_select_schedule(int op, int64_t M, int64_t N);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-inline int launch_status() {
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? RN_OK : RN_ERR_LAUNCH;
-}
 
 }  // namespace rn
