@@ -350,13 +350,14 @@ struct BulkArgs {
 constexpr int kRedStride = 33;
 
 // Shared memory: [stages x (R rows of x [+ R rows of r])][full mbarriers]
-//                [empty mbarriers][partial sums 4 x R x 33 floats][flags: 4 ints]
-// (two double-buffered sets of partial sums: LayerNorm reduces twice a row)
+//                [empty mbarriers][partial sums 6 x R x 33 floats][flags: 4 ints]
+// (three double-buffered sets of partial sums: LayerNorm reduces up to three
+// quantities a row)
 // `nin` is the number of row inputs streamed through the ring (1, or 2 with
 // the fused residual add).
 __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1) {
     return static_cast<size_t>(stages) * nin * R * N * 2 + static_cast<size_t>(stages) * 16 +
-           static_cast<size_t>(4) * R * kRedStride * 4 + 16;
+           static_cast<size_t>(6) * R * kRedStride * 4 + 16;
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
     // flags[0], flags[1]: "consumers give up" for even / odd units (decided
     // before a named barrier, read after it); flags[2]: "someone gave up",
     // polled inside waits so nobody waits out a full timeout needlessly.
-    volatile int *flags = reinterpret_cast<volatile int *>(red + 4 * R * kRedStride);
+    volatile int *flags = reinterpret_cast<volatile int *>(red + 6 * R * kRedStride);
 
     const int nt = GENERIC ? static_cast<int>(blockDim.x) - 32 : NT;
     const int NW = nt / 32;
@@ -546,51 +547,74 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
             }
         }
         if constexpr (LN) {
-            // LayerNorm: mean, then the centred sum of squares, each reduced
-            // over the CTA's consumer warps (two named barriers a unit).
-            float s1[R];
+            // LayerNorm: one CTA reduction of each row's sum and sum of
+            // squares.  Where the mean is small against the spread (mean^2 <=
+            // 4 var) the variance follows directly as E[x^2] - mean^2 (the
+            // fp32 cancellation costs at most ~2 bits of a 2^-23 error).  A
+            // unit with a row outside that bound (a large mean, a constant
+            // row) takes a second reduction over the centred squares, the
+            // exact two-pass form.  Every warp finishes the same partials in
+            // the same order, so the choice is uniform over the CTA.
+            float s1[R], q1[R];
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
-                float acc = 0.f;
+                float acc = 0.f, acq = 0.f;
 #pragma unroll
-                for (int j = 0; j < VPR; ++j) acc += sum8<E>(xv[rr][j]);
+                for (int j = 0; j < VPR; ++j) {
+                    acc += sum8<E>(xv[rr][j]);
+                    acq += sumsq8<E>(xv[rr][j]);
+                }
                 s1[rr] = warp_sum(acc);
+                q1[rr] = warp_sum(acq);
             }
-            float *rb1 = red + (k & 1) * R * kRedStride;
-            float *rb2 = red + (2 + (k & 1)) * R * kRedStride;
+            float *rbs = red + (k & 1) * R * kRedStride;        // sums
+            float *rbq = red + (2 + (k & 1)) * R * kRedStride;  // sums of squares
+            float *rbc = red + (4 + (k & 1)) * R * kRedStride;  // centred squares
             if (lane == 0) {
 #pragma unroll
-                for (int rr = 0; rr < R; ++rr) rb1[rr * kRedStride + warp] = s1[rr];
+                for (int rr = 0; rr < R; ++rr) {
+                    rbs[rr * kRedStride + warp] = s1[rr];
+                    rbq[rr * kRedStride + warp] = q1[rr];
+                }
             }
             named_bar_sync(1, nt);
             if (flags[k & 1]) break;  // same decision in every consumer warp
-            // lane rr finishes row rr's mean once; a shuffle hands it out
-            float my_mean = 0.f;
+            // lane rr finishes row rr's statistics once; shuffles hand them out
+            float my_mean = 0.f, my_rstd = 0.f;
+            bool my_exact = false;
             if (lane < R) {
-                float t = 0.f;
-                for (int q = 0; q < NW; ++q) t += rb1[lane * kRedStride + q];
+                float t = 0.f, u = 0.f;
+                for (int q = 0; q < NW; ++q) {
+                    t += rbs[lane * kRedStride + q];
+                    u += rbq[lane * kRedStride + q];
+                }
                 my_mean = t / static_cast<float>(N);
+                const float var = u / static_cast<float>(N) - my_mean * my_mean;
+                my_exact = lane < rows && !(var > 0.f && my_mean * my_mean <= 4.f * var);
+                my_rstd = __frsqrt_rn(var + a.eps);
             }
             float mean[R];
 #pragma unroll
-            for (int rr = 0; rr < R; ++rr) {
-                mean[rr] = __shfl_sync(0xffffffffu, my_mean, rr);
-                float acc = 0.f;
+            for (int rr = 0; rr < R; ++rr) mean[rr] = __shfl_sync(0xffffffffu, my_mean, rr);
+            if (__any_sync(0xffffffffu, my_exact)) {
 #pragma unroll
-                for (int j = 0; j < VPR; ++j)
-                    if (live(tid, j)) acc += sqdev8<E>(xv[rr][j], mean[rr]);
-                s1[rr] = warp_sum(acc);
-            }
-            if (lane == 0) {
+                for (int rr = 0; rr < R; ++rr) {
+                    float acc = 0.f;
 #pragma unroll
-                for (int rr = 0; rr < R; ++rr) rb2[rr * kRedStride + warp] = s1[rr];
-            }
-            named_bar_sync(1, nt);
-            float my_rstd = 0.f;
-            if (lane < R) {
-                float t = 0.f;
-                for (int q = 0; q < NW; ++q) t += rb2[lane * kRedStride + q];
-                my_rstd = row_rstd(t, N, a.eps);
+                    for (int j = 0; j < VPR; ++j)
+                        if (live(tid, j)) acc += sqdev8<E>(xv[rr][j], mean[rr]);
+                    s1[rr] = warp_sum(acc);
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int rr = 0; rr < R; ++rr) rbc[rr * kRedStride + warp] = s1[rr];
+                }
+                named_bar_sync(1, nt);
+                if (lane < R) {
+                    float t = 0.f;
+                    for (int q = 0; q < NW; ++q) t += rbc[lane * kRedStride + q];
+                    my_rstd = row_rstd(t, N, a.eps);
+                }
             }
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {

@@ -131,3 +131,25 @@ def test_non_power_of_two_widths_on_the_ring(N):
     y = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), 1e-5,
                               schedule=binding.RN_SCHED_PERSIST_BULK)
     assert_parity(bf16_bits(y), want, f"ln ring N={N}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("N", [4096, 8192, 16384])
+def test_rows_either_side_of_the_one_pass_bound(N, dtype):
+    # The ring takes the variance from one reduction (E[x^2] - mean^2) when
+    # mean^2 <= 4 var and falls back to the centred second pass otherwise:
+    # rows with mean / std from 0.5 to 3 put units on both sides, and every
+    # output must match the oracle either way.
+    M = 1200
+    g = torch.Generator().manual_seed(N + 7)
+    ratio = torch.tensor([0.5, 1.5, 1.99, 2.01, 2.5, 3.0, 0.0, 1.0])
+    xf = torch.randn(M, N, generator=g) + ratio[torch.arange(M) % len(ratio)][:, None]
+    x = xf.to(dtype)
+    w = rmsnorm_inputs(1, N, seed=8, dtype=dtype)[1]
+    b = norm_bias(N, seed=9, dtype=dtype)
+    f16 = dtype == torch.float16
+    want = oracle.layernorm(bf16_bits(x), bf16_bits(w), bf16_bits(b), 1e-5, f16=f16)
+    y = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), 1e-5,
+                              schedule=binding.RN_SCHED_PERSIST_BULK)
+    assert_parity(bf16_bits(y), want, f"ln one-pass bound N={N} {dtype}",
+                  fmt="f16" if f16 else "bf16")
