@@ -739,10 +739,9 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
 // stages per CTA, `ctas` co-resident CTAs per SM.  About 64 KiB in flight per
 // SM (two 32 KiB stages) streams best at every width from 4096 to 16384:
 // deeper rings and 64 KiB stages measured slower (more concurrent DRAM
-// streams, no more bandwidth).  4096-wide rows run two CTAs per SM up to
-// M = 8192 rows, where more independent pipelines shorten the ramp that
-// dominates such short launches; launches of 4096 rows take a third stage at
-// widths 8192 and 16384 for the same reason.  With the fused residual add a
+// streams, no more bandwidth).  Short launches are dominated by their ramp:
+// 4096-wide rows run two CTAs per SM up to M = 4096 rows and a third stage up
+// to 8192; launches of 4096 rows take a third stage at widths 8192 and 16384.  With the fused residual add a
 // stage carries R rows of x and R rows of r, so R is halved where needed to
 // keep a stage at 64 KiB or less; 32768-wide rows do not fit two such stages
 // and take the CTA-per-row schedule.
@@ -812,7 +811,12 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
     switch (N) {
         case 1024: *g = {128, 1, 8, 2, 1, false}; break;
         case 2048: *g = {256, 1, 8, 2, 1, false}; break;
-        case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1, false}; break;
+        case 4096:
+            // two CTAs per SM through 4096 rows, then one CTA with a third
+            // stage through 8192 rows, then two stages
+            *g = M <= 4096 ? BulkGeometry{256, 2, 4, 2, 2, false}
+                           : BulkGeometry{256, 2, 4, few_rows ? 3 : 2, 1, false};
+            break;
         case 8192: *g = {256, 4, 2, short_stages, 1, false}; break;
         case 16384: *g = {512, 4, 1, short_stages, 1, false}; break;
         case 32768: *g = {512, 8, 1, 2, 1, false}; break;
