@@ -135,6 +135,22 @@ def measured_peaks() -> dict:
         return {}
 
 
+def max_over_ranks(torch, dist, ms: float, device) -> float:
+    """The slowest rank's time: every rank ends with the max (NCCL on the GPU
+    box, gloo in the CPU tests)."""
+    if not dist:
+        return ms
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_rank: int, ms: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_rank (replicas: weak scaling)
+    in the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -531,15 +547,12 @@ def run_ours(args) -> int:
 
     total_ms = start.elapsed_time(end)
     instrumented_ms = start_i.elapsed_time(end_i)
-    if dist:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, total_ms, device)
     per_launch_ms = [statistics.fmean(ev[s][k].elapsed_time(ev[s][k + 1]) for s in range(K))
                      for k in range(n_launch)]
 
     bytes_step = step_bytes()
-    value = world * bytes_step * K / (total_ms * 1e-3) / 1e9
+    value = job_gbs(world, bytes_step * K, total_ms)
     peaks = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
@@ -728,11 +741,8 @@ def run_e2e(torch, binding, rms, qk, args, dist, device):
     torch.cuda.synchronize()
     wall_ms = (time.perf_counter() - t0) * 1e3
     ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    val = world * step_bytes() * E / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(torch, dist, ms, device)
+    val = job_gbs(world, step_bytes() * E, ms)
     return {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": round(ms / E, 3),
             "host_wall_ms_per_step": round(wall_ms / E, 3),
