@@ -204,3 +204,33 @@ def test_schedule_choice_does_not_depend_on_the_format():
             binding.add_rmsnorm_select_schedule(M, N)
         assert binding.row_norm_select_schedule(binding.RN_OP_LAYERNORM, M, N) == \
             binding.layernorm_select_schedule(M, N)
+
+
+@pytest.mark.parametrize("op", ["rms", "ln", "l2", "add"])
+def test_subnormal_inputs(op):
+    # x ~ 1e-6 lies among fp16 subnormals (the smallest normal is 2^-14 =
+    # 6.1e-5): the kernels widen them exactly, so with a tiny eps the rows
+    # normalise to O(1) outputs that must match the oracle
+    M, N = 600, 4096
+    g = torch.Generator().manual_seed(61)
+    x = (torch.randn(M, N, generator=g) * 1e-6).to(F16)
+    assert (bf16_bits(x) & 0x7C00 == 0).mean() > 0.9  # mostly subnormal
+    w = rmsnorm_inputs(1, N, seed=62, dtype=F16)[1]
+    b = norm_bias(N, seed=63, dtype=F16)
+    r = (torch.randn(M, N, generator=g) * 1e-6).to(F16)
+    eps = {"rms": 1e-14, "ln": 1e-14, "l2": 1e-12, "add": 1e-14}[op]
+    xb, wb = bf16_bits(x), bf16_bits(w)
+    if op == "rms":
+        want = oracle.rmsnorm(xb, wb, eps, f16=True)
+        got = binding.rmsnorm_fwd(x.cuda(), w.cuda(), eps)
+    elif op == "ln":
+        want = oracle.layernorm(xb, wb, bf16_bits(b), eps, f16=True)
+        got = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), eps)
+    elif op == "l2":
+        want = oracle.l2norm(xb, eps, f16=True)
+        got = binding.l2norm_fwd(x.cuda(), eps)
+    else:
+        h_want, want = oracle.add_rmsnorm(xb, bf16_bits(r), wb, eps, f16=True)
+        h, got = binding.add_rmsnorm_fwd(x.cuda(), r.cuda(), w.cuda(), eps)
+        assert np.array_equal(bf16_bits(h), h_want)
+    assert_parity(bf16_bits(got), want, f"f16 subnormal inputs {op}", fmt="f16")
