@@ -194,15 +194,28 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
         }
         uint16_t *yr = y + row * N;
         if constexpr (LN) {
-            float s1 = 0.f;
+            // the sum and the sum of squares in one pass; the centred second
+            // pass only where the mean is large against the spread (the same
+            // rule as the persistent schedule; a butterfly sum leaves the
+            // same bits in every lane, so the branch is warp-uniform)
+            float s1 = 0.f, q1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) s1 += sum8<E>(v[i]);  // absent chunks are zero
+            for (int i = 0; i < VPT; ++i) {  // absent chunks are zero
+                s1 += sum8<E>(v[i]);
+                q1 += sumsq8<E>(v[i]);
+            }
             const float mean = warp_sum(s1) / static_cast<float>(N);
-            float s2 = 0.f;
+            const float var = warp_sum(q1) / static_cast<float>(N) - mean * mean;
+            float rstd;
+            if (var > 0.f && mean * mean <= 4.f * var) {
+                rstd = __frsqrt_rn(var + eps);
+            } else {
+                float s2 = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                if (lane + 32 * i < cpr) s2 += sqdev8<E>(v[i], mean);
-            const float rstd = row_rstd(warp_sum(s2), N, eps);
+                for (int i = 0; i < VPT; ++i)
+                    if (lane + 32 * i < cpr) s2 += sqdev8<E>(v[i], mean);
+                rstd = row_rstd(warp_sum(s2), N, eps);
+            }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
@@ -234,7 +247,8 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
                                                             uint16_t *h_out, const uint16_t *b,
                                                             int l2) {
     __shared__ float red[2][32];
-    __shared__ float red2[2][32];  // LayerNorm's second reduction
+    __shared__ float red2[2][32];  // LayerNorm's sums of squares
+    __shared__ float red3[2][32];  // LayerNorm's centred squares (large-mean rows)
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x;
@@ -262,27 +276,45 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
         }
         uint16_t *yr = y + row * N;
         if constexpr (LN) {
-            // mean first, then the centred sum of squares: two exact passes
-            // over the register-resident row, two CTA reductions.
-            float s1 = 0.f;
+            // one CTA reduction of the sum and the sum of squares; a second
+            // over the centred squares only where the mean is large against
+            // the spread (every thread reads the same partials in the same
+            // order, so the branch is uniform)
+            float s1 = 0.f, q1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) s1 += sum8<E>(v[i]);  // absent chunks are zero
+            for (int i = 0; i < VPT; ++i) {  // absent chunks are zero
+                s1 += sum8<E>(v[i]);
+                q1 += sumsq8<E>(v[i]);
+            }
             s1 = warp_sum(s1);
-            if ((tid & 31) == 0) red[par][tid >> 5] = s1;
+            q1 = warp_sum(q1);
+            if ((tid & 31) == 0) {
+                red[par][tid >> 5] = s1;
+                red2[par][tid >> 5] = q1;
+            }
             __syncthreads();
-            float t1 = 0.f;
-            for (int k = 0; k < nw; ++k) t1 += red[par][k];
+            float t1 = 0.f, u1 = 0.f;
+            for (int k = 0; k < nw; ++k) {
+                t1 += red[par][k];
+                u1 += red2[par][k];
+            }
             const float mean = t1 / static_cast<float>(N);
-            float s2 = 0.f;
+            const float var = u1 / static_cast<float>(N) - mean * mean;
+            float rstd;
+            if (var > 0.f && mean * mean <= 4.f * var) {
+                rstd = __frsqrt_rn(var + eps);
+            } else {
+                float s2 = 0.f;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                if (tid + nt * i < cpr) s2 += sqdev8<E>(v[i], mean);
-            s2 = warp_sum(s2);
-            if ((tid & 31) == 0) red2[par][tid >> 5] = s2;
-            __syncthreads();
-            float t2 = 0.f;
-            for (int k = 0; k < nw; ++k) t2 += red2[par][k];
-            const float rstd = row_rstd(t2, N, eps);
+                for (int i = 0; i < VPT; ++i)
+                    if (tid + nt * i < cpr) s2 += sqdev8<E>(v[i], mean);
+                s2 = warp_sum(s2);
+                if ((tid & 31) == 0) red3[par][tid >> 5] = s2;
+                __syncthreads();
+                float t2 = 0.f;
+                for (int k = 0; k < nw; ++k) t2 += red3[par][k];
+                rstd = row_rstd(t2, N, eps);
+            }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
