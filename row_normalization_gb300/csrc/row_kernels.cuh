@@ -938,11 +938,13 @@ static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &
     BulkGeometry geo;
     // Up to 2048-wide rows one warp per row is ahead of the ring; wider rows
     // take the ring wherever it applies (3072-wide RMSNorm rows measured 0.85
-    // of the copy on the ring against 0.60 one CTA per row), except the fused
-    // add below 4096-wide generic rows, where one CTA per row keeps twice the
-    // loads in flight and measured ahead (0.94-0.97 against 0.89-0.94).
+    // of the copy on the ring against 0.60 one CTA per row) from 6 rows per SM
+    // up: with fewer, one CTA per row keeps every row in flight at once and
+    // measured ahead (608 x 16384: 0.90 against 0.76).  The fused add below
+    // 4096-wide generic rows also stays on one CTA per row, which keeps twice
+    // the loads in flight and measured ahead (0.94-0.97 against 0.89-0.94).
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    if (bulk_geometry(M, N, add, ln, &geo) && M >= 4LL * dev.sm_count &&
+    if (bulk_geometry(M, N, add, ln, &geo) && M >= 6LL * dev.sm_count &&
         !(add && geo.generic && N < 4096))
         return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
