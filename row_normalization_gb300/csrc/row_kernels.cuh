@@ -399,8 +399,17 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, i
 template <int VPR, int R, int NT>
 constexpr int bulk_max_threads() { return NT > 0 ? NT + 32 : (NT == 0 ? 288 : 544); }
 
+// Generic LayerNorm with at most two chunks per thread is built for two CTAs
+// per SM (96 registers, no spills): its per-row chain wants a second CTA's
+// warps more than it wants registers.  The other forms keep one CTA's full
+// register budget (the fused add spills at the two-CTA bound; RMSNorm and the
+// fused add measured no gain from a second CTA; power-of-two LayerNorm with
+// 1-CTA registers is faster over many rows).
+template <int VPR, int NT, bool LN>
+constexpr int bulk_min_ctas() { return (LN && NT == 0 && VPR <= 2) ? 2 : 1; }
+
 template <class E, int VPR, int R, int NT, bool ADD, bool LN>
-__global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), 1)
+__global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<VPR, NT, LN>())
     rms_persistent_bulk_kernel(const BulkArgs a) {
     constexpr bool GENERIC = NT <= 0;
     static_assert(!(ADD && LN), "the fused add is an RMSNorm prologue");
@@ -809,6 +818,13 @@ static bool bulk_geometry_generic(int N, bool add, bool ln, BulkGeometry *g) {
     int stages = static_cast<int>((65536 + stage - 1) / stage);
     if (stages < 2) stages = 2;
     if (stages > 4) stages = 4;
+    // LayerNorm with at most two chunks a thread: two CTAs per SM, two stages
+    // each (the second CTA lifted 16384 x 3072 from 0.68 to 0.79 of the copy;
+    // deeper rings measured 1% behind).
+    if (ln && vpr <= 2) {
+        *g = {nt, vpr, R, 2, 2, true};
+        return true;
+    }
     *g = {nt, vpr, R, stages, 1, true};
     return true;
 }
@@ -822,8 +838,17 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
         switch (N) {
             case 1024: *g = {128, 1, 8, 2, 1, false}; break;
             case 2048: *g = {256, 1, 8, 2, 1, false}; break;
-            case 4096: *g = {256, 2, 4, 2, few_rows ? 2 : 1, false}; break;
-            case 8192: *g = {256, 4, 2, 2, 1, false}; break;
+            case 4096:
+                // Up to 8192 rows the generic layout (the same 4-row stages)
+                // at two CTAs per SM (8192 rows: 0.73 -> 0.85); over more rows
+                // one CTA with the full register budget and a third stage.
+                if (few_rows) return bulk_geometry_generic(N, add, ln, g);
+                *g = {256, 2, 4, 3, 1, false};  // 3 stages: 0.96 -> 0.98 at 65536 rows
+                break;
+            // A third stage pays for LayerNorm (slower consumers than RMSNorm,
+            // whose two-stage rings measured 3-5% ahead of three) at 8192
+            // (16384 rows: 0.94 -> 0.97); at 16384 it measured even.
+            case 8192: *g = {256, 4, 2, 3, 1, false}; break;
             case 16384: *g = {256, 8, 1, 2, 1, false}; break;  // measured ahead of 512 x 4
             default: return false;
         }
@@ -860,23 +885,88 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
     return true;
 }
 
+// How many CTAs of one instantiation of the ring an SM holds at once with
+// `nt` consumers and `smem` bytes of dynamic shared memory (registers, shared
+// memory and threads all counted), or -1 when the runtime cannot say.  Opts
+// the instantiation into `smem_cap` bytes of shared memory on first use.
 template <class E, int VPR, int R, int NT, bool ADD, bool LN>
-static int launch_bulk_inst(const BulkArgs &a, int grid, size_t smem, int smem_cap,
-                            cudaStream_t st, int nt = NT) {
+static int bulk_fit(int nt, size_t smem, int smem_cap) {
     static std::atomic<int> attr_done[kMaxDevices];
+    // last answer per device: (consumers << 20 | smem) << 8 | CTAs, plus bit 63
+    static std::atomic<uint64_t> cache[kMaxDevices];
+    const auto kernel = rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>;
     const int dev = current_device_index();
-    if (dev < 0 || dev >= kMaxDevices) return RN_ERR_DEVICE;
+    if (dev < 0 || dev >= kMaxDevices) return -1;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_cap) != cudaSuccess) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cap) !=
+            cudaSuccess) {
             cudaGetLastError();
-            return RN_ERR_DEVICE;
+            return -1;
         }
         attr_done[dev].store(1, std::memory_order_release);
     }
-    return launch_pdl(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>, dim3(grid), dim3(nt + 32),
-                      smem, st, a);
+    const uint64_t key = (static_cast<uint64_t>(nt) << 20 | static_cast<uint64_t>(smem)) << 8;
+    const uint64_t hit = cache[dev].load(std::memory_order_acquire);
+    if ((hit >> 63) && ((hit & ~(1ull << 63)) >> 8) == (key >> 8)) return static_cast<int>(hit & 0xFF);
+    int fit = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, nt + 32, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (fit > 255) fit = 255;
+    cache[dev].store((1ull << 63) | key | static_cast<uint64_t>(fit), std::memory_order_release);
+    return fit;
+}
+
+// Launches one instantiation of the ring on min(M, SMs x ctas) CTAs.  A
+// request for more than one CTA per SM is clamped to what the SM holds at
+// once: CTAs beyond that would run as a second wave behind the first instead
+// of beside it.
+template <class E, int VPR, int R, int NT, bool ADD, bool LN>
+static int launch_bulk_inst(const BulkArgs &a, int sm_count, int ctas, size_t smem, int smem_cap,
+                            cudaStream_t st, int nt = NT) {
+    const int fit = bulk_fit<E, VPR, R, NT, ADD, LN>(nt, smem, smem_cap);
+    if (fit < 0) return RN_ERR_DEVICE;
+    if (fit == 0) return RN_ERR_SHAPE;
+    if (ctas > fit) ctas = fit;
+    int64_t grid = static_cast<int64_t>(sm_count) * ctas;
+    if (grid > a.M) grid = a.M;
+    return launch_pdl(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>,
+                      dim3(static_cast<unsigned>(grid)), dim3(nt + 32), smem, st, a);
+}
+
+// LayerNorm at a generic width: the layout with the most chunks a thread
+// (1, 2, 4 or 8) whose consumers, rounded up to whole warps, cover the row
+// with at most a tenth of their chunks masked, number at least three warps,
+// and leave room for two or three such CTAs on an SM, each with a two-stage
+// ring.  Several independent CTAs a SM keep the per-row chain of LayerNorm
+// (reduce, derive mean and scale, normalise) in flight in parallel; one CTA
+// with more threads on the same row does not (16384 x 5120: 0.65 -> 0.93 of
+// the copy; 6144: 0.75 -> 0.88; 3072: 0.79 -> 0.85).  Leaves `geo` as it is
+// when no layout qualifies (a masked tenth or more, or one CTA an SM).
+template <class E>
+static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
+    const int cpr = N >> 3;
+    for (int v = 8; v >= 1; v >>= 1) {
+        const int per = (cpr + v - 1) / v;
+        if (per > 256) return;  // fewer chunks a thread only need more consumers
+        const int nt = ((per + 31) / 32) * 32;
+        if (nt < 96 || 10LL * cpr < 9LL * nt * v) continue;
+        const int R = 8 / v;
+        if (2ull * R * N * 2 > 200 * 1024) continue;
+        const size_t smem = bulk_smem_bytes(2, R, N);
+        int fit = -1;
+        switch (v) {
+            case 8: fit = bulk_fit<E, 8, 1, 0, false, true>(nt, smem, smem_cap); break;
+            case 4: fit = bulk_fit<E, 4, 2, 0, false, true>(nt, smem, smem_cap); break;
+            case 2: fit = bulk_fit<E, 2, 4, 0, false, true>(nt, smem, smem_cap); break;
+            case 1: fit = bulk_fit<E, 1, 8, 0, false, true>(nt, smem, smem_cap); break;
+        }
+        if (fit >= 2) {
+            *geo = {nt, v, R, 2, fit < 3 ? fit : 3, true};
+            return;
+        }
+    }
 }
 
 template <class E, bool ADD, bool LN>
@@ -887,6 +977,9 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     const int N = j.N;
     if (!bulk_geometry(j.M, N, ADD, LN, &geo)) return RN_ERR_SHAPE;
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
+    if constexpr (LN) {
+        if (geo.generic && (debug_flags & 0x1FF0) == 0) ln_multi_cta_layout<E>(N, smem_cap, &geo);
+    }
     const size_t stage_cost = static_cast<size_t>(NIN) * geo.R * N * 2 + 16;
     int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N, NIN)) / stage_cost);
     if (max_stages > 16) max_stages = 16;
@@ -898,40 +991,38 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     if (stages * ctas_per_sm > max_stages) stages = max_stages / ctas_per_sm;
     if (stages < 2) return RN_ERR_SHAPE;
     const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN);
-    int64_t grid = static_cast<int64_t>(dev.sm_count) * ctas_per_sm;
-    if (grid > j.M) grid = j.M;
     BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.l2, j.M, N, j.eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
-    const int g = static_cast<int>(grid);
+    const int sm = dev.sm_count, c = ctas_per_sm;
     if (geo.generic) {
         if constexpr (ADD || LN) {  // at most 256 consumers
             switch (geo.vpr) {
-                case 1: return launch_bulk_inst<E, 1, 8, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 2: return launch_bulk_inst<E, 2, 4, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 4: return launch_bulk_inst<E, 4, 2, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 8: return launch_bulk_inst<E, 8, 1, 0, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 1: return launch_bulk_inst<E, 1, 8, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 2: return launch_bulk_inst<E, 2, 4, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 4: return launch_bulk_inst<E, 4, 2, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 8: return launch_bulk_inst<E, 8, 1, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
             }
         } else {  // up to 512 consumers
             switch (geo.vpr) {
-                case 1: return launch_bulk_inst<E, 1, 8, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 2: return launch_bulk_inst<E, 2, 4, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 4: return launch_bulk_inst<E, 4, 2, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
-                case 8: return launch_bulk_inst<E, 8, 1, -1, ADD, LN>(a, g, smem, smem_cap, st, geo.nt);
+                case 1: return launch_bulk_inst<E, 1, 8, -1, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 2: return launch_bulk_inst<E, 2, 4, -1, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 4: return launch_bulk_inst<E, 4, 2, -1, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 8: return launch_bulk_inst<E, 8, 1, -1, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
             }
         }
         return RN_ERR_SHAPE;
     }
     switch (N) {
-        case 1024: return launch_bulk_inst<E, 1, 8, 128, ADD, LN>(a, g, smem, smem_cap, st);
-        case 2048: return launch_bulk_inst<E, 1, 8, 256, ADD, LN>(a, g, smem, smem_cap, st);
-        case 4096: return launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, g, smem, smem_cap, st);
-        case 8192: return launch_bulk_inst<E, 4, 2, 256, ADD, LN>(a, g, smem, smem_cap, st);
+        case 1024: return launch_bulk_inst<E, 1, 8, 128, ADD, LN>(a, sm, c, smem, smem_cap, st);
+        case 2048: return launch_bulk_inst<E, 1, 8, 256, ADD, LN>(a, sm, c, smem, smem_cap, st);
+        case 4096: return launch_bulk_inst<E, 2, 4, 256, ADD, LN>(a, sm, c, smem, smem_cap, st);
+        case 8192: return launch_bulk_inst<E, 4, 2, 256, ADD, LN>(a, sm, c, smem, smem_cap, st);
         case 16384:
-            if constexpr (LN) return launch_bulk_inst<E, 8, 1, 256, ADD, LN>(a, g, smem, smem_cap, st);
-            else return launch_bulk_inst<E, 4, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
+            if constexpr (LN) return launch_bulk_inst<E, 8, 1, 256, ADD, LN>(a, sm, c, smem, smem_cap, st);
+            else return launch_bulk_inst<E, 4, 1, 512, ADD, LN>(a, sm, c, smem, smem_cap, st);
         case 32768:
             if constexpr (!ADD && !LN)
-                return launch_bulk_inst<E, 8, 1, 512, ADD, LN>(a, g, smem, smem_cap, st);
+                return launch_bulk_inst<E, 8, 1, 512, ADD, LN>(a, sm, c, smem, smem_cap, st);
             break;
     }
     return RN_ERR_SHAPE;

@@ -122,15 +122,21 @@ def test_full_size_sampled_rows(M, N):
     assert_parity(bf16_bits(y.index_select(0, idx)), want, f"ln sampled M={M} N={N}")
 
 
-@pytest.mark.parametrize("N", [3072, 5120, 12288, 1000])
-def test_non_power_of_two_widths_on_the_ring(N):
+# Generic widths take one of several ring layouts: 1, 2, 4 or 8 chunks a
+# thread, with two or three CTAs an SM where a layout covers the row with few
+# masked chunks (1000, 2560, 3072, 3584, 5120, 6144, 10240), else one CTA with
+# up to 256 consumers (6656, 12288).  2001 rows leave a ragged last round.
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("N", [1000, 2560, 3072, 3584, 5120, 6144, 6656, 10240, 12288])
+def test_non_power_of_two_widths_on_the_ring(N, dtype):
     M = 2001
-    x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=N + 1)
-    b = norm_bias(N, seed=N + 2)
-    want = oracle.layernorm(bf16_bits(x), bf16_bits(w), bf16_bits(b), 1e-5)
+    x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=N + 1, dtype=dtype)
+    b = norm_bias(N, seed=N + 2, dtype=dtype)
+    f16 = dtype == torch.float16
+    want = oracle.layernorm(bf16_bits(x), bf16_bits(w), bf16_bits(b), 1e-5, f16=f16)
     y = binding.layernorm_fwd(x.cuda(), w.cuda(), b.cuda(), 1e-5,
                               schedule=binding.RN_SCHED_PERSIST_BULK)
-    assert_parity(bf16_bits(y), want, f"ln ring N={N}")
+    assert_parity(bf16_bits(y), want, f"ln ring N={N} {dtype}", fmt="f16" if f16 else "bf16")
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
