@@ -70,6 +70,12 @@ def qk_bytes(T: int, r: int) -> int:
     return T * (2 * (HQ + HKV) * D * 2 + r * 4 + 8) + 2 * D * 2
 
 
+def qk_v_bytes(T: int) -> int:
+    """The V heads' bytes if they were read and written too (the count that
+    treats QKV as moved in and out whole): reported beside the ideal count."""
+    return T * HKV * D * 2 * 2
+
+
 def add_bytes(M: int, N: int) -> int:
     """Ideal bytes of the fused residual add: read x and r, write h and y, w once."""
     return 8 * M * N + 2 * N
@@ -476,7 +482,8 @@ def steady_per_shape(torch, binding, rms, qk, reps: int, hbm_peak: float) -> lis
         out.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
                     "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                     "frac_of_measured": round(gbs / hbm_peak, 4),
-                    "stream_same_bytes_frac": copy_frac(b)})
+                    "stream_same_bytes_frac": copy_frac(b),
+                    "gbs_counting_v": round((b + qk_v_bytes(QK_T)) / (ms * 1e-3) / 1e9, 1)})
     return out
 
 
@@ -579,7 +586,9 @@ def run_ours(args) -> int:
         per_shape.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
                           "kernel": QK_KERNELS.get(qs, str(qs)),
                           "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,
-                          "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
+                          "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1),
+                          "gbs_counting_v": round((b + qk_v_bytes(QK_T))
+                                                  / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
     for p in per_shape:
         p["frac_of_measured"] = round(p["gbs"] / hbm_peak, 4)
     dom = max(per_shape, key=lambda p: p["us"])
