@@ -395,9 +395,12 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, i
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
 // NT <= 0 is the generic form: the consumer count comes from the launch
 // (blockDim.x - 32, a multiple of 32; at most 256 for NT == 0, 512 for
-// NT == -1) and chunks past the end of a row (any N % 8 == 0) are masked.
+// NT == -1, 192 for NT == -2) and chunks past the end of a row (any
+// N % 8 == 0) are masked.
 template <int VPR, int R, int NT>
-constexpr int bulk_max_threads() { return NT > 0 ? NT + 32 : (NT == 0 ? 288 : 544); }
+constexpr int bulk_max_threads() {
+    return NT > 0 ? NT + 32 : (NT == 0 ? 288 : (NT == -2 ? 224 : 544));
+}
 
 // Generic LayerNorm with at most two chunks per thread is built for two CTAs
 // per SM (96 registers, no spills): its per-row chain wants a second CTA's
@@ -405,8 +408,12 @@ constexpr int bulk_max_threads() { return NT > 0 ? NT + 32 : (NT == 0 ? 288 : 54
 // register budget (the fused add spills at the two-CTA bound; RMSNorm and the
 // fused add measured no gain from a second CTA; power-of-two LayerNorm with
 // 1-CTA registers is faster over many rows).
+// NT == -2 is a second build of generic LayerNorm at 8 chunks a thread, for
+// two CTAs of at most 192 consumers (128 registers, no spills, against 165 in
+// the one-CTA build): the launcher takes it only where the one-CTA build's
+// registers leave one CTA an SM (12288-wide rows: 0.76 -> 0.83 of the copy).
 template <int VPR, int NT, bool LN>
-constexpr int bulk_min_ctas() { return (LN && NT == 0 && VPR <= 2) ? 2 : 1; }
+constexpr int bulk_min_ctas() { return ((LN && NT == 0 && VPR <= 2) || NT == -2) ? 2 : 1; }
 
 template <class E, int VPR, int R, int NT, bool ADD, bool LN>
 __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<VPR, NT, LN>())
@@ -788,7 +795,8 @@ static int launch_cta_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &d
 // and take the CTA-per-row schedule.
 struct BulkGeometry {
     int nt, vpr, R, stages, ctas;
-    bool generic;  // masked instantiation with a run-time consumer count
+    bool generic;        // masked instantiation with a run-time consumer count
+    bool tight = false;  // LayerNorm's two-CTA build at 8 chunks a thread (NT == -2)
 };
 
 // Rows that are not a power-of-two width (any N % 8 == 0 from 512 to 32768)
@@ -941,11 +949,13 @@ static int launch_bulk_inst(const BulkArgs &a, int sm_count, int ctas, size_t sm
 // (1, 2, 4 or 8) whose consumers, rounded up to whole warps, cover the row
 // with at most a tenth of their chunks masked, number at least three warps,
 // and leave room for two or three such CTAs on an SM, each with a two-stage
-// ring.  Several independent CTAs a SM keep the per-row chain of LayerNorm
-// (reduce, derive mean and scale, normalise) in flight in parallel; one CTA
-// with more threads on the same row does not (16384 x 5120: 0.65 -> 0.93 of
-// the copy; 6144: 0.75 -> 0.88; 3072: 0.79 -> 0.85).  Leaves `geo` as it is
-// when no layout qualifies (a masked tenth or more, or one CTA an SM).
+// ring (at 8 chunks, in the two-CTA build when the one-CTA build's registers
+// leave room for one).  Several independent CTAs a SM keep the per-row chain
+// of LayerNorm (reduce, derive mean and scale, normalise) in flight in
+// parallel; one CTA with more threads on the same row does not (16384 x 5120:
+// 0.65 -> 0.93 of the copy; 6144: 0.75 -> 0.88; 3072: 0.79 -> 0.85).  Leaves
+// `geo` as it is when no layout qualifies (a masked tenth or more, or one CTA
+// an SM).
 template <class E>
 static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
     const int cpr = N >> 3;
@@ -959,7 +969,16 @@ static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
         const size_t smem = bulk_smem_bytes(2, R, N);
         int fit = -1;
         switch (v) {
-            case 8: fit = bulk_fit<E, 8, 1, 0, false, true>(nt, smem, smem_cap); break;
+            case 8:
+                fit = bulk_fit<E, 8, 1, 0, false, true>(nt, smem, smem_cap);
+                if (fit < 2 && nt <= 192) {  // the two-CTA build, at fewer registers
+                    const int f2 = bulk_fit<E, 8, 1, -2, false, true>(nt, smem, smem_cap);
+                    if (f2 >= 2) {
+                        *geo = {nt, v, R, 2, f2 < 3 ? f2 : 3, true, true};
+                        return;
+                    }
+                }
+                break;
             case 4: fit = bulk_fit<E, 4, 2, 0, false, true>(nt, smem, smem_cap); break;
             case 2: fit = bulk_fit<E, 2, 4, 0, false, true>(nt, smem, smem_cap); break;
             case 1: fit = bulk_fit<E, 1, 8, 0, false, true>(nt, smem, smem_cap); break;
@@ -1002,7 +1021,13 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
                 case 1: return launch_bulk_inst<E, 1, 8, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
                 case 2: return launch_bulk_inst<E, 2, 4, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
                 case 4: return launch_bulk_inst<E, 4, 2, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
-                case 8: return launch_bulk_inst<E, 8, 1, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
+                case 8:
+                    if constexpr (LN) {
+                        if (geo.tight)
+                            return launch_bulk_inst<E, 8, 1, -2, ADD, LN>(a, sm, c, smem, smem_cap, st,
+                                                                          geo.nt);
+                    }
+                    return launch_bulk_inst<E, 8, 1, 0, ADD, LN>(a, sm, c, smem, smem_cap, st, geo.nt);
             }
         } else {  // up to 512 consumers
             switch (geo.vpr) {

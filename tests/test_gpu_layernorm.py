@@ -124,10 +124,12 @@ def test_full_size_sampled_rows(M, N):
 
 # Generic widths take one of several ring layouts: 1, 2, 4 or 8 chunks a
 # thread, with two or three CTAs an SM where a layout covers the row with few
-# masked chunks (1000, 2560, 3072, 3584, 5120, 6144, 10240), else one CTA with
-# up to 256 consumers (6656, 12288).  2001 rows leave a ragged last round.
+# masked chunks (1000, 2560, 3072, 3584, 5120, 6144, 10240; 11776 and 12288 in
+# the two-CTA build at 8 chunks), else one CTA with up to 256 consumers (6656,
+# 14336).  2001 rows leave a ragged last round.
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("N", [1000, 2560, 3072, 3584, 5120, 6144, 6656, 10240, 12288])
+@pytest.mark.parametrize("N", [1000, 2560, 3072, 3584, 5120, 6144, 6656, 10240, 11776, 12288,
+                               14336])
 def test_non_power_of_two_widths_on_the_ring(N, dtype):
     M = 2001
     x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=N + 1, dtype=dtype)
