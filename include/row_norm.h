@@ -135,9 +135,13 @@ enum {
  * returns.  `debug_flags` is 0 in normal use.  Tests and tuning set:
  *   bit 0      the persistent schedule never issues its copies, so its
  *              waits run out (exercises the timeout path);
- *   bits 4-7   persistent schedule: CTAs per SM (0 = the tuned value);
+ *   bits 4-7   persistent schedule: CTAs per SM (0 = the tuned value),
+ *              lowered to what the SM's shared memory (at two stages a
+ *              CTA) and registers hold at once;
  *   bits 8-12  persistent schedule: ring stages, capped by shared memory
- *              (0 = the tuned value). */
+ *              (0 = the tuned value).
+ * Setting bits 4-12 also keeps LayerNorm at generic widths on its one-CTA
+ * layout (its multi-CTA layouts are chosen only when both are 0). */
 int rmsnorm_fwd_sched(const rn_bf16 *x, const rn_bf16 *w, float eps,
                       int64_t M, int64_t N, rn_bf16 *y, int schedule,
                       uint64_t wait_timeout_ns, int debug_flags,

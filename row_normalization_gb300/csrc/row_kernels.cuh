@@ -1009,6 +1009,9 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     if (forced_stages > 0) stages = forced_stages;
     int ctas_per_sm = (debug_flags >> 4) & 0xF;
     if (ctas_per_sm <= 0) ctas_per_sm = geo.ctas;
+    // The CTAs of an SM share its shared memory: give up stages first (down
+    // to two a CTA), then CTAs.  Registers are checked at launch.
+    while (ctas_per_sm > 1 && max_stages / ctas_per_sm < 2) --ctas_per_sm;
     if (stages * ctas_per_sm > max_stages) stages = max_stages / ctas_per_sm;
     if (stages < 2) return RN_ERR_SHAPE;
     const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN);

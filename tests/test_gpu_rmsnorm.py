@@ -82,6 +82,19 @@ def test_two_ctas_per_sm_variant():
     assert_parity(bf16_bits(y), want, "2 CTAs/SM")
 
 
+@pytest.mark.parametrize("N,ctas", [(16384, 8), (32768, 4), (5120, 15)])
+def test_more_ctas_per_sm_than_fit_are_clamped(N, ctas):
+    # A request for more CTAs an SM than registers and shared memory allow is
+    # clamped to what fits (otherwise the rest would queue as a second wave);
+    # the rows still all come out right, ragged last round included.
+    M = 1301
+    x, w = rmsnorm_inputs(M, N, seed=N + ctas)
+    want = oracle.rmsnorm(bf16_bits(x), bf16_bits(w), 1e-6)
+    y = binding.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6, schedule=binding.RN_SCHED_PERSIST_BULK,
+                            debug_flags=ctas << 4)
+    assert_parity(bf16_bits(y), want, f"ring N={N} asking {ctas} CTAs/SM")
+
+
 def exact_rmsnorm(x, w, eps):
     """Unrounded RMSNorm outputs in float64 (the oracle's row scale)."""
     xb, wb = bf16_bits(x), bf16_bits(w)
