@@ -672,50 +672,52 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
                         if (live(tid, j))
-                            st16(yr + 8 * (tid + j * nt), (WIDE_W ? ln8w<E>(xv[rr][j], &wf[4 * j], bv[j], mean[rr], rstd)
-                                          : ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd)));
+                            st16(yr + 8 * (tid + j * nt),
+                                 WIDE_W ? ln8w<E>(xv[rr][j], &wf[4 * j], bv[j], mean[rr], rstd)
+                                        : ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
                 }
             }
-            continue;
-        }
-        float ss[R];
+        } else {
+            float ss[R];
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
-            float acc = 0.f;
+            for (int rr = 0; rr < R; ++rr) {
+                float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < VPR; ++j) acc += sumsq8<E>(xv[rr][j]);
-            ss[rr] = warp_sum(acc);
-        }
-        // Same for x: hold it packed across the barrier, widen again after.
+                for (int j = 0; j < VPR; ++j) acc += sumsq8<E>(xv[rr][j]);
+                ss[rr] = warp_sum(acc);
+            }
+            // Same for x: hold it packed across the barrier, widen again after.
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr)
-#pragma unroll
-            for (int j = 0; j < VPR; ++j)
-                asm volatile("" : "+r"(xv[rr][j].x), "+r"(xv[rr][j].y), "+r"(xv[rr][j].z),
-                             "+r"(xv[rr][j].w));
-        float *rb = red + (k & 1) * R * kRedStride;
-        if (lane == 0) {
-#pragma unroll
-            for (int rr = 0; rr < R; ++rr) rb[rr * kRedStride + warp] = ss[rr];
-        }
-        named_bar_sync(1, nt);
-        if (flags[k & 1]) break;  // same decision in every consumer warp
-        // Lane rr finishes row rr's sum and scale once; a shuffle hands it to
-        // the warp (instead of every thread redoing all R rows).
-        float my_scale = 0.f;
-        if (lane < R) {
-            float tot = 0.f;
-            for (int q = 0; q < NW; ++q) tot += rb[lane * kRedStride + q];
-            my_scale = row_scale(tot, N, a.eps, a.l2);
-        }
-#pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
-            const float rstd = __shfl_sync(0xffffffffu, my_scale, rr);
-            if (rr < rows) {
-                uint16_t *yr = a.y + (r0 + rr) * N;
+            for (int rr = 0; rr < R; ++rr)
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
-                    if (live(tid, j)) st16(yr + 8 * (tid + j * nt), scale8<E>(xv[rr][j], wv[j], rstd));
+                    asm volatile("" : "+r"(xv[rr][j].x), "+r"(xv[rr][j].y), "+r"(xv[rr][j].z),
+                                 "+r"(xv[rr][j].w));
+            float *rb = red + (k & 1) * R * kRedStride;
+            if (lane == 0) {
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) rb[rr * kRedStride + warp] = ss[rr];
+            }
+            named_bar_sync(1, nt);
+            if (flags[k & 1]) break;  // same decision in every consumer warp
+            // Lane rr finishes row rr's sum and scale once; a shuffle hands it
+            // to the warp (instead of every thread redoing all R rows).
+            float my_scale = 0.f;
+            if (lane < R) {
+                float tot = 0.f;
+                for (int q = 0; q < NW; ++q) tot += rb[lane * kRedStride + q];
+                my_scale = row_scale(tot, N, a.eps, a.l2);
+            }
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                const float rstd = __shfl_sync(0xffffffffu, my_scale, rr);
+                if (rr < rows) {
+                    uint16_t *yr = a.y + (r0 + rr) * N;
+#pragma unroll
+                    for (int j = 0; j < VPR; ++j)
+                        if (live(tid, j))
+                            st16(yr + 8 * (tid + j * nt), scale8<E>(xv[rr][j], wv[j], rstd));
+                }
             }
         }
     }
