@@ -98,6 +98,9 @@ def _load():
         lib.rn_oracle_rope_cos_sin.argtypes = [ctypes.c_double, ctypes.c_int64,
                                                ctypes.c_int, f32p]
         lib.rn_oracle_rope_cos_sin.restype = ctypes.c_int
+        lib.rn_oracle_rope_cos_sin_bf16.argtypes = [ctypes.c_double, ctypes.c_int64,
+                                                    ctypes.c_int, u16p]
+        lib.rn_oracle_rope_cos_sin_bf16.restype = ctypes.c_int
         lib.rn_oracle_qk_norm_rope.argtypes = [
             u16p, u16p, u16p, f32p, i64p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float]
@@ -188,6 +191,15 @@ def rope_cos_sin(theta: float, max_pos: int, rotary_dim: int) -> np.ndarray:
     out = np.zeros((max_pos, rotary_dim), dtype=np.float32)
     _check(_load().rn_oracle_rope_cos_sin(float(theta), int(max_pos), int(rotary_dim),
                                           _ptr(out, ctypes.c_float)), "rope_cos_sin")
+    return out
+
+
+def rope_cos_sin_bf16(theta: float, max_pos: int, rotary_dim: int) -> np.ndarray:
+    """bf16 table (uint16 bit patterns) [max_pos, rotary_dim]: the same angles as
+    rope_cos_sin, each entry rounded once from double to bf16."""
+    out = np.zeros((max_pos, rotary_dim), dtype=np.uint16)
+    _check(_load().rn_oracle_rope_cos_sin_bf16(float(theta), int(max_pos), int(rotary_dim),
+                                               _ptr(out, ctypes.c_uint16)), "rope_cos_sin_bf16")
     return out
 
 

@@ -15,7 +15,8 @@
  *     QKV: "[pretuned] Optimize fused_qk_norm_rope on B200", section
  *     "Summary" (norm over the whole head, Q/K weights, RoPE, one store per
  *     half; partial rotary still normalises the non-rotary tail).
- *   - The rotary cos/sin table used as an input by the above.
+ *   - The rotary cos/sin table used as an input by the above, with binary32
+ *     or bf16 entries.
  *   - L2Norm (x / max(||x||, eps)): "[Inductor] Codegen Gluon", section 3.2.
  *   - Fused residual add + RMSNorm: "TorchInductor: from ATen IR to Triton
  *     kernel", sections 14.3 and 14.27.
@@ -217,6 +218,31 @@ int rn_oracle_rope_cos_sin(double theta, int64_t max_pos, int rotary_dim,
             double a = (double)p * f;
             row[i] = (float)cos(a);
             row[half + i] = (float)sin(a);
+        }
+    }
+    return 0;
+}
+
+/* The same table with bf16 entries: the angle and the trig functions in
+ * double as above, each entry rounded ONCE to bf16 (ties to even), not
+ * through binary32 (rounding twice could land on the other neighbour).  A
+ * bf16 table is read by the fused kernel widened exactly to fp32, so the
+ * fused oracle below takes it as the binary32 values it widens to. */
+int rn_oracle_rope_cos_sin_bf16(double theta, int64_t max_pos, int rotary_dim,
+                                uint16_t *cos_sin)
+{
+    if (max_pos < 0 || rotary_dim <= 0 || (rotary_dim & 1) || !(theta > 0.0))
+        return -3;
+    if (max_pos == 0) return 0;
+    if (!cos_sin) return -1;
+    const int half = rotary_dim / 2;
+    for (int64_t p = 0; p < max_pos; ++p) {
+        uint16_t *row = cos_sin + p * (int64_t)rotary_dim;
+        for (int i = 0; i < half; ++i) {
+            double f = pow(theta, -2.0 * (double)i / (double)rotary_dim);
+            double a = (double)p * f;
+            row[i] = rn_oracle_double_to_bf16(cos(a));
+            row[half + i] = rn_oracle_double_to_bf16(sin(a));
         }
     }
     return 0;

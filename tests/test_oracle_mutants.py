@@ -40,6 +40,10 @@ MUTANTS = {
                           "double f = pow(theta, -1.0 * (double)i / (double)rotary_dim);"),
     "table_sin_first": ("row[i] = (float)cos(a);\n            row[half + i] = (float)sin(a);",
                         "row[i] = (float)sin(a);\n            row[half + i] = (float)cos(a);"),
+    "table_bf16_through_float": ("row[i] = rn_oracle_double_to_bf16(cos(a));\n            row[half + i] = rn_oracle_double_to_bf16(sin(a));",
+                                 "row[i] = rn_oracle_double_to_bf16((double)(float)cos(a));\n            row[half + i] = rn_oracle_double_to_bf16((double)(float)sin(a));"),
+    "table_bf16_sin_first": ("row[i] = rn_oracle_double_to_bf16(cos(a));\n            row[half + i] = rn_oracle_double_to_bf16(sin(a));",
+                             "row[i] = rn_oracle_double_to_bf16(sin(a));\n            row[half + i] = rn_oracle_double_to_bf16(cos(a));"),
     "gptj_partner": ("int b = style ? 2 * i + 1 : i + half;", "int b = style ? 2 * i + 2 - (2 * i + 2) / rotary_dim : i + half;"),
     "gptj_cos_index": ("int a = style ? 2 * i : i;", "int a = style ? 2 * i + 1 : i;"),
     "l2_norm_squared": ("double nrm = sqrt(ss);", "double nrm = ss;"),

@@ -272,6 +272,44 @@ class TestRopeTable:
         assert abs(t[1, 1] - math.cos(0.01)) < 1e-7
         assert abs(t[2, 3] - math.sin(0.02)) < 1e-7
 
+    # The bf16 table: the same angles, each entry rounded once to bf16.
+
+    def test_bf16_position_zero_is_identity(self):
+        t = oracle.rope_cos_sin_bf16(1e6, 4, 128)
+        assert np.all(t[0, :64] == 0x3F80) and np.all(t[0, 64:] == 0)
+
+    def test_bf16_unit_circle(self):
+        t = bits_to_f64(oracle.rope_cos_sin_bf16(1e6, 2048, 64))
+        c, s = t[:, :32], t[:, 32:]
+        # each entry within half a bf16 step (2^-9 relative): c^2 + s^2 within 2^-7 of 1
+        assert np.max(np.abs(c * c + s * s - 1.0)) < 2**-7
+
+    @pytest.mark.parametrize("theta,r,p,i", [(10000.0, 4, 1, 0), (10000.0, 4, 1, 1),
+                                             (1e6, 128, 131071, 0), (1e6, 128, 131071, 5),
+                                             (1e6, 64, 99991, 31), (1e6, 128, 7, 63)])
+    def test_bf16_entries_against_decimal(self, theta, r, p, i):
+        t = oracle.rope_cos_sin_bf16(theta, p + 1, r)
+        a = Decimal(p) * Decimal(theta) ** (Decimal(-2 * i) / Decimal(r))
+        assert t[p, i] == round_bf16(dcos(a))
+        assert t[p, r // 2 + i] == round_bf16(dsin(a))
+
+    @pytest.mark.parametrize("p,col", [(137, 59), (1247, 50), (6883, 60), (6985, 16)])
+    def test_bf16_entries_rounded_once(self, p, col):
+        # At these entries (theta 1e6, r 64) the binary32 value lies exactly
+        # halfway between two bf16 values and ties to the even one, which is
+        # not the bf16 nearest the exact value: a table rounded through
+        # binary32 would differ here.
+        r, half = 64, 32
+        k = col % half
+        a = Decimal(p) * Decimal(1e6) ** (Decimal(-2 * k) / Decimal(r))
+        exact = dcos(a) if col < half else dsin(a)
+        t = oracle.rope_cos_sin_bf16(1e6, p + 1, r)
+        assert t[p, col] == round_bf16(exact)
+        f32 = int(oracle.rope_cos_sin(1e6, p + 1, r).view(np.uint32)[p, col])
+        assert f32 & 0xFFFF == 0x8000
+        twice = (f32 >> 16) + ((f32 >> 16) & 1)  # ties to even from the binary32 value
+        assert twice != t[p, col]
+
 
 # ---------------------------------------------------------------------------
 # fused Q/K RMSNorm + neox RoPE
