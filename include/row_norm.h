@@ -15,7 +15,9 @@
  *                     reduce over the whole head in registers, apply the Q/K
  *                     weight and the rotation, store each half once; partial
  *                     rotary still normalises the non-rotary tail.
- *   rope_cos_sin_table  builds the cos/sin table the rotary step reads.
+ *   rope_cos_sin_table  builds the cos/sin table the rotary step reads
+ *                     (fp32 entries; rope_cos_sin_table_bf16 for bf16 ones,
+ *                     which qk_norm_rope_fwd_ex_bf16_table reads).
  *   l2norm_fwd        y = x / max(||x||_2, eps), row by row: one reduction, a
  *                     scale by the inverse norm ("[Inductor] Codegen Gluon",
  *                     section 3.2).
@@ -344,6 +346,20 @@ int qk_norm_rope_fwd_ex(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                         int schedule, uint64_t wait_timeout_ns, int debug_flags,
                         rn_stream_t stream);
 
+/* qk_norm_rope_fwd_ex with a bf16 table: cos_sin [max_pos, r] holds bf16
+ * entries (the same layout; see rope_cos_sin_table_bf16), which the rotation
+ * uses widened exactly to fp32.  Every other argument, requirement and error
+ * is that of qk_norm_rope_fwd_ex; cos_sin is 16-byte aligned.  The table's
+ * bytes per token halve (r * 2 instead of r * 4). */
+int qk_norm_rope_fwd_ex_bf16_table(rn_bf16 *qkv, const rn_bf16 *wq,
+                                   const rn_bf16 *wk, const rn_bf16 *cos_sin,
+                                   const int64_t *positions, int64_t T, int Hq,
+                                   int Hkv, int D, int rotary_dim, float eps,
+                                   int rope_style, int64_t max_pos,
+                                   int *d_err_flag, int schedule,
+                                   uint64_t wait_timeout_ns, int debug_flags,
+                                   rn_stream_t stream);
+
 /* The schedule (RN_QK_*) that qk_norm_rope_fwd picks for T tokens (RN_ERR_SHAPE
  * if T < 0).  When it picks RN_QK_BULK for a layout the ring cannot hold
  * (D = 64 with rotary_dim = 16, or a token wider than the ring's shared
@@ -357,6 +373,13 @@ int qk_norm_rope_select_schedule(int64_t T);
  * caller's DEVICE buffer cos_sin [max_pos, r] fp32.  theta > 0. */
 int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim,
                        float *cos_sin, rn_stream_t stream);
+
+/* rope_cos_sin_table with bf16 entries: the same fp64 angles and trig, each
+ * entry rounded once from double to bf16 (ties to even; not through fp32,
+ * which would round twice); written to the caller's DEVICE buffer
+ * cos_sin [max_pos, r] bf16, 16-byte aligned. */
+int rope_cos_sin_table_bf16(double theta, int64_t max_pos, int rotary_dim,
+                            rn_bf16 *cos_sin, rn_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status word                                                                */

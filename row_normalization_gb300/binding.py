@@ -98,6 +98,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qk_norm_rope_fwd_ex.restype = i32
         L.rope_cos_sin_table.argtypes = [f64, i64, i32, vp, vp]
         L.rope_cos_sin_table.restype = i32
+        L.qk_norm_rope_fwd_ex_bf16_table.argtypes = L.qk_norm_rope_fwd_ex.argtypes
+        L.qk_norm_rope_fwd_ex_bf16_table.restype = i32
+        L.rope_cos_sin_table_bf16.argtypes = [f64, i64, i32, vp, vp]
+        L.rope_cos_sin_table_bf16.restype = i32
         L.add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
         L.add_rmsnorm_fwd.restype = i32
         L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
@@ -362,7 +366,8 @@ def _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim):
     _need(qkv, "qkv", torch.bfloat16)
     _need(wq, "wq", torch.bfloat16)
     _need(wk, "wk", torch.bfloat16)
-    _need(cos_sin, "cos_sin", torch.float32)
+    # the table may hold fp32 or bf16 entries (the bf16 form has its own entry point)
+    _need(cos_sin, "cos_sin", torch.bfloat16 if cos_sin.dtype == torch.bfloat16 else torch.float32)
     _need(positions, "positions", torch.int64)
     T = qkv.shape[0]
     if qkv.numel() != T * (Hq + 2 * Hkv) * D:
@@ -384,6 +389,10 @@ def qk_norm_rope_fwd(qkv: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
     """In place: per-head RMSNorm of Q and K heads, then neox RoPE.  Returns qkv."""
     T = _qk_common(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim)
     L = load()
+    if cos_sin.dtype == torch.bfloat16:
+        return _qk_bf16_table(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
+                              RN_ROPE_NEOX, 0, None, schedule, wait_timeout_ns, debug_flags,
+                              stream, "qk_norm_rope_fwd")
     if schedule == RN_QK_AUTO and wait_timeout_ns == 0 and debug_flags == 0:
         rc = L.qk_norm_rope_fwd(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(), cos_sin.data_ptr(),
                                 positions.data_ptr(), T, Hq, Hkv, D, rotary_dim, eps,
@@ -394,6 +403,16 @@ def qk_norm_rope_fwd(qkv: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
                                       rotary_dim, eps, schedule, wait_timeout_ns, debug_flags,
                                       _stream(stream))
     _check(rc, "qk_norm_rope_fwd")
+    return qkv
+
+
+def _qk_bf16_table(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps, style,
+                   max_pos, err_ptr, schedule, wait_timeout_ns, debug_flags, stream, what):
+    rc = load().qk_norm_rope_fwd_ex_bf16_table(
+        qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(), cos_sin.data_ptr(), positions.data_ptr(), T,
+        Hq, Hkv, D, rotary_dim, eps, style, int(max_pos), err_ptr, schedule, wait_timeout_ns,
+        debug_flags, _stream(stream))
+    _check(rc, what)
     return qkv
 
 
@@ -408,6 +427,10 @@ def qk_norm_rope_fwd_ex(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary_dim,
     if err_flag is not None:
         _need(err_flag, "err_flag", torch.int32)
         ep = err_flag.data_ptr()
+    if cos_sin.dtype == torch.bfloat16:
+        return _qk_bf16_table(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
+                              rope_style, max_pos, ep, schedule, wait_timeout_ns, debug_flags,
+                              stream, "qk_norm_rope_fwd_ex")
     rc = load().qk_norm_rope_fwd_ex(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(),
                                     cos_sin.data_ptr(), positions.data_ptr(), T, Hq, Hkv, D,
                                     rotary_dim, eps, rope_style, int(max_pos), ep, schedule,
@@ -425,6 +448,12 @@ def qk_norm_rope_fwd_checked(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary
     _need(err_flag, "err_flag", torch.int32)
     if max_pos is None:
         max_pos = cos_sin.shape[0]
+    if cos_sin.dtype == torch.bfloat16:
+        if int(max_pos) < 1:
+            raise RowNormError("qk_norm_rope_fwd_checked", RN_ERR_SHAPE)
+        return _qk_bf16_table(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
+                              RN_ROPE_NEOX, max_pos, err_flag.data_ptr(), RN_QK_AUTO, 0, 0,
+                              stream, "qk_norm_rope_fwd_checked")
     rc = load().qk_norm_rope_fwd_checked(qkv.data_ptr(), wq.data_ptr(), wk.data_ptr(),
                                          cos_sin.data_ptr(), positions.data_ptr(), T, Hq, Hkv, D,
                                          rotary_dim, eps, int(max_pos), err_flag.data_ptr(),
@@ -435,16 +464,23 @@ def qk_norm_rope_fwd_checked(qkv, wq, wk, cos_sin, positions, Hq, Hkv, D, rotary
 
 def rope_cos_sin_table(theta: float, max_pos: int, rotary_dim: int,
                        out: torch.Tensor | None = None, *, device=None,
-                       stream=None) -> torch.Tensor:
-    """fp32 [max_pos, rotary_dim] table: cos half then sin half of p * theta^(-2i/r)."""
+                       dtype: torch.dtype | None = None, stream=None) -> torch.Tensor:
+    """[max_pos, rotary_dim] table: cos half then sin half of p * theta^(-2i/r),
+    fp32 (default) or bf16 (dtype=torch.bfloat16, or a bf16 `out`), each entry
+    rounded once from fp64."""
+    if dtype is None:
+        dtype = out.dtype if out is not None else torch.float32
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("rope_cos_sin_table builds fp32 or bf16 tables")
     if out is None:
-        out = torch.empty(max_pos, rotary_dim, dtype=torch.float32,
+        out = torch.empty(max_pos, rotary_dim, dtype=dtype,
                           device=device if device is not None else "cuda")
-    _need(out, "out", torch.float32)
+    _need(out, "out", dtype)
     if out.shape != (max_pos, rotary_dim):
         raise ValueError("out must be [max_pos, rotary_dim]")
-    rc = load().rope_cos_sin_table(float(theta), int(max_pos), int(rotary_dim), out.data_ptr(),
-                                   _stream(stream))
+    L = load()
+    fn = L.rope_cos_sin_table_bf16 if dtype == torch.bfloat16 else L.rope_cos_sin_table
+    rc = fn(float(theta), int(max_pos), int(rotary_dim), out.data_ptr(), _stream(stream))
     _check(rc, "rope_cos_sin_table")
     return out
 

@@ -140,7 +140,7 @@ struct QkArgs {
     uint16_t *qkv;
     const uint16_t *wq;
     const uint16_t *wk;
-    const float *cos_sin;
+    const void *cos_sin;  // fp32 or bf16 [max_pos, R]: the kernels' TB parameter says which
     const int64_t *pos;
     int64_t T;
     int Hq;
@@ -152,8 +152,9 @@ struct QkArgs {
 
 // STYLE 0: neox pairs (i, i + r/2).  STYLE 1: GPT-J pairs (2i, 2i + 1): the
 // lane's rotary slice is then 2A contiguous elements, de-interleaved into the
-// same (first, second) arrays so the arithmetic is shared.
-template <int D, int R, int LPH, int STYLE>
+// same (first, second) arrays so the arithmetic is shared.  TB: the cos/sin
+// table holds bf16 entries (widened exactly to fp32 on load) instead of fp32.
+template <int D, int R, int LPH, int STYLE, bool TB>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
     constexpr int H2 = R / 2;
     constexpr int A = H2 / LPH;
@@ -210,9 +211,15 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
             for (int i = 0; i < (B > 0 ? B : 1); ++i) x3[i] = 0.f;
         }
         float c[A], s[A];
-        const float *cs = a.cos_sin + p * R;
-        load_f32<A>(cs + sub * A, c);
-        load_f32<A>(cs + H2 + sub * A, s);
+        if constexpr (TB) {  // bf16 entries, widened exactly
+            const uint16_t *cs = static_cast<const uint16_t *>(a.cos_sin) + p * R;
+            load_bf<A>(cs + sub * A, c);
+            load_bf<A>(cs + H2 + sub * A, s);
+        } else {
+            const float *cs = static_cast<const float *>(a.cos_sin) + p * R;
+            load_f32<A>(cs + sub * A, c);
+            load_f32<A>(cs + H2 + sub * A, s);
+        }
 
         float ss = 0.f;
 #pragma unroll
@@ -453,7 +460,7 @@ __device__ __forceinline__ void qk_rotate(const uint32_t (&x1)[A2], const uint32
         qk_rotate_slice_gptj<A2, B2, TAIL>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
 }
 
-template <int D, int R, int STYLE>
+template <int D, int R, int STYLE, bool TB>
 __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
     qk_persistent_bulk_kernel(const QkBulkArgs args) {
     constexpr int LPH = 8;
@@ -475,7 +482,7 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
     const int Hq = a.Hq;
     const int H = a.Hq + a.Hkv;
     const uint32_t tok_bytes = static_cast<uint32_t>(H) * D * 2;
-    const uint32_t cs_bytes = R * 4;
+    const uint32_t cs_bytes = R * (TB ? 2 : 4);
     const uint32_t stage_bytes = static_cast<uint32_t>(TPS) * (tok_bytes + cs_bytes);
     const int64_t W = static_cast<int64_t>(a.Hq + 2 * a.Hkv) * D;
     uint8_t *ring = smem;
@@ -557,7 +564,9 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
                 // A rejected position still completes the stage's byte count
                 // (row 0 is copied); its token is flagged and never stored.
                 bulk_copy_g2s_plain(st + static_cast<size_t>(TPS) * tok_bytes + lane * cs_bytes,
-                                    a.cos_sin + (pos_ok ? p : 0) * R, cs_bytes, &full[s]);
+                                    static_cast<const uint8_t *>(a.cos_sin) +
+                                        (pos_ok ? p : 0) * static_cast<int64_t>(cs_bytes),
+                                    cs_bytes, &full[s]);
             }
         }
         if (lane == 0) {
@@ -610,8 +619,7 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
         int rows;
         sched.unit(bid, k, &r0, &rows);
         const uint8_t *st = ring + static_cast<size_t>(s) * stage_bytes;
-        const float *cs_base =
-            reinterpret_cast<const float *>(st + static_cast<size_t>(TPS) * tok_bytes);
+        const uint8_t *cs_base = st + static_cast<size_t>(TPS) * tok_bytes;
         const int heads = rows * H;
         const int quads = (heads + HPW - 1) / HPW;
         for (int q = static_cast<int>((warp + k) % NW); q < quads; q += NW) {
@@ -627,10 +635,18 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
             load_words<A>(xs + off1, x1);
             load_words<A>(xs + off2, x2);
             if constexpr (B > 0) load_words<B>(xs + R + sub * B, x3);
-            const float *cs = cs_base + ts * R;
             float c[A], sn[A];
-            load_f32_smem_lanes<A>(cs + sub * A, c, sub);
-            load_f32_smem_lanes<A>(cs + H2 + sub * A, sn, sub);
+            if constexpr (TB) {
+                // 8 lanes read one 2A-byte run each, one contiguous span: no
+                // bank is shared within a phase, so no reordering is needed.
+                const uint16_t *cs = reinterpret_cast<const uint16_t *>(cs_base) + ts * R;
+                load_bf<A>(cs + sub * A, c);
+                load_bf<A>(cs + H2 + sub * A, sn);
+            } else {
+                const float *cs = reinterpret_cast<const float *>(cs_base) + ts * R;
+                load_f32_smem_lanes<A>(cs + sub * A, c, sub);
+                load_f32_smem_lanes<A>(cs + H2 + sub * A, sn, sub);
+            }
 
             // two independent accumulators: half the dependent FMA chain
             float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
@@ -687,8 +703,16 @@ __global__ void __launch_bounds__(qk_bulk_consumers<D>() + 32, 1)
 
 // ---- table builder ----------------------------------------------------------------
 
-// fp64 angle and trig, rounded once to fp32.
-__global__ void rope_table_kernel(double theta, int64_t max_pos, int r, float *out) {
+// fp64 angle and trig, rounded once to the table's element type (fp32, or
+// bf16 straight from the double: going through fp32 would round twice).
+__device__ __forceinline__ void put_table(float *p, double v) { *p = __double2float_rn(v); }
+__device__ __forceinline__ void put_table(uint16_t *p, double v) {
+    const __nv_bfloat16 b = __double2bfloat16(v);
+    *p = *reinterpret_cast<const uint16_t *>(&b);
+}
+
+template <class OUT>
+__global__ void rope_table_kernel(double theta, int64_t max_pos, int r, OUT *out) {
     pdl_trigger();
     pdl_wait();
     const int h = r / 2;
@@ -701,14 +725,14 @@ __global__ void rope_table_kernel(double theta, int64_t max_pos, int r, float *o
         const double ang = static_cast<double>(p) * f;
         double sv, cv;
         sincos(ang, &sv, &cv);
-        out[p * r + i] = __double2float_rn(cv);
-        out[p * r + h + i] = __double2float_rn(sv);
+        put_table(out + p * r + i, cv);
+        put_table(out + p * r + h + i, sv);
     }
 }
 
 // ---- host side ----------------------------------------------------------------------
 
-template <int D, int R, int LPH, int STYLE>
+template <int D, int R, int LPH, int STYLE, bool TB>
 static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const DeviceInfo &dev) {
     constexpr int HPW = 32 / LPH;
     constexpr int kThreads = 256;
@@ -720,35 +744,35 @@ static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const De
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7fffffffULL) blocks = 0x7fffffffULL;
-    return launch_pdl(qk_norm_rope_kernel<D, R, LPH, STYLE>, dim3(static_cast<unsigned>(blocks)),
+    return launch_pdl(qk_norm_rope_kernel<D, R, LPH, STYLE, TB>, dim3(static_cast<unsigned>(blocks)),
                       dim3(kThreads), 0, st, a);
 }
 
 // Largest lanes-per-head <= the request that tiles both rotary halves and
 // the tail of this (D, rotary_dim); 8 always does.
-template <int D, int R, int STYLE>
+template <int D, int R, int STYLE, bool TB>
 static int launch_qk_lph(const QkArgs &a, int lph, bool persistent, cudaStream_t st,
                          const DeviceInfo &dev) {
     constexpr int H2 = R / 2;
     if constexpr (H2 % 32 == 0 && (D - R) % 32 == 0) {
-        if (lph >= 32) return launch_qk<D, R, 32, STYLE>(a, persistent, st, dev);
+        if (lph >= 32) return launch_qk<D, R, 32, STYLE, TB>(a, persistent, st, dev);
     }
     if constexpr (H2 % 16 == 0 && (D - R) % 16 == 0) {
-        if (lph >= 16) return launch_qk<D, R, 16, STYLE>(a, persistent, st, dev);
+        if (lph >= 16) return launch_qk<D, R, 16, STYLE, TB>(a, persistent, st, dev);
     }
     if constexpr (H2 % 8 == 0 && (D - R) % 8 == 0) {
-        return launch_qk<D, R, 8, STYLE>(a, persistent, st, dev);
+        return launch_qk<D, R, 8, STYLE, TB>(a, persistent, st, dev);
     }
     return RN_ERR_SHAPE;
 }
 
-template <int D, int R, int STYLE>
+template <int D, int R, int STYLE, bool TB>
 static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &dev,
                           uint64_t timeout_ns, int debug_flags) {
     static std::atomic<int> attr_done[kMaxDevices];
     const int H = a.Hq + a.Hkv;
     const int tok_bytes = H * D * 2;
-    const int cs_bytes = R * 4;
+    const int cs_bytes = R * (TB ? 2 : 4);
     // About 32 KiB a stage; 44 KiB when the rotation spans the whole head,
     // whose consumers hold a stage longer (more arithmetic per token): 4
     // tokens a stage instead of 3 at D = 128, measured on GB300.
@@ -771,7 +795,7 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     const int dev_idx = current_device_index();
     if (dev_idx < 0 || dev_idx >= kMaxDevices) return RN_ERR_DEVICE;
     if (!attr_done[dev_idx].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(qk_persistent_bulk_kernel<D, R, STYLE>,
+        if (cudaFuncSetAttribute(qk_persistent_bulk_kernel<D, R, STYLE, TB>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_cap) != cudaSuccess) {
             cudaGetLastError();
@@ -783,7 +807,7 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
     if (grid > a.T) grid = a.T;
     const uint64_t inv_h = ((1ull << 32) + H - 1) / H;
     QkBulkArgs b{a, tps, stages, debug_flags & 1, inv_h, timeout_ns ? timeout_ns : 2000000000ull};
-    return launch_pdl(qk_persistent_bulk_kernel<D, R, STYLE>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl(qk_persistent_bulk_kernel<D, R, STYLE, TB>, dim3(static_cast<unsigned>(grid)),
                       dim3(qk_bulk_consumers<D>() + 32), smem, st, b);
 }
 
@@ -799,7 +823,7 @@ static int auto_qk_schedule(int64_t T) {
     return RN_QK_BULK;
 }
 
-template <int STYLE>
+template <int STYLE, bool TB>
 static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic, int lph,
                      bool persistent, cudaStream_t st, const DeviceInfo &dev,
                      uint64_t timeout_ns, int debug_flags) {
@@ -807,7 +831,7 @@ static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic
         int rc = RN_ERR_SHAPE;
 #define RN_QK_BULK_GO(D_, R_)                                                           \
     if (D == (D_) && r == (R_))                                                         \
-        rc = launch_qk_bulk<D_, R_, STYLE>(a, st, dev, timeout_ns, debug_flags);
+        rc = launch_qk_bulk<D_, R_, STYLE, TB>(a, st, dev, timeout_ns, debug_flags);
         // (64, 16) leaves one element per lane per half: the warp schedules serve it.
         RN_QK_BULK_GO(64, 64) RN_QK_BULK_GO(64, 32)
         RN_QK_BULK_GO(128, 128) RN_QK_BULK_GO(128, 64) RN_QK_BULK_GO(128, 32)
@@ -817,7 +841,7 @@ static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic
         persistent = true;  // a token too wide for the ring: the warp grid serves it
     }
 #define RN_QK_GO(D_, R_)                                                               \
-    if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_, STYLE>(a, lph, persistent, st, dev);
+    if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_, STYLE, TB>(a, lph, persistent, st, dev);
     RN_QK_GO(64, 64) RN_QK_GO(64, 32) RN_QK_GO(64, 16)
     RN_QK_GO(128, 128) RN_QK_GO(128, 64) RN_QK_GO(128, 32)
     RN_QK_GO(256, 256) RN_QK_GO(256, 128) RN_QK_GO(256, 64)
@@ -825,11 +849,12 @@ static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic
     return RN_ERR_SHAPE;
 }
 
+// `cos_sin` holds fp32 entries, or bf16 ones when table_bf16.
 static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
-                       const float *cos_sin, const int64_t *positions, int64_t T, int Hq,
+                       const void *cos_sin, const int64_t *positions, int64_t T, int Hq,
                        int Hkv, int D, int rotary_dim, float eps, int64_t max_pos, int *err,
                        int schedule, uint64_t timeout_ns, int debug_flags, rn_stream_t stream,
-                       int style = RN_ROPE_NEOX) {
+                       int style = RN_ROPE_NEOX, bool table_bf16 = false) {
     if (style != RN_ROPE_NEOX && style != RN_ROPE_GPTJ) return RN_ERR_ARG;
     if (T < 0 || Hq < 0 || Hkv < 0) return RN_ERR_SHAPE;
     if (D != 64 && D != 128 && D != 256) return RN_ERR_SHAPE;
@@ -863,11 +888,16 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
     QkArgs a{reinterpret_cast<uint16_t *>(qkv), wq, wk, cos_sin, positions, T, Hq, Hkv,
              eps, max_pos, err};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (style == RN_ROPE_GPTJ)
-        return qk_launch<1>(a, D, rotary_dim, schedule, automatic, lph, persistent, st, *dev,
-                            timeout_ns, debug_flags);
-    return qk_launch<0>(a, D, rotary_dim, schedule, automatic, lph, persistent, st, *dev,
-                        timeout_ns, debug_flags);
+#define RN_QK_STYLE(S_, TB_)                                                                \
+    return qk_launch<S_, TB_>(a, D, rotary_dim, schedule, automatic, lph, persistent, st, *dev, \
+                              timeout_ns, debug_flags)
+    if (style == RN_ROPE_GPTJ) {
+        if (table_bf16) RN_QK_STYLE(1, true);
+        RN_QK_STYLE(1, false);
+    }
+    if (table_bf16) RN_QK_STYLE(0, true);
+    RN_QK_STYLE(0, false);
+#undef RN_QK_STYLE
 }
 
 int qk_status(unsigned int *out, int clear) {
@@ -928,27 +958,58 @@ int qk_norm_rope_fwd_ex(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
                            rope_style);
 }
 
+int qk_norm_rope_fwd_ex_bf16_table(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
+                                   const rn_bf16 *cos_sin, const int64_t *positions, int64_t T,
+                                   int Hq, int Hkv, int D, int rotary_dim, float eps,
+                                   int rope_style, int64_t max_pos, int *d_err_flag, int schedule,
+                                   uint64_t wait_timeout_ns, int debug_flags, rn_stream_t stream) {
+    if (max_pos < 0) return RN_ERR_SHAPE;
+    if (max_pos > 0 && !d_err_flag && T > 0 && Hq + Hkv > 0) return RN_ERR_NULL;
+    return rn::qk_dispatch(qkv, wq, wk, cos_sin, positions, T, Hq, Hkv, D, rotary_dim, eps,
+                           max_pos, d_err_flag, schedule, wait_timeout_ns, debug_flags, stream,
+                           rope_style, true);
+}
+
 int qk_norm_rope_select_schedule(int64_t T) {
     if (T < 0) return RN_ERR_SHAPE;
     return rn::auto_qk_schedule(T);
 }
 
-int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim, float *cos_sin,
-                       rn_stream_t stream) {
+}  // extern "C"
+
+namespace rn {
+
+template <class OUT>
+static int build_rope_table(double theta, int64_t max_pos, int rotary_dim, OUT *cos_sin,
+                            rn_stream_t stream) {
     if (max_pos < 0 || rotary_dim <= 0 || (rotary_dim & 1) || !(theta > 0.0))
         return RN_ERR_SHAPE;
     if (max_pos == 0) return RN_OK;
     if (!cos_sin) return RN_ERR_NULL;
-    if (!rn::aligned16(cos_sin)) return RN_ERR_ALIGN;
-    const rn::DeviceInfo *dev = rn::current_device_info();
+    if (!aligned16(cos_sin)) return RN_ERR_ALIGN;
+    const DeviceInfo *dev = current_device_info();
     if (!dev) return RN_ERR_DEVICE;
     const int64_t n = max_pos * (rotary_dim / 2);
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = static_cast<int64_t>(dev->sm_count) * 16;
     if (blocks > cap) blocks = cap;
-    return rn::launch_pdl(rn::rope_table_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
-                          reinterpret_cast<cudaStream_t>(stream), theta, max_pos, rotary_dim,
-                          cos_sin);
+    return launch_pdl(rope_table_kernel<OUT>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                      reinterpret_cast<cudaStream_t>(stream), theta, max_pos, rotary_dim, cos_sin);
+}
+
+}  // namespace rn
+
+extern "C" {
+
+int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim, float *cos_sin,
+                       rn_stream_t stream) {
+    return rn::build_rope_table(theta, max_pos, rotary_dim, cos_sin, stream);
+}
+
+int rope_cos_sin_table_bf16(double theta, int64_t max_pos, int rotary_dim, rn_bf16 *cos_sin,
+                            rn_stream_t stream) {
+    return rn::build_rope_table(theta, max_pos, rotary_dim, reinterpret_cast<uint16_t *>(cos_sin),
+                                stream);
 }
 
 }  // extern "C"

@@ -25,6 +25,15 @@ def oracle_table(theta: float, max_pos: int, rotary_dim: int) -> np.ndarray:
     return oracle.rope_cos_sin(theta, max_pos, rotary_dim)
 
 
+def oracle_table_bf16(theta: float, max_pos: int, rotary_dim: int):
+    """The oracle's bf16 table twice: as a CUDA bf16 tensor for the library,
+    and widened (exactly) to fp32 for the oracle's fused Q/K step."""
+    bits = oracle.rope_cos_sin_bf16(theta, max_pos, rotary_dim)
+    dev = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    wide = (bits.astype(np.uint32) << 16).view(np.float32)
+    return dev, wide
+
+
 def padded_empty(shape, dtype, pad: int, fill_bits: int):
     """A CUDA tensor of `shape` carved from a larger buffer whose `pad`
     elements on each side are set to a canary bit pattern."""

@@ -16,7 +16,8 @@ import torch
 import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, qkv_inputs
-from tests.gpu_util import canary_intact, oracle_table, padded_empty, require_gpu
+from tests.gpu_util import (canary_intact, oracle_table, oracle_table_bf16, padded_empty,
+                            require_gpu)
 from tests.parity import assert_parity
 
 pytestmark = pytest.mark.gpu
@@ -32,24 +33,28 @@ def _gpu():
 
 def run_case(T, Hq, Hkv, D, r, *, positions="arange", max_pos=None, theta=1e6, eps=1e-6,
              schedule=binding.RN_QK_AUTO, device_inputs=False, seed=0, debug_flags=0,
-             style=binding.RN_ROPE_NEOX):
+             style=binding.RN_ROPE_NEOX, bf16_table=False):
     max_pos = max_pos or max(T, 1)
     qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions=positions, max_pos=max_pos,
                                   device="cuda" if device_inputs else "cpu", seed=seed)
-    table = oracle_table(theta, max_pos, r)
+    if bf16_table:
+        # the oracle reads the bf16 entries widened to fp32, as the kernels do
+        dev_table, table = oracle_table_bf16(theta, max_pos, r)
+    else:
+        table = oracle_table(theta, max_pos, r)
+        dev_table = torch.from_numpy(table).cuda()
     want = oracle.qk_norm_rope(bf16_bits(qkv), bf16_bits(wq), bf16_bits(wk), table,
                                pos.cpu().numpy(), Hq, Hkv, D, r, eps, style=style)
     pad = 128
     buf, q = padded_empty(tuple(qkv.shape), torch.bfloat16, pad, 0x7FC3)
     q.copy_(qkv)
     if style == binding.RN_ROPE_NEOX:
-        binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(),
-                                 pos.cuda(), Hq, Hkv, D, r, eps, schedule=schedule,
-                                 debug_flags=debug_flags)
+        binding.qk_norm_rope_fwd(q, wq.cuda(), wk.cuda(), dev_table, pos.cuda(), Hq, Hkv, D, r,
+                                 eps, schedule=schedule, debug_flags=debug_flags)
     else:
-        binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(),
-                                    pos.cuda(), Hq, Hkv, D, r, eps, rope_style=style,
-                                    schedule=schedule, debug_flags=debug_flags)
+        binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), dev_table, pos.cuda(), Hq, Hkv, D,
+                                    r, eps, rope_style=style, schedule=schedule,
+                                    debug_flags=debug_flags)
     torch.cuda.synchronize()
     got = bf16_bits(q)
     assert canary_intact(buf, pad, 0x7FC3), "write outside qkv"
@@ -261,3 +266,68 @@ def test_gptj_checked_positions():
     assert np.array_equal(got[[5, 2222]], src[[5, 2222]])
     ok_rows = [t for t in range(T) if t not in (5, 2222)]
     assert_parity(got[ok_rows], want[ok_rows], "gptj checked")
+
+
+# ---------------------------------------------------------------------------
+# bf16 cos/sin table
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("style", [binding.RN_ROPE_NEOX, binding.RN_ROPE_GPTJ])
+@pytest.mark.parametrize("schedule", QK_SCHEDULES)
+@pytest.mark.parametrize("D,r", LAYOUTS)
+def test_bf16_table_layouts_every_schedule(D, r, schedule, style):
+    if schedule == binding.RN_QK_BULK and (D, r) == (64, 16):
+        return  # the ring does not take this layout (warp schedules do)
+    got, want = run_case(7, 4, 2, D, r, positions="uniform", max_pos=211, schedule=schedule,
+                         seed=D + 3 * r + style, style=style, bf16_table=True)
+    assert_parity(got, want, f"bf16 table D={D} r={r} sched={schedule} style={style}")
+
+
+@pytest.mark.parametrize("style", [binding.RN_ROPE_NEOX, binding.RN_ROPE_GPTJ])
+@pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_PERSISTENT,
+                                      binding.RN_QK_BULK])
+@pytest.mark.parametrize("r", [128, 64])
+def test_bf16_table_many_tokens_full_compare(r, schedule, style):
+    # 16384 tokens (4096 for the warp grid), uniform positions over 131072
+    T = 4096 if schedule == binding.RN_QK_PERSISTENT else 16384
+    got, want = run_case(T, 32, 8, 128, r, positions="uniform", max_pos=131072,
+                         device_inputs=True, seed=17 + r, schedule=schedule, style=style,
+                         bf16_table=True)
+    assert_parity(got, want, f"bf16 table T={T} r={r} sched={schedule} style={style}")
+
+
+def test_bf16_table_checked_positions():
+    T, Hq, Hkv, D, r = 3000, 4, 2, 128, 128
+    max_pos = 64
+    qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions="uniform", max_pos=max_pos, seed=31)
+    bad = torch.arange(0, T, 7)
+    pos[bad] = torch.where(bad % 2 == 0, torch.tensor(-1), torch.tensor(max_pos + 5))
+    dev_table, table = oracle_table_bf16(1e6, max_pos, r)
+    good = (pos >= 0) & (pos < max_pos)
+    want = bf16_bits(qkv).copy()
+    ok_rows = good.numpy()
+    want[ok_rows] = oracle.qk_norm_rope(bf16_bits(qkv[good]), bf16_bits(wq), bf16_bits(wk), table,
+                                        pos[good].numpy(), Hq, Hkv, D, r, 1e-6)
+    for schedule in (binding.RN_QK_FOUR_HEADS, binding.RN_QK_BULK):
+        q = qkv.cuda()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), dev_table, pos.cuda(), Hq, Hkv, D, r,
+                                    1e-6, max_pos=max_pos, err_flag=err, schedule=schedule)
+        assert int(err.item()) & binding.RN_STATUS_BAD_POSITION
+        got = bf16_bits(q)
+        assert np.array_equal(got[~ok_rows], bf16_bits(qkv)[~ok_rows]), "rejected tokens touched"
+        assert_parity(got[ok_rows], want[ok_rows], f"bf16 table checked sched={schedule}")
+
+
+@pytest.mark.parametrize("theta,max_pos,r", [(1e6, 131072, 128), (1e6, 131072, 64),
+                                             (10000.0, 4096, 64), (500000.0, 333, 32)])
+def test_bf16_table_builder_matches_oracle(theta, max_pos, r):
+    ref = oracle.rope_cos_sin_bf16(theta, max_pos, r)
+    got = bf16_bits(binding.rope_cos_sin_table(theta, max_pos, r, dtype=torch.bfloat16))
+    # Both sides round the double value once to bf16; pow/sin/cos may differ
+    # in the last double bit, which flips the rounding only for a value within
+    # ~1e-10 of a bf16 midpoint: at most a step, and almost never.
+    from tests.exact import ulp_distance_bf16
+    d = ulp_distance_bf16(got, ref)
+    assert d.max() <= 1
+    assert np.mean(d == 0) > 0.99999
