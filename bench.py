@@ -48,6 +48,7 @@ ADD_SHAPES: list = []   # fused residual add + RMSNorm: only with --only add:MxN
 LN_SHAPES: list = []    # LayerNorm (with bias): only with --only ln:MxN
 L2_SHAPES: list = []    # L2Norm: only with --only l2:MxN
 ROW_DTYPE = "bf16"      # element format of the row norms (--row-dtype f16 for fp16)
+QK_TABLE = "f32"        # element type of the rotary cos/sin table (--qk-table bf16)
 RMS_EPS = 1e-6
 QK_T = 16384
 QK_ROT = (128, 64)
@@ -65,9 +66,10 @@ def rms_bytes(M: int, N: int) -> int:
 
 
 def qk_bytes(T: int, r: int) -> int:
-    """Ideal bytes: read+write every Q/K head (V untouched), one fp32 cos/sin
-    row and one int64 position per token, both weights once."""
-    return T * (2 * (HQ + HKV) * D * 2 + r * 4 + 8) + 2 * D * 2
+    """Ideal bytes: read+write every Q/K head (V untouched), one cos/sin row
+    (fp32, or bf16 with --qk-table bf16) and one int64 position per token,
+    both weights once."""
+    return T * (2 * (HQ + HKV) * D * 2 + r * (2 if QK_TABLE == "bf16" else 4) + 8) + 2 * D * 2
 
 
 def qk_v_bytes(T: int) -> int:
@@ -261,6 +263,10 @@ QK_KERNELS = {1: "qk_norm_rope_kernel", 2: "qk_norm_rope_kernel", 4: "qk_norm_ro
               8: "qk_norm_rope_kernel", 16: "qk_persistent_bulk_kernel"}
 
 
+def table_dtype(torch):
+    return torch.bfloat16 if QK_TABLE == "bf16" else torch.float32
+
+
 def build_inputs(torch, binding, inputs, device):
     """All inputs of one step, resident on the device."""
     dt = torch.float16 if ROW_DTYPE == "f16" else torch.bfloat16
@@ -289,7 +295,7 @@ def build_inputs(torch, binding, inputs, device):
     for j, r in enumerate(QK_ROT):
         qkv, wq, wk, pos = inputs.qkv_inputs(QK_T, HQ, HKV, D, positions="uniform",
                                              max_pos=MAX_POS, device=device, seed=1000 + j)
-        table = binding.rope_cos_sin_table(THETA, MAX_POS, r, device=device)
+        table = binding.rope_cos_sin_table(THETA, MAX_POS, r, device=device, dtype=table_dtype(torch))
         qk.append({"r": r, "qkv": qkv, "wq": wq, "wk": wk, "pos": pos, "table": table})
     return rms, qk
 
@@ -395,7 +401,8 @@ def config_points(torch, binding, inputs, hbm_peak: float) -> dict:
         return pt
 
     def qk_point(T, r, positions, latency):
-        table = binding.rope_cos_sin_table(THETA, MAX_POS, r, device="cuda")
+        table = binding.rope_cos_sin_table(THETA, MAX_POS, r, device="cuda",
+                                           dtype=table_dtype(torch))
         bufs = [inputs.qkv_inputs(T, HQ, HKV, D, positions=positions, max_pos=MAX_POS,
                                   device="cuda", seed=s) for s in (21, 22)]
 
@@ -624,6 +631,7 @@ def run_ours(args) -> int:
         "data": "synthetic (seeded torch generators; see DESIGN.md input recipe)",
         "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step,
                    "launches_per_step": n_launch, "parallelism": f"replicas x{world}",
+                   "qk_cos_sin_table": "bf16" if QK_TABLE == "bf16" else "fp32",
                    "l2": (("inputs larger than L2: each buffer is touched once per step and a "
                            f"step moves {bytes_step / 1e9:.2f} GB, "
                            f"{bytes_step / L2_BYTES:.0f}x the 126 MiB L2")
@@ -784,7 +792,11 @@ def _cpu_sample(frac_den: int):
         qkv, wq, wk, pos = qkv_inputs(t, HQ, HKV, D, positions="uniform", max_pos=MAX_POS,
                                       device="cpu", seed=1000 + j)
         qk.append((bf16_bits(qkv), bf16_bits(wq), bf16_bits(wk), pos.numpy(), r))
-    tables = {r: oracle.rope_cos_sin(THETA, MAX_POS, r) for r in QK_ROT}
+    if QK_TABLE == "bf16":  # the oracle reads bf16 entries widened exactly to fp32
+        tables = {r: (oracle.rope_cos_sin_bf16(THETA, MAX_POS, r).astype(np.uint32) << 16)
+                  .view(np.float32) for r in QK_ROT}
+    else:
+        tables = {r: oracle.rope_cos_sin(THETA, MAX_POS, r) for r in QK_ROT}
     nbytes = sum(rms_bytes(x.shape[0], x.shape[1]) for x, _ in rms) + \
         sum(qk_bytes(q[0].shape[0], q[4]) for q in qk)
     return rms, qk, tables, nbytes, np
@@ -873,7 +885,8 @@ def run_reference(args) -> int:
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": sample},
+            "config": {"workload": WORKLOAD, "sample": sample,
+                       "qk_cos_sin_table": "bf16" if QK_TABLE == "bf16" else "fp32"},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -894,6 +907,8 @@ def main() -> int:
     ap.add_argument("--steady-reps", type=int, default=50,
                     help="back-to-back launches per shape for steady_per_shape (0: skip)")
     ap.add_argument("--only", default="", help="profile a subset, e.g. rms:8192x16384")
+    ap.add_argument("--qk-table", choices=("f32", "bf16"), default="f32",
+                    help="element type of the rotary cos/sin table the QK launches read")
     ap.add_argument("--row-dtype", choices=("bf16", "f16"), default="bf16",
                     help="element format of the row norms in the step (the QK op stays bf16)")
     ap.add_argument("--rms-schedule", type=int, default=0, help="force an RN_SCHED_* value")
@@ -902,8 +917,9 @@ def main() -> int:
     FORCE["rms"], FORCE["qk"] = args.rms_schedule, args.qk_schedule
     if args.only:
         restrict_workload(args.only)
-    global ROW_DTYPE
+    global ROW_DTYPE, QK_TABLE
     ROW_DTYPE = args.row_dtype
+    QK_TABLE = args.qk_table
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3  # never time without at least three warm-up steps
     if args.impl == "reference":
