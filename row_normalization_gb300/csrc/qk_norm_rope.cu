@@ -182,15 +182,11 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
         uint16_t *head = a.qkv + static_cast<int64_t>(t) * W + static_cast<int64_t>(h) * D;
 
         int64_t p = active ? __ldg(a.pos + t) : 0;
-        bool ok = active;
-        if (a.max_pos > 0 && active && (p < 0 || p >= a.max_pos)) {
-            ok = false;
-            if (sub == 0) atomicOr(a.err, RN_STATUS_BAD_POSITION);
-        }
-        if (!ok) p = 0;  // keeps every address in range; nothing is stored
-
+        // The head's loads do not wait for the position: only the cos/sin
+        // row and the store depend on it (a token rejected below is read but
+        // never written).
         float x1[A], x2[A], x3[B > 0 ? B : 1];
-        if (ok) {
+        if (active) {
             if constexpr (STYLE == 0) {
                 load_bf<A>(head + sub * A, x1);
                 load_bf<A>(head + H2 + sub * A, x2);
@@ -210,6 +206,27 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
 #pragma unroll
             for (int i = 0; i < (B > 0 ? B : 1); ++i) x3[i] = 0.f;
         }
+        // the weights do not wait for the reduction either
+        const uint16_t *wp = (h < static_cast<uint32_t>(a.Hq)) ? a.wq : a.wk;
+        float w1[A], w2[A];
+        if constexpr (STYLE == 0) {
+            load_bf<A>(wp + sub * A, w1);
+            load_bf<A>(wp + H2 + sub * A, w2);
+        } else {
+            float wr[2 * A];
+            load_bf<2 * A>(wp + sub * 2 * A, wr);
+#pragma unroll
+            for (int i = 0; i < A; ++i) {
+                w1[i] = wr[2 * i];
+                w2[i] = wr[2 * i + 1];
+            }
+        }
+        bool ok = active;
+        if (a.max_pos > 0 && active && (p < 0 || p >= a.max_pos)) {
+            ok = false;
+            if (sub == 0) atomicOr(a.err, RN_STATUS_BAD_POSITION);
+        }
+        if (!ok) p = 0;  // keeps every address in range; nothing is stored
         float c[A], s[A];
         if constexpr (TB) {  // bf16 entries, widened exactly
             const uint16_t *cs = static_cast<const uint16_t *>(a.cos_sin) + p * R;
@@ -230,21 +247,6 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
         }
         ss = group_sum<LPH>(ss);
         const float rstd = __frsqrt_rn(ss / static_cast<float>(D) + a.eps);
-
-        const uint16_t *wp = (h < static_cast<uint32_t>(a.Hq)) ? a.wq : a.wk;
-        float w1[A], w2[A];
-        if constexpr (STYLE == 0) {
-            load_bf<A>(wp + sub * A, w1);
-            load_bf<A>(wp + H2 + sub * A, w2);
-        } else {
-            float wr[2 * A];
-            load_bf<2 * A>(wp + sub * 2 * A, wr);
-#pragma unroll
-            for (int i = 0; i < A; ++i) {
-                w1[i] = wr[2 * i];
-                w2[i] = wr[2 * i + 1];
-            }
-        }
 
         float o1[A], o2[A];
 #pragma unroll
