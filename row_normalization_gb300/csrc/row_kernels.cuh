@@ -222,6 +222,18 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
                 if (c < cpr) st16(yr + 8 * c, ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
             }
         } else {
+            // With up to 4 chunks a lane the weights' loads go out with the
+            // row's, ahead of the reduction; with 8 the extra registers cost
+            // more occupancy than the early loads gain (2048-wide rows).
+            constexpr bool EARLY_W = VPT <= 4 && !ADD;
+            uint4 wv[EARLY_W ? VPT : 1];
+            if constexpr (EARLY_W) {
+#pragma unroll
+                for (int i = 0; i < VPT; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < cpr) wv[i] = weight16<E>(w, c);
+                }
+            }
             float ss = 0.f;
 #pragma unroll
             for (int i = 0; i < VPT; ++i) ss += sumsq8<E>(v[i]);
@@ -230,7 +242,8 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
-                if (c < cpr) st16(yr + 8 * c, scale8<E>(v[i], weight16<E>(w, c), rstd));
+                if (c < cpr)
+                    st16(yr + 8 * c, scale8<E>(v[i], EARLY_W ? wv[i] : weight16<E>(w, c), rstd));
             }
         }
     }
@@ -323,6 +336,17 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             }
             continue;
         }
+        // The weights' loads go out with the row's, ahead of the reduction
+        // (at 1024 threads, 64 registers a thread, they are streamed at the
+        // end instead).
+        uint4 wv[MAXT < 1024 ? VPT : 1];
+        if constexpr (MAXT < 1024) {
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int c = tid + nt * i;
+                if (c < cpr) wv[i] = weight16<E>(w, c);
+            }
+        }
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) ss += sumsq8<E>(v[i]);
@@ -333,13 +357,6 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
         for (int k = 0; k < nw; ++k) tot += red[par][k];
         const float rstd = row_scale(tot, N, eps, l2);
         if constexpr (MAXT < 1024) {
-            // issue every weight load before the first store
-            uint4 wv[VPT];
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                const int c = tid + nt * i;
-                if (c < cpr) wv[i] = weight16<E>(w, c);
-            }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
