@@ -131,12 +131,25 @@ def test_qk_ex_checks(lib):
     assert lib.qk_norm_rope_fwd_ex(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 1, 16, None, 0, 0, 0, None) == binding.RN_ERR_NULL
 
 
-def test_table_checks(lib):
-    assert lib.rope_cos_sin_table(1e6, 16, 7, P, None) == binding.RN_ERR_SHAPE
-    assert lib.rope_cos_sin_table(-1.0, 16, 8, P, None) == binding.RN_ERR_SHAPE
-    assert lib.rope_cos_sin_table(1e6, 0, 8, P, None) == binding.RN_OK
-    assert lib.rope_cos_sin_table(1e6, 16, 8, None, None) == binding.RN_ERR_NULL
-    assert lib.rope_cos_sin_table(1e6, 16, 8, MISALIGNED, None) == binding.RN_ERR_ALIGN
+def test_qk_ex_bf16_table_checks(lib):
+    f = lib.qk_norm_rope_fwd_ex_bf16_table
+    assert f(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 2, 0, None, 0, 0, 0, None) == binding.RN_ERR_ARG
+    assert f(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 1, -1, None, 0, 0, 0, None) == binding.RN_ERR_SHAPE
+    assert f(P, P, P, P, P, 4, 2, 1, 128, 128, 1e-6, 1, 16, None, 0, 0, 0, None) == binding.RN_ERR_NULL
+    assert f(P, P, P, MISALIGNED, P, 4, 2, 1, 128, 128, 1e-6, 0, 0, None, 0, 0, 0, None) == binding.RN_ERR_ALIGN
+    assert f(P, P, P, None, P, 4, 2, 1, 128, 128, 1e-6, 0, 0, None, 0, 0, 0, None) == binding.RN_ERR_NULL
+    assert f(P, P, P, P, P, 4, 2, 1, 128, 96, 1e-6, 0, 0, None, 0, 0, 0, None) == binding.RN_ERR_SHAPE
+    assert f(P, P, P, P, P, 0, 2, 1, 128, 128, 1e-6, 0, 0, None, 0, 0, 0, None) == binding.RN_OK
+
+
+@pytest.mark.parametrize("fn", ["rope_cos_sin_table", "rope_cos_sin_table_bf16"])
+def test_table_checks(lib, fn):
+    f = getattr(lib, fn)
+    assert f(1e6, 16, 7, P, None) == binding.RN_ERR_SHAPE
+    assert f(-1.0, 16, 8, P, None) == binding.RN_ERR_SHAPE
+    assert f(1e6, 0, 8, P, None) == binding.RN_OK
+    assert f(1e6, 16, 8, None, None) == binding.RN_ERR_NULL
+    assert f(1e6, 16, 8, MISALIGNED, None) == binding.RN_ERR_ALIGN
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
