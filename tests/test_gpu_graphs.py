@@ -15,6 +15,7 @@ import torch
 import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, norm_bias, qkv_inputs, rmsnorm_inputs
+from tests.exact import ulp_distance_bf16
 from tests.gpu_util import oracle_table, require_gpu
 from tests.parity import assert_parity
 
@@ -44,6 +45,8 @@ def test_graph_replay_matches_the_oracle_every_op():
     wq, wk = wq.to(dev), wk.to(dev)
     pos = torch.empty(T, dtype=torch.int64, device=dev)
     table = torch.from_numpy(oracle_table(1e6, 4096, R)).to(dev)
+    qkv2 = torch.empty_like(qkv)
+    table16 = torch.empty(4096, R, dtype=torch.bfloat16, device=dev)  # built inside the graph
 
     def step():
         binding.rmsnorm_fwd(x, w, eps, ys[0])
@@ -52,6 +55,9 @@ def test_graph_replay_matches_the_oracle_every_op():
         binding.l2norm_fwd(x, 1e-12, ys[3])
         binding.rmsnorm_fwd(x16, w16, eps, y16)
         binding.qk_norm_rope_fwd(qkv, wq, wk, table, pos, HQ, HKV, D, R, eps)
+        binding.rope_cos_sin_table(1e6, 4096, R, table16)
+        binding.qk_norm_rope_fwd_ex(qkv2, wq, wk, table16, pos, HQ, HKV, D, R, eps,
+                                    rope_style=binding.RN_ROPE_GPTJ)
 
     def fill(seed):
         xs, _ = rmsnorm_inputs(M, N, outlier_frac=0.01, seed=seed)
@@ -61,6 +67,7 @@ def test_graph_replay_matches_the_oracle_every_op():
         r.copy_(rs)
         x16.copy_(xs.float().to(torch.float16))
         qkv.copy_(q)
+        qkv2.copy_(q)
         pos.copy_(p)
         return xs, rs, q, p
 
@@ -93,3 +100,10 @@ def test_graph_replay_matches_the_oracle_every_op():
         want_q = oracle.qk_norm_rope(bf16_bits(q), bf16_bits(wq), bf16_bits(wk),
                                      oracle_table(1e6, 4096, R), p.numpy(), HQ, HKV, D, R, eps)
         assert_parity(bf16_bits(qkv), want_q, f"graph qk {seed}")
+        # the bf16 table the graph builds, then GPT-J pairs reading it
+        t16 = bf16_bits(table16)
+        assert ulp_distance_bf16(t16, oracle.rope_cos_sin_bf16(1e6, 4096, R)).max() <= 1
+        wide = (t16.astype(np.uint32) << 16).view(np.float32)
+        want_j = oracle.qk_norm_rope(bf16_bits(q), bf16_bits(wq), bf16_bits(wk), wide, p.numpy(),
+                                     HQ, HKV, D, R, eps, style=1)
+        assert_parity(bf16_bits(qkv2), want_j, f"graph qk bf16 table gptj {seed}")
