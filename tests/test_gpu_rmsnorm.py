@@ -182,7 +182,7 @@ def _check_full_size(M, N, eps, outlier_frac, seed=0, n_sample=96):
     got = bf16_bits(y.index_select(0, idx))
     assert_parity(got, want, f"sampled rows M={M} N={N}")
     # 2) every row: within one bf16 step of an fp32 torch restatement (a
-    #    property that holds at any size; the oracle is the judge above)
+    #    property that holds at any size; the sampled rows above are held to the oracle)
     wf = w.float()
     for r0 in range(0, M, 4096):
         xb = x[r0:r0 + 4096].float()
