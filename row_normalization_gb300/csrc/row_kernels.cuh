@@ -966,23 +966,23 @@ static int launch_bulk_inst(const BulkArgs &a, int sm_count, int ctas, size_t sm
 
 // LayerNorm at a generic width: the layout with the most chunks a thread
 // (1, 2, 4 or 8) whose consumers, rounded up to whole warps, cover the row
-// with at most a tenth of their chunks masked, number at least three warps,
-// and leave room for two or three such CTAs on an SM, each with a two-stage
-// ring (at 8 chunks, in the two-CTA build when the one-CTA build's registers
-// leave room for one).  Several independent CTAs a SM keep the per-row chain
-// of LayerNorm (reduce, derive mean and scale, normalise) in flight in
-// parallel; one CTA with more threads on the same row does not (16384 x 5120:
-// 0.65 -> 0.93 of the copy; 6144: 0.75 -> 0.88; 3072: 0.79 -> 0.85).  Leaves
-// `geo` as it is when no layout qualifies (a masked tenth or more, or one CTA
-// an SM).
+// with at most `max_masked_tenths` tenths of their chunk slots masked, number
+// at least three warps, and leave room for two or three such CTAs on an SM,
+// each with a two-stage ring (at 8 chunks, in the two-CTA build when the
+// one-CTA build's registers leave room for one).  Several independent CTAs a
+// SM keep the per-row chain of LayerNorm (reduce, derive mean and scale,
+// normalise) in flight in parallel; one CTA with more threads on the same row
+// does not (16384 x 5120: 0.65 -> 0.93 of the copy; 6144: 0.75 -> 0.88;
+// 3072: 0.79 -> 0.85).  Returns false, `geo` untouched, when none qualifies.
 template <class E>
-static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
+static bool ln_multi_cta_try(int N, int smem_cap, int max_masked_tenths, BulkGeometry *geo) {
     const int cpr = N >> 3;
     for (int v = 8; v >= 1; v >>= 1) {
         const int per = (cpr + v - 1) / v;
-        if (per > 256) return;  // fewer chunks a thread only need more consumers
+        if (per > 256) return false;  // fewer chunks a thread only need more consumers
         const int nt = ((per + 31) / 32) * 32;
-        if (nt < 96 || 10LL * cpr < 9LL * nt * v) continue;
+        // at most max_masked_tenths tenths of the chunk slots masked
+        if (nt < 96 || 10LL * cpr < (10LL - max_masked_tenths) * nt * v) continue;
         const int R = 8 / v;
         if (2ull * R * N * 2 > 200 * 1024) continue;
         const size_t smem = bulk_smem_bytes(2, R, N);
@@ -994,7 +994,7 @@ static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
                     const int f2 = bulk_fit<E, 8, 1, -2, false, true>(nt, smem, smem_cap);
                     if (f2 >= 2) {
                         *geo = {nt, v, R, 2, f2 < 3 ? f2 : 3, true, true};
-                        return;
+                        return true;
                     }
                 }
                 break;
@@ -1004,9 +1004,17 @@ static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
         }
         if (fit >= 2) {
             *geo = {nt, v, R, 2, fit < 3 ? fit : 3, true};
-            return;
+            return true;
         }
     }
+    return false;
+}
+
+template <class E>
+static void ln_multi_cta_layout(int N, int smem_cap, BulkGeometry *geo) {
+    // A tenth of the slots masked at most; failing that, a fifth, which still
+    // beats one CTA an SM (6656: 0.81 -> 0.82, 7168: 0.87 -> 0.88 of the copy).
+    if (!ln_multi_cta_try<E>(N, smem_cap, 1, geo)) ln_multi_cta_try<E>(N, smem_cap, 2, geo);
 }
 
 template <class E, bool ADD, bool LN>
