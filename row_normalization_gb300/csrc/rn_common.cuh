@@ -54,7 +54,8 @@ struct Bf16 {
             "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
             : "+f"(acc) : "r"(u));
         return acc;
-    }    __device__ static __forceinline__ float pair_sum(uint32_t u) {
+    }
+    __device__ static __forceinline__ float pair_sum(uint32_t u) {
         float r;
         asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 t;\n\tmov.b32 {l, h}, %1;\n\t"
             "add.rn.f32.bf16 t, l, 0f80000000;\n\tadd.rn.f32.bf16 %0, h, t;\n\t}"
@@ -96,7 +97,8 @@ struct F16 {
             "fma.rn.f32.f16 %0, l, l, %0;\n\tfma.rn.f32.f16 %0, h, h, %0;\n\t}"
             : "+f"(acc) : "r"(u));
         return acc;
-    }    __device__ static __forceinline__ float pair_sum(uint32_t u) {
+    }
+    __device__ static __forceinline__ float pair_sum(uint32_t u) {
         float r;
         asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 t;\n\tmov.b32 {l, h}, %1;\n\t"
             "add.rn.f32.f16 t, l, 0f80000000;\n\tadd.rn.f32.f16 %0, h, t;\n\t}"
