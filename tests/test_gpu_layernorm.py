@@ -109,7 +109,12 @@ def test_wait_timeout_reports_status_and_context_survives():
     assert binding.device_status(clear=True) == 0
 
 
-@pytest.mark.parametrize("M,N", [(8192, 8192), (32768, 4096), (4096, 16384), (1024, 32768)])
+# Power-of-two widths, and generic ones in each multi-CTA form at sizes where
+# every CTA wraps its ring many times: 3072 (96 x 4, 3 CTAs), 5120 (160 x 4,
+# 2 CTAs), 6656 (128 x 8 with a fifth of the slots masked), 12288 (the
+# two-CTA build at 8 chunks).
+@pytest.mark.parametrize("M,N", [(8192, 8192), (32768, 4096), (4096, 16384), (1024, 32768),
+                                 (32768, 3072), (16384, 5120), (16384, 6656), (8192, 12288)])
 def test_full_size_sampled_rows(M, N):
     x, w = rmsnorm_inputs(M, N, outlier_frac=0.01, device="cuda", seed=9)
     b = norm_bias(N, device="cuda", seed=10)
