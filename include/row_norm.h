@@ -123,7 +123,8 @@ int rmsnorm_fwd(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M,
 /* Schedules that rmsnorm_fwd_sched can force (for tests and measurement). */
 enum {
     RN_SCHED_AUTO = 0,
-    RN_SCHED_WARP_ROW = 1,    /* one warp per row, row in registers (N <= 2048)  */
+    RN_SCHED_WARP_ROW = 1,    /* one warp per row, row in registers (N <= 2048;
+                                 RMSNorm and L2Norm up to 4096)                    */
     RN_SCHED_CTA_ROW = 2,     /* one CTA per row, row in registers               */
     RN_SCHED_PERSIST_BULK = 3 /* persistent CTAs, bulk-copy shared-memory ring
                                  (N a power of two, 1024 <= N <= 32768)          */

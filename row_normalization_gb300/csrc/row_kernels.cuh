@@ -773,6 +773,13 @@ static int launch_warp_rows(const RowJob &j, cudaStream_t st, const DeviceInfo &
     if (cpr <= 64) RN_WARP(2);
     if (cpr <= 128) RN_WARP(4);
     if (cpr <= 256) RN_WARP(8);
+    if constexpr (!ADD && !LN) {
+        // RMSNorm and L2Norm rows up to 4096 wide: 12 or 16 chunks a lane
+        // (120 registers, no spills; two CTAs of 8 warps an SM, 8 KiB of
+        // loads in flight a warp).  The fused forms would spill.
+        if (cpr <= 384) RN_WARP(12);
+        if (cpr <= 512) RN_WARP(16);
+    }
 #undef RN_WARP
     return RN_ERR_SHAPE;
 }
@@ -1095,6 +1102,12 @@ static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &
     // 4096-wide generic rows also stays on one CTA per row, which keeps twice
     // the loads in flight and measured ahead (0.94-0.97 against 0.89-0.94).
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
+    // RMSNorm / L2Norm rows up to 4096 wide over many rows (128 a SM and
+    // more): one warp per row, loads straight into registers, measured ahead
+    // of the ring (32768 x 4096: 0.95 -> 0.97, 32768 x 3584: 0.88 -> 0.96,
+    // 131072 x 4096: 0.98 -> 1.02 of the copy); with fewer rows the ring's
+    // deeper prefetch wins.
+    if (!add && !ln && N <= 4096 && M >= 128LL * dev.sm_count) return RN_SCHED_WARP_ROW;
     if (bulk_geometry(M, N, add, ln, &geo) && M >= 6LL * dev.sm_count &&
         !(add && geo.generic && N < 4096))
         return RN_SCHED_PERSIST_BULK;

@@ -34,7 +34,7 @@ def _gpu():
 
 def eligible(op: str, schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
-        return N <= 2048
+        return N <= (4096 if op in ("rms", "l2") else 2048)
     if schedule == binding.RN_SCHED_PERSIST_BULK:
         return bulk_eligible(N, MODE[op])
     return True

@@ -23,7 +23,7 @@ SCHEDULES = [binding.RN_SCHED_AUTO, binding.RN_SCHED_WARP_ROW, binding.RN_SCHED_
 
 def eligible(schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
-        return N <= 2048
+        return N <= 4096  # RMSNorm and L2Norm take one warp per row up to 4096 wide
     if schedule == binding.RN_SCHED_PERSIST_BULK:
         return bulk_eligible(N, "rms")
     return True

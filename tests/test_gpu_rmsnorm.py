@@ -27,7 +27,7 @@ SCHEDULES = [binding.RN_SCHED_AUTO, binding.RN_SCHED_WARP_ROW, binding.RN_SCHED_
 
 def eligible(schedule: int, N: int) -> bool:
     if schedule == binding.RN_SCHED_WARP_ROW:
-        return N <= 2048
+        return N <= 4096  # RMSNorm and L2Norm take one warp per row up to 4096 wide
     if schedule == binding.RN_SCHED_PERSIST_BULK:
         return bulk_eligible(N, "rms")
     return True
@@ -40,7 +40,7 @@ def _gpu():
 
 SMALL_SHAPES = [(1, 8), (3, 8), (7, 64), (5, 1000), (33, 2048), (3, 4104), (130, 1024),
                 (300, 4096), (17, 8192), (9, 16384), (5, 32768), (2, 65536), (1000, 512),
-                (157, 3072), (611, 2048)]
+                (157, 3072), (611, 2048), (45, 2056), (61, 2560), (29, 3584)]
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
@@ -202,6 +202,14 @@ def test_latency_config_full():
 @pytest.mark.parametrize("M", [4096, 8192, 16384, 32768])
 @pytest.mark.parametrize("N", [4096, 8192, 16384])
 def test_sweep_full_size(M, N):
+    _check_full_size(M, N, 1e-6, 0.01)
+
+
+@pytest.mark.parametrize("M,N", [(24576, 3072), (20480, 3584), (32768, 2560), (131072, 4096)])
+def test_many_rows_up_to_4096_wide_take_one_warp_a_row(M, N):
+    # 128 rows an SM and more, 2049..4096 wide: one warp per row, 12 or 16
+    # chunks a lane (masked past the row end), chosen automatically
+    assert binding.rmsnorm_select_schedule(M, N) == binding.RN_SCHED_WARP_ROW
     _check_full_size(M, N, 1e-6, 0.01)
 
 
