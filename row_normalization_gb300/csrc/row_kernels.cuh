@@ -1104,8 +1104,8 @@ static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
     // RMSNorm / L2Norm rows up to 4096 wide over many rows (128 a SM and
     // more): one warp per row, loads straight into registers, measured ahead
-    // of the ring (32768 x 4096: 0.95 -> 0.97, 32768 x 3584: 0.88 -> 0.96,
-    // 131072 x 4096: 0.98 -> 1.02 of the copy); with fewer rows the ring's
+    // of the ring (32768 x 4096: 0.94 -> 0.97, 32768 x 3584: 0.89 -> 0.97,
+    // 65536 x 4096: 0.97 -> 1.01 of the copy); with fewer rows the ring's
     // deeper prefetch wins.
     if (!add && !ln && N <= 4096 && M >= 128LL * dev.sm_count) return RN_SCHED_WARP_ROW;
     if (bulk_geometry(M, N, add, ln, &geo) && M >= 6LL * dev.sm_count &&
