@@ -22,6 +22,14 @@ MUTANTS = {
     "eps_on_sum": ("double ms = ss / (double)N;\n        double rs = 1.0 / sqrt(ms + deps);",
                    "double ms = ss / (double)N;\n        double rs = 1.0 / sqrt((ss + deps) / (double)N);"),
     "eps_outside_sqrt": ("double rs = 1.0 / sqrt(ms + deps);", "double rs = 1.0 / (sqrt(ms) + deps);"),
+    "rstd_eps_outside_sqrt": ("rstd[r] = 1.0 / sqrt(ss / (double)N + (double)eps);",
+                              "rstd[r] = 1.0 / (sqrt(ss / (double)N) + (double)eps);"),
+    "rstd_eps_on_sum": ("rstd[r] = 1.0 / sqrt(ss / (double)N + (double)eps);",
+                        "rstd[r] = 1.0 / sqrt((ss + (double)eps) / (double)N);"),
+    "rstd_eps_dropped": ("rstd[r] = 1.0 / sqrt(ss / (double)N + (double)eps);",
+                         "rstd[r] = 1.0 / sqrt(ss / (double)N);"),
+    "rstd_mean_divisor_n_minus_1": ("rstd[r] = 1.0 / sqrt(ss / (double)N + (double)eps);",
+                                    "rstd[r] = 1.0 / sqrt(ss / (double)(N > 1 ? N - 1 : 1) + (double)eps);"),
     "no_weight": ("yr[j] = narrow(v * rs * g, f16);", "yr[j] = narrow(v * rs + 0.0 * g, f16);"),
     "round_via_float": ("double n = nearbyint(v / q);", "double n = nearbyint((double)(float)v / q);"),
     "ties_away": ("double n = nearbyint(v / q);", "double n = round(v / q);"),

@@ -173,6 +173,31 @@ def test_rmsnorm_unit_rms_invariant():
     np.testing.assert_allclose((y * y).sum(axis=1), 300.0, rtol=2**-7)
 
 
+@pytest.mark.parametrize("eps", [1e-6, 1e-5, 0.25])
+def test_rms_rstd_against_exact_decimal(eps):
+    # The row statistic alone, with eps > 0: rstd = 1/sqrt(sum(x^2)/N + eps)
+    # against 60-digit decimals on exact rationals (x and eps as the binary
+    # values the oracle receives).  Rows of three scales, including values
+    # near 1e-3 where x^2 ~ eps and eps's placement (inside the root, on the
+    # mean, not on the sum) moves rstd by far more than double rounding.
+    rng = np.random.default_rng(31)
+    epsq = f32_to_fraction(eps)
+    for N, scale in [(1, 1.0), (7, 1e-3), (64, 1e-3), (300, 1.0), (129, 30.0)]:
+        x = rand_bf16(rng, (3, N), scale=scale)
+        got = oracle.rms_rstd(x, eps)
+        for r in range(3):
+            ms = sum(bits_to_fraction(v) ** 2 for v in x[r]) / N
+            want = Decimal(1) / dsqrt(ms + epsq)
+            assert abs(Decimal(float(got[r])) - want) <= want * Decimal("1e-14"), (N, r)
+    # constant row c: rstd = 1/sqrt(c^2 + eps) whatever N is
+    cb = bf([0.0009994507])[0]
+    cq = bits_to_fraction(cb)
+    for N in (1, 5, 4096):
+        got = oracle.rms_rstd(np.full((1, N), cb, dtype=np.uint16), eps)[0]
+        want = Decimal(1) / dsqrt(cq * cq + epsq)
+        assert abs(Decimal(float(got)) - want) <= want * Decimal("1e-14"), N
+
+
 def test_rmsnorm_power_of_two_scale_is_exact():
     # eps = 0: scaling a row by 2^k scales mean(x^2) by 4^k and rstd by 2^-k,
     # all exact in binary arithmetic, so the outputs are bit-identical.
