@@ -78,59 +78,97 @@ __device__ __forceinline__ uint4 add8(uint4 a, uint4 b) {
     return o;
 }
 
-// LayerNorm pieces: sum of 8, sum of squared deviations from `mean`, and
-// y = (x - mean) * rstd * w (+ b) rounded once.  The widening of x is folded
-// into mixed-precision adds and subtracts (pair_sum, sub2), which round
-// exactly as widen-then-add does.
+// LayerNorm pieces: sum of 8, the sum of deviations from `m` with the sum of
+// their squares, and y = ((x - m) [+ nc]) * rstd * w (+ b) rounded once.  The
+// widening of x is folded into mixed-precision adds and subtracts (pair_sum,
+// sub2), which round exactly as widen-then-add does.
 template <class E>
 __device__ __forceinline__ float sum8(uint4 v) {
     return (E::pair_sum(v.x) + E::pair_sum(v.y)) + (E::pair_sum(v.z) + E::pair_sum(v.w));
 }
 
+// Adds the deviations x_k - m of 8 packed elements to `sd` and their squares
+// to `sq` (fp32 pairs; each pair is consumed at once, so few registers).
 template <class E>
-__device__ __forceinline__ float sqdev8(uint4 v, float m) {
-    const float2 p = E::sub2(v.x, m), q = E::sub2(v.y, m), r = E::sub2(v.z, m), t = E::sub2(v.w, m);
-    const float2 a = __ffma2_rn(r, r, __fmul2_rn(p, p));
-    const float2 b = __ffma2_rn(t, t, __fmul2_rn(q, q));
-    const float2 s2 = __fadd2_rn(a, b);
-    return s2.x + s2.y;
+__device__ __forceinline__ void dev8(uint4 v, float m, float2 &sd, float2 &sq) {
+    float2 d = E::sub2(v.x, m);
+    sd = __fadd2_rn(sd, d);
+    sq = __ffma2_rn(d, d, sq);
+    d = E::sub2(v.y, m);
+    sd = __fadd2_rn(sd, d);
+    sq = __ffma2_rn(d, d, sq);
+    d = E::sub2(v.z, m);
+    sd = __fadd2_rn(sd, d);
+    sq = __ffma2_rn(d, d, sq);
+    d = E::sub2(v.w, m);
+    sd = __fadd2_rn(sd, d);
+    sq = __ffma2_rn(d, d, sq);
 }
 
-// Same, on fp32 pairs (Blackwell FADD2/FMUL2/FFMA2): per pair one subtract,
-// one multiply by rstd, one fused multiply-add with (w, b).
+// Centring of a row whose mean is large against its spread.  The first
+// reduction's fp32 mean m is off by up to |mean| * 2^-24 plus its sum's
+// rounding, and that error would move every x - m by the same amount.  A
+// second reduction over the deviations d = x - m (exact, or within 2^-24 of
+// |d|) gives the correction c = sum(d) / N, which is small against the
+// spread, and the variance sum(d^2) / N - c^2 without cancellation.  The
+// output then takes (x - m) * rstd - c * rstd as one fused multiply-add in
+// place of the product (x - m) * rstd, leaving an error of order 2^-24 of
+// |x - mean| * rstd instead of |mean| * rstd.  Rows centred on the first
+// reduction's mean pass ncr = +0, which gives the plain product's bits.
+struct Centring {
+    float rstd;  // 1 / sqrt(var + eps)
+    float ncr;   // -c * rstd
+};
+
+__device__ __forceinline__ Centring centre(float sum_d, float sum_d2, int N, float eps) {
+    const float c = sum_d / static_cast<float>(N);
+    const float var = fmaxf(sum_d2 / static_cast<float>(N) - c * c, 0.f);
+    const float rstd = __frsqrt_rn(var + eps);
+    return {rstd, -c * rstd};
+}
+
+// Same, on fp32 pairs (Blackwell FFMA2): per pair one subtract, one fused
+// multiply-add by rstd (with the centring correction), one fused
+// multiply-add with (w, b).
 template <class E>
-__device__ __forceinline__ uint32_t ln2w(uint32_t x, uint32_t w, uint32_t b, float m, float2 r) {
-    const float2 d = __fmul2_rn(E::sub2(x, m), r);
+__device__ __forceinline__ uint32_t ln2w(uint32_t x, uint32_t w, uint32_t b, float m, float2 r,
+                                         float2 ncr) {
+    const float2 d = __ffma2_rn(E::sub2(x, m), r, ncr);
     const float2 y = __ffma2_rn(d, make_float2(E::lo(w), E::hi(w)), make_float2(E::lo(b), E::hi(b)));
     return E::pack(y.x, y.y);
 }
 
 template <class E>
-__device__ __forceinline__ uint4 ln8(uint4 xv, uint4 wv, uint4 bv, float m, float rstd) {
+__device__ __forceinline__ uint4 ln8(uint4 xv, uint4 wv, uint4 bv, float m, float rstd,
+                                     float ncr) {
     const float2 r = make_float2(rstd, rstd);
+    const float2 c = make_float2(ncr, ncr);
     uint4 o;
-    o.x = ln2w<E>(xv.x, wv.x, bv.x, m, r);
-    o.y = ln2w<E>(xv.y, wv.y, bv.y, m, r);
-    o.z = ln2w<E>(xv.z, wv.z, bv.z, m, r);
-    o.w = ln2w<E>(xv.w, wv.w, bv.w, m, r);
+    o.x = ln2w<E>(xv.x, wv.x, bv.x, m, r, c);
+    o.y = ln2w<E>(xv.y, wv.y, bv.y, m, r, c);
+    o.z = ln2w<E>(xv.z, wv.z, bv.z, m, r, c);
+    o.w = ln2w<E>(xv.w, wv.w, bv.w, m, r, c);
     return o;
 }
 
 // ln8 with the weights already widened to fp32 pairs (w[0..3]).
 template <class E>
-__device__ __forceinline__ uint32_t ln2f(uint32_t x, float2 w, uint32_t b, float m, float2 r) {
-    const float2 y = __ffma2_rn(__fmul2_rn(E::sub2(x, m), r), w, make_float2(E::lo(b), E::hi(b)));
+__device__ __forceinline__ uint32_t ln2f(uint32_t x, float2 w, uint32_t b, float m, float2 r,
+                                         float2 ncr) {
+    const float2 y = __ffma2_rn(__ffma2_rn(E::sub2(x, m), r, ncr), w, make_float2(E::lo(b), E::hi(b)));
     return E::pack(y.x, y.y);
 }
 
 template <class E>
-__device__ __forceinline__ uint4 ln8w(uint4 xv, const float2 *w, uint4 bv, float m, float rstd) {
+__device__ __forceinline__ uint4 ln8w(uint4 xv, const float2 *w, uint4 bv, float m, float rstd,
+                                      float ncr) {
     const float2 r = make_float2(rstd, rstd);
+    const float2 c = make_float2(ncr, ncr);
     uint4 o;
-    o.x = ln2f<E>(xv.x, w[0], bv.x, m, r);
-    o.y = ln2f<E>(xv.y, w[1], bv.y, m, r);
-    o.z = ln2f<E>(xv.z, w[2], bv.z, m, r);
-    o.w = ln2f<E>(xv.w, w[3], bv.w, m, r);
+    o.x = ln2f<E>(xv.x, w[0], bv.x, m, r, c);
+    o.y = ln2f<E>(xv.y, w[1], bv.y, m, r, c);
+    o.z = ln2f<E>(xv.z, w[2], bv.z, m, r, c);
+    o.w = ln2f<E>(xv.w, w[3], bv.w, m, r, c);
     return o;
 }
 
@@ -206,20 +244,20 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
             }
             const float mean = warp_sum(s1) / static_cast<float>(N);
             const float var = warp_sum(q1) / static_cast<float>(N) - mean * mean;
-            float rstd;
-            if (var > 0.f && mean * mean <= 4.f * var) {
-                rstd = __frsqrt_rn(var + eps);
-            } else {
-                float s2 = 0.f;
+            Centring ce{__frsqrt_rn(var + eps), 0.f};
+            if (!(var > 0.f && mean * mean <= 4.f * var)) {
+                float2 sd = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
-                    if (lane + 32 * i < cpr) s2 += sqdev8<E>(v[i], mean);
-                rstd = row_rstd(warp_sum(s2), N, eps);
+                    if (lane + 32 * i < cpr) dev8<E>(v[i], mean, sd, sq);
+                ce = centre(warp_sum(sd.x + sd.y), warp_sum(sq.x + sq.y), N, eps);
             }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = lane + 32 * i;
-                if (c < cpr) st16(yr + 8 * c, ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
+                if (c < cpr)
+                    st16(yr + 8 * c,
+                         ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, ce.rstd, ce.ncr));
             }
         } else {
             // With up to 4 chunks a lane the weights' loads go out with the
@@ -262,6 +300,7 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
     __shared__ float red[2][32];
     __shared__ float red2[2][32];  // LayerNorm's sums of squares
     __shared__ float red3[2][32];  // LayerNorm's centred squares (large-mean rows)
+    __shared__ float red4[2][32];  // and their deviations
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x;
@@ -313,26 +352,31 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             }
             const float mean = t1 / static_cast<float>(N);
             const float var = u1 / static_cast<float>(N) - mean * mean;
-            float rstd;
-            if (var > 0.f && mean * mean <= 4.f * var) {
-                rstd = __frsqrt_rn(var + eps);
-            } else {
-                float s2 = 0.f;
+            Centring ce{__frsqrt_rn(var + eps), 0.f};
+            if (!(var > 0.f && mean * mean <= 4.f * var)) {
+                float2 sd = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
-                    if (tid + nt * i < cpr) s2 += sqdev8<E>(v[i], mean);
-                s2 = warp_sum(s2);
-                if ((tid & 31) == 0) red3[par][tid >> 5] = s2;
+                    if (tid + nt * i < cpr) dev8<E>(v[i], mean, sd, sq);
+                const float2 dv = make_float2(warp_sum(sd.x + sd.y), warp_sum(sq.x + sq.y));
+                if ((tid & 31) == 0) {
+                    red3[par][tid >> 5] = dv.y;
+                    red4[par][tid >> 5] = dv.x;
+                }
                 __syncthreads();
-                float t2 = 0.f;
-                for (int k = 0; k < nw; ++k) t2 += red3[par][k];
-                rstd = row_rstd(t2, N, eps);
+                float t2 = 0.f, d2 = 0.f;
+                for (int k = 0; k < nw; ++k) {
+                    t2 += red3[par][k];
+                    d2 += red4[par][k];
+                }
+                ce = centre(d2, t2, N, eps);
             }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int c = tid + nt * i;
                 if (c < cpr)
-                    st16(yr + 8 * c, ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, rstd));
+                    st16(yr + 8 * c,
+                         ln8<E>(v[i], ld_ro16(w + 8 * c), bias16(b, c), mean, ce.rstd, ce.ncr));
             }
             continue;
         }
@@ -400,13 +444,16 @@ constexpr int kRedStride = 33;
 
 // Shared memory: [stages x (R rows of x [+ R rows of r])][full mbarriers]
 //                [empty mbarriers][partial sums 6 x R x 33 floats][flags: 4 ints]
-// (three double-buffered sets of partial sums: LayerNorm reduces up to three
-// quantities a row)
+// (three double-buffered sets of partial sums; LayerNorm reduces up to four
+// quantities a row and has four sets, 8 x R x 33 floats)
 // `nin` is the number of row inputs streamed through the ring (1, or 2 with
 // the fused residual add).
-__host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1) {
+constexpr int bulk_red_sets(bool ln) { return ln ? 8 : 6; }
+
+__host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1,
+                                                     bool ln = false) {
     return static_cast<size_t>(stages) * nin * R * N * 2 + static_cast<size_t>(stages) * 16 +
-           static_cast<size_t>(6) * R * kRedStride * 4 + 16;
+           static_cast<size_t>(bulk_red_sets(ln)) * R * kRedStride * 4 + 16;
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
@@ -450,7 +497,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
     // flags[0], flags[1]: "consumers give up" for even / odd units (decided
     // before a named barrier, read after it); flags[2]: "someone gave up",
     // polled inside waits so nobody waits out a full timeout needlessly.
-    volatile int *flags = reinterpret_cast<volatile int *>(red + 6 * R * kRedStride);
+    volatile int *flags = reinterpret_cast<volatile int *>(red + bulk_red_sets(LN) * R * kRedStride);
 
     const int nt = GENERIC ? static_cast<int>(blockDim.x) - 32 : NT;
     const int NW = nt / 32;
@@ -635,6 +682,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
             float *rbs = red + (k & 1) * R * kRedStride;        // sums
             float *rbq = red + (2 + (k & 1)) * R * kRedStride;  // sums of squares
             float *rbc = red + (4 + (k & 1)) * R * kRedStride;  // centred squares
+            float *rbd = red + (6 + (k & 1)) * R * kRedStride;  // and deviations
             if (lane == 0) {
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr) {
@@ -645,7 +693,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
             named_bar_sync(1, nt);
             if (flags[k & 1]) break;  // same decision in every consumer warp
             // lane rr finishes row rr's statistics once; shuffles hand them out
-            float my_mean = 0.f, my_rstd = 0.f;
+            float my_mean = 0.f, my_rstd = 0.f, my_ncr = 0.f;
             bool my_exact = false;
             if (lane < R) {
                 float t = 0.f, u = 0.f;
@@ -664,34 +712,41 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
             if (__any_sync(0xffffffffu, my_exact)) {
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr) {
-                    float acc = 0.f;
+                    float2 sd = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
-                        if (live(tid, j)) acc += sqdev8<E>(xv[rr][j], mean[rr]);
-                    s1[rr] = warp_sum(acc);
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int rr = 0; rr < R; ++rr) rbc[rr * kRedStride + warp] = s1[rr];
+                        if (live(tid, j)) dev8<E>(xv[rr][j], mean[rr], sd, sq);
+                    const float dsum = warp_sum(sd.x + sd.y);
+                    const float qsum = warp_sum(sq.x + sq.y);
+                    if (lane == 0) {
+                        rbd[rr * kRedStride + warp] = dsum;
+                        rbc[rr * kRedStride + warp] = qsum;
+                    }
                 }
                 named_bar_sync(1, nt);
                 if (lane < R) {
-                    float t = 0.f;
-                    for (int q = 0; q < NW; ++q) t += rbc[lane * kRedStride + q];
-                    my_rstd = row_rstd(t, N, a.eps);
+                    float t = 0.f, u = 0.f;
+                    for (int q = 0; q < NW; ++q) {
+                        t += rbc[lane * kRedStride + q];
+                        u += rbd[lane * kRedStride + q];
+                    }
+                    const Centring ce = centre(u, t, N, a.eps);
+                    my_rstd = ce.rstd;
+                    my_ncr = ce.ncr;
                 }
             }
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
                 const float rstd = __shfl_sync(0xffffffffu, my_rstd, rr);
+                const float ncr = __shfl_sync(0xffffffffu, my_ncr, rr);
                 if (rr < rows) {
                     uint16_t *yr = a.y + (r0 + rr) * N;
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
                         if (live(tid, j))
                             st16(yr + 8 * (tid + j * nt),
-                                 WIDE_W ? ln8w<E>(xv[rr][j], &wf[4 * j], bv[j], mean[rr], rstd)
-                                        : ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd));
+                                 WIDE_W ? ln8w<E>(xv[rr][j], &wf[4 * j], bv[j], mean[rr], rstd, ncr)
+                                        : ln8<E>(xv[rr][j], wv[j], bv[j], mean[rr], rstd, ncr));
                 }
             }
         } else {
@@ -993,7 +1048,7 @@ static bool ln_multi_cta_try(int N, int smem_cap, int max_masked_tenths, BulkGeo
         if (nt < 96 || 10LL * cpr < (10LL - max_masked_tenths) * nt * v) continue;
         const int R = 8 / v;
         if (2ull * R * N * 2 > 200 * 1024) continue;
-        const size_t smem = bulk_smem_bytes(2, R, N);
+        const size_t smem = bulk_smem_bytes(2, R, N, 1, true);
         int fit = -1;
         switch (v) {
             case 8:
@@ -1037,7 +1092,7 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
         if (geo.generic && (debug_flags & 0x1FF0) == 0) ln_multi_cta_layout<E>(N, smem_cap, &geo);
     }
     const size_t stage_cost = static_cast<size_t>(NIN) * geo.R * N * 2 + 16;
-    int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N, NIN)) / stage_cost);
+    int max_stages = static_cast<int>((smem_cap - bulk_smem_bytes(0, geo.R, N, NIN, LN)) / stage_cost);
     if (max_stages > 16) max_stages = 16;
     int stages = geo.stages;
     const int forced_stages = (debug_flags >> 8) & 0x1F;
@@ -1049,7 +1104,7 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     while (ctas_per_sm > 1 && max_stages / ctas_per_sm < 2) --ctas_per_sm;
     if (stages * ctas_per_sm > max_stages) stages = max_stages / ctas_per_sm;
     if (stages < 2) return RN_ERR_SHAPE;
-    const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN);
+    const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN, LN);
     BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.l2, j.M, N, j.eps, stages, debug_flags & 1,
                timeout_ns ? timeout_ns : 2000000000ull};
     const int sm = dev.sm_count, c = ctas_per_sm;

@@ -16,6 +16,7 @@ import torch
 import oracle
 from row_normalization_gb300 import binding
 from row_normalization_gb300.inputs import bf16_bits, norm_bias, rmsnorm_inputs
+from tests.full_compare import assert_full_parity
 from tests.gpu_util import bulk_eligible, canary_intact, padded_empty, require_gpu
 from tests.parity import assert_parity, parity_report
 
@@ -124,19 +125,24 @@ def test_non_power_of_two_widths_on_the_ring(op, N):
 
 @pytest.mark.parametrize("op", ["rms", "add", "ln"])
 @pytest.mark.parametrize("M,N", [(8192, 8192), (32768, 4096), (4096, 16384), (1024, 32768)])
-def test_full_size_sampled_rows(op, M, N):
+def test_full_size_every_element(op, M, N):
     x, r, w, b = make(op, M, N, seed=7, device="cuda")
     h, y = run(op, x, r, w, b, EPS[op])
     torch.cuda.synchronize()
-    rng = np.random.default_rng(M + N)
-    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, size=96, replace=False)]))
-    idx = torch.from_numpy(rows).cuda()
-    sel = lambda t: None if t is None else t.index_select(0, idx)  # noqa: E731
-    h_want, y_want = want(op, sel(x), sel(r), w, b, EPS[op])
-    if op == "add":
-        assert np.array_equal(bf16_bits(sel(h)), h_want)
-        assert torch.equal(h.view(torch.int16), (x + r).view(torch.int16))
-    assert_parity(bf16_bits(sel(y)), y_want, f"f16 {op} sampled M={M} N={N}", fmt="f16")
+    xb, wb = bf16_bits(x), bf16_bits(w)
+    rb = None if r is None else bf16_bits(r)
+    bb = None if b is None else bf16_bits(b)
+    eps = EPS[op]
+
+    def rows(a, e):
+        if op == "rms":
+            return None, oracle.rmsnorm(xb[a:e], wb, eps, f16=True)
+        if op == "add":
+            return oracle.add_rmsnorm(xb[a:e], rb[a:e], wb, eps, f16=True)
+        return None, oracle.layernorm(xb[a:e], wb, bb, eps, f16=True)
+
+    assert_full_parity(bf16_bits(y), rows, f"f16 {op} full size M={M} N={N}", fmt="f16",
+                       got_h=None if h is None else bf16_bits(h))
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES[1:])

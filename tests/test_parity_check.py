@@ -84,3 +84,34 @@ def test_midpoint_mode_accepts_ties_and_rejects_other_one_step_errors():
     # fp16: 1 + 2^-11 is a midpoint
     assert near_midpoint(np.array([1 + 2.0**-11]), fmt="f16").tolist() == [True]
     assert near_midpoint(np.array([1 + 2.0**-12]), fmt="f16").tolist() == [False]
+
+
+def test_full_size_checker_adds_up_chunks_and_rejects_planted_errors(monkeypatch):
+    # The chunked whole-tensor check (tests/full_compare.py) on an oracle
+    # output: identical passes; a two-step element in a late chunk, a one-step
+    # fraction above 0.1% spread over chunk boundaries, or one differing h
+    # element fails, with the element's flat index reported.
+    import oracle
+    from tests import full_compare
+    monkeypatch.setattr(full_compare, "CHUNK_ELEMS", 3 * 64)   # 3 rows a chunk
+    rng = np.random.default_rng(5)
+    x = bits(rng.standard_normal((40, 64)), "bf16")
+    w = bits(1 + 0.1 * rng.standard_normal(64), "bf16")
+    y = oracle.rmsnorm(x, w, 1e-6)
+    rows = lambda a, b: (None, oracle.rmsnorm(x[a:b], w, 1e-6))  # noqa: E731
+    rep = full_compare.assert_full_parity(y.copy(), rows, "same")
+    assert rep["n"] == y.size and rep["bad"] == 0 and rep["chunks"] == 14
+    two = y.copy()
+    two[37, 5] += 2
+    with pytest.raises(AssertionError, match=str(37 * 64 + 5)):
+        full_compare.assert_full_parity(two, rows, "two steps")
+    many = y.copy()
+    many[::7, 3] += 1                                    # 6 rows of 40: 0.23% of elements
+    with pytest.raises(AssertionError, match="one step off"):
+        full_compare.assert_full_parity(many, rows, "fraction")
+    h = x.copy()
+    with pytest.raises(AssertionError, match="of h differ"):
+        h_bad = h.copy()
+        h_bad[20, 0] ^= 1
+        full_compare.assert_full_parity(y.copy(), lambda a, b: (h[a:b], rows(a, b)[1]), "h",
+                                        got_h=h_bad)
