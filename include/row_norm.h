@@ -375,6 +375,26 @@ int qk_norm_rope_select_schedule(int64_t T);
 int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim,
                        float *cos_sin, rn_stream_t stream);
 
+/* rope_cos_sin_table written to a caller-owned HOST buffer: the same table
+ * (cos half, then sin half, of p * theta^(-2i/r); angle, pow, cos and sin in
+ * fp64, each entry rounded once to fp32), computed on the calling CPU thread
+ * with the C library's pow, cos and sin.  Synchronous; launches nothing and
+ * needs no GPU.  cos_sin_host [max_pos, r] fp32 in ordinary host memory
+ * (pageable or pinned), 4-byte aligned.  The fp64 pow, cos and sin of the
+ * host's C library and of the device may differ in the last bit.  An entry of
+ * this table and of rope_cos_sin_table then differs by one fp32 step at most,
+ * except where cos or sin is close to zero: there the angle's last-bit
+ * difference (below 1e-10 for positions up to 2^17) can move a tiny entry by
+ * more steps, while the absolute difference stays below 1e-10.  The table is
+ * an input of the fused kernel, which uses whatever entries it is given.  Errors: RN_ERR_SHAPE (max_pos < 0,
+ * rotary_dim odd or <= 0, theta not > 0), RN_ERR_NULL (cos_sin_host NULL
+ * with max_pos > 0), RN_ERR_ALIGN (cos_sin_host not 4-byte aligned).
+ * max_pos = 0 writes nothing and returns RN_OK.
+ * ("[pretuned] Optimize fused_qk_norm_rope on B200", "Summary": the cos/sin
+ * row of each token's position feeds the rotation.) */
+int rope_cos_sin_table_host(double theta, int64_t max_pos, int rotary_dim,
+                            float *cos_sin_host);
+
 /* rope_cos_sin_table with bf16 entries: the same fp64 angles and trig, each
  * entry rounded once from double to bf16 (ties to even; not through fp32,
  * which would round twice); written to the caller's DEVICE buffer

@@ -102,6 +102,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qk_norm_rope_fwd_ex_bf16_table.restype = i32
         L.rope_cos_sin_table_bf16.argtypes = [f64, i64, i32, vp, vp]
         L.rope_cos_sin_table_bf16.restype = i32
+        L.rope_cos_sin_table_host.argtypes = [f64, i64, i32, vp]
+        L.rope_cos_sin_table_host.restype = i32
         L.add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
         L.add_rmsnorm_fwd.restype = i32
         L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
@@ -467,11 +469,26 @@ def rope_cos_sin_table(theta: float, max_pos: int, rotary_dim: int,
                        dtype: torch.dtype | None = None, stream=None) -> torch.Tensor:
     """[max_pos, rotary_dim] table: cos half then sin half of p * theta^(-2i/r),
     fp32 (default) or bf16 (dtype=torch.bfloat16, or a bf16 `out`), each entry
-    rounded once from fp64."""
+    rounded once from fp64.  Built on the GPU into a CUDA tensor; with
+    device="cpu" (or a CPU `out`) an fp32 table is built by the library's host
+    form (rope_cos_sin_table_host) into host memory."""
     if dtype is None:
         dtype = out.dtype if out is not None else torch.float32
     if dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("rope_cos_sin_table builds fp32 or bf16 tables")
+    on_host = (out is not None and out.device.type == "cpu") or \
+        (out is None and device is not None and torch.device(device).type == "cpu")
+    if on_host:
+        if dtype != torch.float32:
+            raise TypeError("the host table builder writes fp32 entries")
+        if out is None:
+            out = torch.empty(max_pos, rotary_dim, dtype=torch.float32)
+        if out.shape != (max_pos, rotary_dim) or not out.is_contiguous():
+            raise ValueError("out must be a contiguous [max_pos, rotary_dim] tensor")
+        rc = load().rope_cos_sin_table_host(float(theta), int(max_pos), int(rotary_dim),
+                                            out.data_ptr())
+        _check(rc, "rope_cos_sin_table_host")
+        return out
     if out is None:
         out = torch.empty(max_pos, rotary_dim, dtype=dtype,
                           device=device if device is not None else "cuda")

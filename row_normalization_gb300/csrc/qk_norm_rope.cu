@@ -15,6 +15,8 @@
 //   x[r+sub*B   .. r+sub*B + B)      tail                (B = (D-r) / LPH)
 // so every neox pair (i, i + r/2) sits in one lane and the rotation needs no
 // shuffle; only the sum of squares crosses lanes (log2(LPH) xor-shuffles).
+#include <cmath>
+
 #include "rn_common.cuh"
 #include "rn_host.h"
 
@@ -1006,6 +1008,27 @@ extern "C" {
 int rope_cos_sin_table(double theta, int64_t max_pos, int rotary_dim, float *cos_sin,
                        rn_stream_t stream) {
     return rn::build_rope_table(theta, max_pos, rotary_dim, cos_sin, stream);
+}
+
+// Host form: one column i at a time, so f_i = theta^(-2i/r) is evaluated once
+// per column; every entry is the fp64 cos or sin of p * f_i rounded once to
+// fp32 (a C++ double -> float conversion rounds to nearest, ties to even).
+int rope_cos_sin_table_host(double theta, int64_t max_pos, int rotary_dim, float *cos_sin_host) {
+    if (max_pos < 0 || rotary_dim <= 0 || (rotary_dim & 1) || !(theta > 0.0)) return RN_ERR_SHAPE;
+    if (max_pos == 0) return RN_OK;
+    if (!cos_sin_host) return RN_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(cos_sin_host) & 3u) return RN_ERR_ALIGN;
+    const int h = rotary_dim / 2;
+    for (int i = 0; i < h; ++i) {
+        const double f = std::pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(rotary_dim));
+        float *col = cos_sin_host + i;
+        for (int64_t p = 0; p < max_pos; ++p) {
+            const double ang = static_cast<double>(p) * f;
+            col[p * rotary_dim] = static_cast<float>(std::cos(ang));
+            col[p * rotary_dim + h] = static_cast<float>(std::sin(ang));
+        }
+    }
+    return RN_OK;
 }
 
 int rope_cos_sin_table_bf16(double theta, int64_t max_pos, int rotary_dim, rn_bf16 *cos_sin,

@@ -87,22 +87,40 @@ __device__ __forceinline__ float sum8(uint4 v) {
     return (E::pair_sum(v.x) + E::pair_sum(v.y)) + (E::pair_sum(v.z) + E::pair_sum(v.w));
 }
 
-// Adds the deviations x_k - m of 8 packed elements to `sd` and their squares
-// to `sq` (fp32 pairs; each pair is consumed at once, so few registers).
+// Adds the deviations x_k - m of 8 packed elements and their squares to two
+// sets of fp32-pair accumulators (words x, y to a; z, w to b): each pair is
+// consumed at once (few registers) and the two sets halve the dependent
+// chains.  The row's sums are dev_sum(sd) and dev_sum(sq).
+struct DevAcc {
+    float2 sd_a, sq_a, sd_b, sq_b;
+};
+
+__device__ __forceinline__ DevAcc dev_zero() {
+    const float2 z = make_float2(0.f, 0.f);
+    return {z, z, z, z};
+}
+
 template <class E>
-__device__ __forceinline__ void dev8(uint4 v, float m, float2 &sd, float2 &sq) {
+__device__ __forceinline__ void dev8(uint4 v, float m, DevAcc &acc) {
     float2 d = E::sub2(v.x, m);
-    sd = __fadd2_rn(sd, d);
-    sq = __ffma2_rn(d, d, sq);
-    d = E::sub2(v.y, m);
-    sd = __fadd2_rn(sd, d);
-    sq = __ffma2_rn(d, d, sq);
+    acc.sd_a = __fadd2_rn(acc.sd_a, d);
+    acc.sq_a = __ffma2_rn(d, d, acc.sq_a);
     d = E::sub2(v.z, m);
-    sd = __fadd2_rn(sd, d);
-    sq = __ffma2_rn(d, d, sq);
+    acc.sd_b = __fadd2_rn(acc.sd_b, d);
+    acc.sq_b = __ffma2_rn(d, d, acc.sq_b);
+    d = E::sub2(v.y, m);
+    acc.sd_a = __fadd2_rn(acc.sd_a, d);
+    acc.sq_a = __ffma2_rn(d, d, acc.sq_a);
     d = E::sub2(v.w, m);
-    sd = __fadd2_rn(sd, d);
-    sq = __ffma2_rn(d, d, sq);
+    acc.sd_b = __fadd2_rn(acc.sd_b, d);
+    acc.sq_b = __ffma2_rn(d, d, acc.sq_b);
+}
+
+// (sum of deviations, sum of squared deviations) held in `acc`.
+__device__ __forceinline__ float2 dev_sums(const DevAcc &acc) {
+    const float2 d = __fadd2_rn(acc.sd_a, acc.sd_b);
+    const float2 q = __fadd2_rn(acc.sq_a, acc.sq_b);
+    return make_float2(d.x + d.y, q.x + q.y);
 }
 
 // Centring of a row whose mean is large against its spread.  The first
@@ -246,11 +264,12 @@ __global__ void __launch_bounds__(256) rms_warp_rows_kernel(const uint16_t *x,
             const float var = warp_sum(q1) / static_cast<float>(N) - mean * mean;
             Centring ce{__frsqrt_rn(var + eps), 0.f};
             if (!(var > 0.f && mean * mean <= 4.f * var)) {
-                float2 sd = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
+                DevAcc acc = dev_zero();
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
-                    if (lane + 32 * i < cpr) dev8<E>(v[i], mean, sd, sq);
-                ce = centre(warp_sum(sd.x + sd.y), warp_sum(sq.x + sq.y), N, eps);
+                    if (lane + 32 * i < cpr) dev8<E>(v[i], mean, acc);
+                const float2 ds = dev_sums(acc);
+                ce = centre(warp_sum(ds.x), warp_sum(ds.y), N, eps);
             }
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
@@ -354,11 +373,12 @@ __global__ void __launch_bounds__(MAXT) rms_cta_rows_kernel(const uint16_t *x,
             const float var = u1 / static_cast<float>(N) - mean * mean;
             Centring ce{__frsqrt_rn(var + eps), 0.f};
             if (!(var > 0.f && mean * mean <= 4.f * var)) {
-                float2 sd = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
+                DevAcc acc = dev_zero();
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
-                    if (tid + nt * i < cpr) dev8<E>(v[i], mean, sd, sq);
-                const float2 dv = make_float2(warp_sum(sd.x + sd.y), warp_sum(sq.x + sq.y));
+                    if (tid + nt * i < cpr) dev8<E>(v[i], mean, acc);
+                const float2 ds = dev_sums(acc);
+                const float2 dv = make_float2(warp_sum(ds.x), warp_sum(ds.y));
                 if ((tid & 31) == 0) {
                     red3[par][tid >> 5] = dv.y;
                     red4[par][tid >> 5] = dv.x;
@@ -712,12 +732,13 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
             if (__any_sync(0xffffffffu, my_exact)) {
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr) {
-                    float2 sd = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
+                    DevAcc acc = dev_zero();
 #pragma unroll
                     for (int j = 0; j < VPR; ++j)
-                        if (live(tid, j)) dev8<E>(xv[rr][j], mean[rr], sd, sq);
-                    const float dsum = warp_sum(sd.x + sd.y);
-                    const float qsum = warp_sum(sq.x + sq.y);
+                        if (live(tid, j)) dev8<E>(xv[rr][j], mean[rr], acc);
+                    const float2 ds = dev_sums(acc);
+                    const float dsum = warp_sum(ds.x);
+                    const float qsum = warp_sum(ds.y);
                     if (lane == 0) {
                         rbd[rr * kRedStride + warp] = dsum;
                         rbc[rr * kRedStride + warp] = qsum;

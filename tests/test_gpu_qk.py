@@ -331,3 +331,19 @@ def test_bf16_table_builder_matches_oracle(theta, max_pos, r):
     d = ulp_distance_bf16(got, ref)
     assert d.max() <= 1
     assert np.mean(d == 0) > 0.99999
+
+
+@pytest.mark.parametrize("r", [128, 64])
+def test_device_and_host_tables_agree(r):
+    # rope_cos_sin_table (fp64 on the device) and rope_cos_sin_table_host (fp64
+    # on the CPU) round their angles once to fp32.  The two fp64 pow and
+    # sincos may differ in the last bit: f_i by a few 2^-53 relative, so the
+    # angle p * f_i by under 1e-10 for p < 2^17.  An entry then differs by one
+    # fp32 step at most, or, where cos or sin is near zero and a step is
+    # tiny, by at most 1e-10 absolute.
+    dev = binding.rope_cos_sin_table(1e6, 131072, r).cpu().numpy()
+    host = binding.rope_cos_sin_table(1e6, 131072, r, device="cpu").numpy()
+    steps = np.abs(dev.view(np.int32).astype(np.int64) - host.view(np.int32).astype(np.int64))
+    close = np.abs(dev.astype(np.float64) - host.astype(np.float64)) <= 1e-10
+    assert np.all((steps <= 1) | close)
+    assert np.count_nonzero(steps) <= dev.size * 1e-3
