@@ -301,18 +301,23 @@ def build_inputs(torch, binding, inputs, device):
 
 
 FORCE = {"rms": 0, "qk": 0}  # schedule overrides (--rms-schedule / --qk-schedule)
+# The row norms' workspace (dynamic unit order on the row ring): one, shared by
+# every row launch, which all run in stream order.  None with --no-workspace.
+WS = {"ws": None}
 
 
 def launch_row(binding, c):
+    ws = WS["ws"]
     if "r" in c:
         binding.add_rmsnorm_fwd(c["x"], c["r"], c["w"], RMS_EPS, c["h"], c["y"],
-                                schedule=FORCE["rms"])
+                                schedule=FORCE["rms"], workspace=ws)
     elif "b" in c:
-        binding.layernorm_fwd(c["x"], c["w"], c["b"], 1e-5, c["y"], schedule=FORCE["rms"])
+        binding.layernorm_fwd(c["x"], c["w"], c["b"], 1e-5, c["y"], schedule=FORCE["rms"],
+                              workspace=ws)
     elif "l2" in c:
-        binding.l2norm_fwd(c["x"], 1e-12, c["y"], schedule=FORCE["rms"])
+        binding.l2norm_fwd(c["x"], 1e-12, c["y"], schedule=FORCE["rms"], workspace=ws)
     else:
-        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"])
+        binding.rmsnorm_fwd(c["x"], c["w"], RMS_EPS, c["y"], schedule=FORCE["rms"], workspace=ws)
 
 
 def launch_qk(binding, c):
@@ -390,7 +395,8 @@ def config_points(torch, binding, inputs, hbm_peak: float) -> dict:
     def rms_point(M, N, eps, latency):
         pair = [inputs.rmsnorm_inputs(M, N, device="cuda", seed=s) for s in (11, 12)]
         ys = [torch.empty_like(pair[0][0]) for _ in range(2)]
-        fn = lambda i: binding.rmsnorm_fwd(pair[i & 1][0], pair[0][1], eps, ys[i & 1])  # noqa: E731
+        fn = lambda i: binding.rmsnorm_fwd(pair[i & 1][0], pair[0][1], eps, ys[i & 1],  # noqa: E731
+                                           workspace=WS["ws"])
         ms = graph_ms(torch, fn, 100 if latency else 20)
         b = rms_bytes(M, N)
         pt = {"M": M, "N": N, "eps": eps, "us": round(ms * 1e3, 2),
@@ -518,6 +524,8 @@ def run_ours(args) -> int:
     device = torch.device("cuda", local)
 
     rms, qk = build_inputs(torch, binding, inputs, device)
+    if not args.no_workspace:
+        WS["ws"] = binding.new_workspace(device)
     n_launch = len(rms) + len(qk)
     torch.cuda.synchronize()
 
@@ -631,6 +639,9 @@ def run_ours(args) -> int:
         "data": "synthetic (seeded torch generators: x ~ N(0,1) with 1% outlier rows x100, w = 1 + 0.1 N(0,1); QKV ~ N(0,1), positions uniform)",
         "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step,
                    "launches_per_step": n_launch, "parallelism": f"replicas x{world}",
+                   "row_entry": ("rmsnorm_fwd_ws: one caller-owned workspace, dynamic unit order "
+                                 "on the row ring" if WS["ws"] is not None else
+                                 "rmsnorm_fwd: fixed unit order"),
                    "qk_cos_sin_table": "bf16" if QK_TABLE == "bf16" else "fp32",
                    "l2": (("inputs larger than L2: each buffer is touched once per step and a "
                            f"step moves {bytes_step / 1e9:.2f} GB, "
@@ -721,7 +732,8 @@ def run_e2e(torch, binding, rms, qk, args, dist, device):
             if done_out[i] is not None:
                 s_comp.wait_event(done_out[i])
             if kind == "rms":
-                binding.rmsnorm_fwd(dv[0], c["w"], RMS_EPS, dv[1], stream=s_comp)
+                binding.rmsnorm_fwd(dv[0], c["w"], RMS_EPS, dv[1], stream=s_comp,
+                                    workspace=WS["ws"])
                 out_dev, out_host = dv[1], hv[1]
             else:
                 binding.qk_norm_rope_fwd(dv[0], c["wq"], c["wk"], c["table"], dv[1], HQ, HKV, D,
@@ -912,6 +924,8 @@ def main() -> int:
     ap.add_argument("--row-dtype", choices=("bf16", "f16"), default="bf16",
                     help="element format of the row norms in the step (the QK op stays bf16)")
     ap.add_argument("--rms-schedule", type=int, default=0, help="force an RN_SCHED_* value")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="row norms without a workspace (the ring's fixed unit order)")
     ap.add_argument("--qk-schedule", type=int, default=0, help="force an RN_QK_* value")
     args = ap.parse_args()
     FORCE["rms"], FORCE["qk"] = args.rms_schedule, args.qk_schedule

@@ -34,7 +34,8 @@
  *     (rn_bf16); fp32 and int64 tensors as float* and int64_t*.
  *   - Every tensor pointer is a DEVICE pointer (cudaMalloc'd or managed) on
  *     the current CUDA device, 16-byte aligned, densely packed row-major.
- *   - The caller owns every buffer.  The library allocates no device memory,
+ *   - The caller owns every buffer (the *_ws forms also take a small
+ *     caller-owned workspace).  The library allocates no device memory,
  *     never synchronises, and enqueues its kernels on `stream` (NULL = the
  *     legacy default stream).  Results are ready when the stream reaches
  *     that point.  The calls can be captured into a CUDA graph.
@@ -401,6 +402,51 @@ int rope_cos_sin_table_host(double theta, int64_t max_pos, int rotary_dim,
  * cos_sin [max_pos, r] bf16, 16-byte aligned. */
 int rope_cos_sin_table_bf16(double theta, int64_t max_pos, int rotary_dim,
                             rn_bf16 *cos_sin, rn_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Workspace forms: dynamic unit order on the persistent rings                */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device memory one workspace needs. */
+#define RN_WORKSPACE_BYTES 256
+
+/* The persistent row schedule (the ring RN_SCHED_PERSIST_BULK: a
+ * warp-specialised persistent kernel, "[Inductor] Codegen Gluon", section
+ * 3.3) gives each CTA a fixed round-robin share of the units (R rows each)
+ * by default.  The SMs of one GPU do not all stream from HBM at the same
+ * rate (on a GB300 some SMs finish such a share up to 15% later than the
+ * rest), so a launch lasts as long as its slowest SMs.  With a workspace,
+ * each CTA takes about 70% of its share in the fixed order and every later
+ * unit from a counter in the workspace: CTAs on faster SMs take more units
+ * and all finish within about a stage of each other.  Launches of fewer
+ * than six units a CTA keep the fixed order.  The outputs are bit-identical
+ * either way (a row gets the same arithmetic whichever CTA takes it).  (The
+ * fused Q/K token ring measured no gain from this order and takes no
+ * workspace.)
+ *
+ * The workspace:
+ *   - RN_WORKSPACE_BYTES of DEVICE memory on the current device, 16-byte
+ *     aligned (else RN_ERR_ALIGN), owned by the caller;
+ *   - zero-filled by the caller before its first use (cudaMemset); every
+ *     launch leaves it zero again when it completes, also one whose waits
+ *     ran out (RN_STATUS_WAIT_TIMEOUT);
+ *   - serves any number of calls that run one after another (the same
+ *     stream, or streams ordered by events); calls whose kernels may run at
+ *     the same time need separate workspaces;
+ *   - NULL selects the fixed order: the call is then exactly the form
+ *     without a workspace.
+ * Schedules other than the ring never touch it. */
+
+/* rmsnorm_fwd with a workspace; otherwise the same contract and errors. */
+int rmsnorm_fwd_ws(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M,
+                   int64_t N, rn_bf16 *y, void *workspace, rn_stream_t stream);
+
+/* row_norm_fwd_ex (any row norm, either format, explicit schedule, wait
+ * limit and test flags) with a workspace. */
+int row_norm_fwd_ws(int op, int dtype, const void *x, const void *residual,
+                    const void *w, const void *b, float eps, int64_t M, int64_t N,
+                    void *h_out, void *y, void *workspace, int schedule,
+                    uint64_t wait_timeout_ns, int debug_flags, rn_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status word                                                                */

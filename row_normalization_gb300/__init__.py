@@ -11,8 +11,8 @@ from .binding import (  # noqa: F401
     RN_QK_AUTO, RN_QK_BULK, RN_ROPE_GPTJ, RN_ROPE_NEOX, RN_QK_FOUR_HEADS, RN_QK_HEAD_PER_WARP,
     RN_QK_PERSISTENT, RN_QK_TWO_HEADS,
     RN_SCHED_AUTO, RN_SCHED_CTA_ROW, RN_SCHED_PERSIST_BULK, RN_SCHED_WARP_ROW,
-    RN_STATUS_BAD_POSITION, RN_STATUS_WAIT_TIMEOUT, RowNormError, add_rmsnorm_fwd,
+    RN_STATUS_BAD_POSITION, RN_STATUS_WAIT_TIMEOUT, RN_WORKSPACE_BYTES, RowNormError, add_rmsnorm_fwd,
     add_rmsnorm_select_schedule, device_status, error_string, l2norm_fwd, layernorm_fwd,
-    layernorm_select_schedule, qk_norm_rope_fwd, qk_norm_rope_fwd_checked, qk_norm_rope_fwd_ex,
+    layernorm_select_schedule, new_workspace, qk_norm_rope_fwd, qk_norm_rope_fwd_checked, qk_norm_rope_fwd_ex,
     qk_norm_rope_select_schedule, rmsnorm_fwd, rmsnorm_select_schedule, rope_cos_sin_table,
     row_norm_select_schedule, version)

@@ -53,6 +53,8 @@ RN_OP_L2NORM = 1
 RN_OP_ADD_RMSNORM = 2
 RN_OP_LAYERNORM = 3
 
+RN_WORKSPACE_BYTES = 256
+
 _ROW_DTYPES = {torch.bfloat16: RN_DTYPE_BF16, torch.float16: RN_DTYPE_F16}
 
 
@@ -104,6 +106,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.rope_cos_sin_table_bf16.restype = i32
         L.rope_cos_sin_table_host.argtypes = [f64, i64, i32, vp]
         L.rope_cos_sin_table_host.restype = i32
+        L.rmsnorm_fwd_ws.argtypes = [vp, vp, f32, i64, i64, vp, vp, vp]
+        L.rmsnorm_fwd_ws.restype = i32
+        L.row_norm_fwd_ws.argtypes = [i32, i32, vp, vp, vp, vp, f32, i64, i64, vp, vp, vp, i32,
+                                      u64, i32, vp]
+        L.row_norm_fwd_ws.restype = i32
         L.add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
         L.add_rmsnorm_fwd.restype = i32
         L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
@@ -196,13 +203,43 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def new_workspace(device=None) -> torch.Tensor:
+    """A zeroed workspace for the *_ws entry points (RN_WORKSPACE_BYTES of
+    device memory).  Calls that run one after another (one stream) can share
+    one; calls that may run at the same time need one each."""
+    return torch.zeros(RN_WORKSPACE_BYTES, dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def _ws(workspace: torch.Tensor | None):
+    """Device pointer of a caller's workspace (checked), or None."""
+    if workspace is None:
+        return None
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    if not workspace.is_contiguous() or \
+            workspace.numel() * workspace.element_size() < RN_WORKSPACE_BYTES:
+        raise ValueError(f"workspace must be a contiguous tensor of >= {RN_WORKSPACE_BYTES} bytes")
+    return workspace.data_ptr()
+
+
+def _row_ws(name, op, dt, x, r, w, b, eps, M, N, h, y, workspace, schedule, wait_timeout_ns,
+            debug_flags, stream):
+    rc = load().row_norm_fwd_ws(op, _ROW_DTYPES[dt], _ptr(x), _ptr(r), _ptr(w), _ptr(b), eps, M,
+                                N, _ptr(h), _ptr(y), _ws(workspace), schedule, wait_timeout_ns,
+                                debug_flags, _stream(stream))
+    _check(rc, name)
+
+
 # ---------------------------------------------------------------------------
 
 def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | None = None,
                 *, schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0,
-                debug_flags: int = 0, stream=None) -> torch.Tensor:
+                debug_flags: int = 0, stream=None,
+                workspace: torch.Tensor | None = None) -> torch.Tensor:
     """y = x * rsqrt(mean(x^2, -1) + eps) * w for x [M, N] in bf16 or fp16
-    (w and y in x's dtype); returns y."""
+    (w and y in x's dtype); returns y.  With a `workspace` (new_workspace())
+    the persistent schedule takes its units in the dynamic order."""
     dt = _row_dtype(x)
     _need(x, "x", dt)
     _need(w, "w", dt)
@@ -217,6 +254,14 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
     M, N = x.shape
     L = load()
     plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if workspace is not None:
+        if plain and dt == torch.bfloat16:
+            _check(L.rmsnorm_fwd_ws(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
+                                    _ws(workspace), _stream(stream)), "rmsnorm_fwd_ws")
+        else:
+            _row_ws("row_norm_fwd_ws", RN_OP_RMSNORM, dt, x, None, w, None, eps, M, N, None, y,
+                    workspace, schedule, wait_timeout_ns, debug_flags, stream)
+        return y
     if dt == torch.float16:
         if plain:
             _check(L.rmsnorm_fwd_f16(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
@@ -236,7 +281,7 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
 
 def l2norm_fwd(x: torch.Tensor, eps: float, y: torch.Tensor | None = None, *,
                schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0, debug_flags: int = 0,
-               stream=None) -> torch.Tensor:
+               stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """y = x / max(||x||_2, eps) per row of x [M, N] (bf16 or fp16)."""
     dt = _row_dtype(x)
     _need(x, "x", dt)
@@ -249,6 +294,10 @@ def l2norm_fwd(x: torch.Tensor, eps: float, y: torch.Tensor | None = None, *,
     M, N = x.shape
     L = load()
     plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if workspace is not None:
+        _row_ws("row_norm_fwd_ws", RN_OP_L2NORM, dt, x, None, None, None, eps, M, N, None, y,
+                workspace, schedule, wait_timeout_ns, debug_flags, stream)
+        return y
     if dt == torch.float16:
         if plain:
             _check(L.l2norm_fwd_f16(x.data_ptr(), eps, M, N, y.data_ptr(), _stream(stream)),
@@ -268,7 +317,8 @@ def l2norm_fwd(x: torch.Tensor, eps: float, y: torch.Tensor | None = None, *,
 
 def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None, eps: float,
                   y: torch.Tensor | None = None, *, schedule: int = RN_SCHED_AUTO,
-                  wait_timeout_ns: int = 0, debug_flags: int = 0, stream=None) -> torch.Tensor:
+                  wait_timeout_ns: int = 0, debug_flags: int = 0, stream=None,
+                  workspace: torch.Tensor | None = None) -> torch.Tensor:
     """y = (x - mean) / sqrt(var + eps) * w + b per row (biased variance); b may
     be None.  bf16 or fp16, every tensor in x's dtype."""
     dt = _row_dtype(x)
@@ -288,6 +338,10 @@ def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None, eps:
     bp = None if b is None else b.data_ptr()
     L = load()
     plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if workspace is not None:
+        _row_ws("row_norm_fwd_ws", RN_OP_LAYERNORM, dt, x, None, w, b, eps, M, N, None, y,
+                workspace, schedule, wait_timeout_ns, debug_flags, stream)
+        return y
     if dt == torch.float16:
         if plain:
             _check(L.layernorm_fwd_f16(x.data_ptr(), w.data_ptr(), bp, eps, M, N, y.data_ptr(),
@@ -326,7 +380,7 @@ def layernorm_select_schedule(M: int, N: int) -> int:
 def add_rmsnorm_fwd(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: float,
                     h: torch.Tensor | None = None, y: torch.Tensor | None = None, *,
                     schedule: int = RN_SCHED_AUTO, wait_timeout_ns: int = 0,
-                    debug_flags: int = 0, stream=None):
+                    debug_flags: int = 0, stream=None, workspace: torch.Tensor | None = None):
     """h = x + residual, y = rmsnorm(h); returns (h, y).  bf16 or fp16, every
     tensor in x's dtype.  Pass h=residual for an in-place residual update."""
     dt = _row_dtype(x)
@@ -344,6 +398,10 @@ def add_rmsnorm_fwd(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, ep
     M, N = x.shape
     L = load()
     plain = schedule == RN_SCHED_AUTO and wait_timeout_ns == 0 and debug_flags == 0
+    if workspace is not None:
+        _row_ws("row_norm_fwd_ws", RN_OP_ADD_RMSNORM, dt, x, residual, w, None, eps, M, N, h, y,
+                workspace, schedule, wait_timeout_ns, debug_flags, stream)
+        return h, y
     if dt == torch.float16:
         if plain:
             _check(L.add_rmsnorm_fwd_f16(x.data_ptr(), residual.data_ptr(), w.data_ptr(), eps, M,

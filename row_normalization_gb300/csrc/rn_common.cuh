@@ -306,4 +306,45 @@ struct UnitSchedule {
     }
 };
 
+// Dynamic unit order of a persistent grid (the row ring).  CTA b takes its first `lead`
+// units statically (unit k * G + b for k < lead) and every later one from a
+// counter in the caller's workspace: ws[0] counts the units handed out after
+// the static ones, so a CTA whose SM streams faster takes more of them and
+// all CTAs finish within about a stage of each other.  (Under a fixed
+// round-robin some SMs of a GB300 finish up to 15% later than the rest.)
+// The static lead is about 70% of a CTA's fair share (and at least the ring
+// depth): the dynamic rest absorbs such a spread, and the CTAs reach the
+// counter spread out in time rather than all at once.  ws[1] counts the
+// producers that have finished; the last one sets both words back to zero,
+// so the workspace is zero again when the grid completes, and the next
+// launch that uses it touches it only after that completion (stream order,
+// or griddepcontrol.wait under programmatic dependent launch).
+struct DynUnits {
+    unsigned long long *ws;
+    int64_t G;
+    int64_t b;
+    int64_t lead;
+
+    __device__ __forceinline__ DynUnits(unsigned long long *ws_, int64_t G_, int64_t b_,
+                                        int64_t total_units, int stages)
+        : ws(ws_), G(G_), b(b_) {
+        const int64_t share = total_units * 7 / (10 * G_);
+        lead = share > stages ? share : stages;
+    }
+
+    __device__ __forceinline__ int64_t first(int64_t k) const { return k * G + b; }
+    // The next unit after the static ones (atomic: the caller should issue it
+    // early and use the result late, to hide the round trip).
+    __device__ __forceinline__ int64_t fetch() const {
+        return lead * G + static_cast<int64_t>(atomicAdd(ws, 1ull));
+    }
+    // Called once by every CTA's producer after its last fetch.
+    __device__ __forceinline__ void finish() const {
+        if (atomicAdd(ws + 1, 1ull) == static_cast<unsigned long long>(G - 1)) {
+            atomicExch(ws, 0ull);
+            atomicExch(ws + 1, 0ull);
+        }
+    }
+};
+
 }  // namespace rn

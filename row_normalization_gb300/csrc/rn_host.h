@@ -76,6 +76,7 @@ struct RowCall {
     uint64_t timeout_ns;
     int debug_flags;
     rn_stream_t stream;
+    void *workspace;       // RN_WORKSPACE_BYTES of zeroed device memory, or null
 };
 
 // Row kernels instantiated per element format (rows_bf16.cu, rows_f16.cu).

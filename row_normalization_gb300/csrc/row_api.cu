@@ -8,7 +8,7 @@ namespace {
 
 int run(int op, int dtype, const void *x, const void *r, const void *w, const void *b, float eps,
         int64_t M, int64_t N, void *h, void *y, int schedule, uint64_t timeout_ns,
-        int debug_flags, rn_stream_t stream) {
+        int debug_flags, rn_stream_t stream, void *workspace = nullptr) {
     const rn::RowCall c{op,
                         static_cast<const uint16_t *>(x),
                         op == rn::ROW_ADD_RMS ? static_cast<const uint16_t *>(r) : nullptr,
@@ -22,7 +22,8 @@ int run(int op, int dtype, const void *x, const void *r, const void *w, const vo
                         schedule,
                         timeout_ns,
                         debug_flags,
-                        stream};
+                        stream,
+                        workspace};
     if (dtype == RN_DTYPE_BF16) return rn::rows_run_bf16(c);
     if (dtype == RN_DTYPE_F16) return rn::rows_run_f16(c);
     return RN_ERR_ARG;
@@ -127,6 +128,21 @@ int row_norm_fwd_ex(int op, int dtype, const void *x, const void *residual, cons
     if (op < RN_OP_RMSNORM || op > RN_OP_LAYERNORM) return RN_ERR_ARG;
     return run(op, dtype, x, residual, w, b, eps, M, N, h_out, y, schedule, wait_timeout_ns,
                debug_flags, stream);
+}
+
+int rmsnorm_fwd_ws(const rn_bf16 *x, const rn_bf16 *w, float eps, int64_t M, int64_t N,
+                   rn_bf16 *y, void *workspace, rn_stream_t stream) {
+    return run(rn::ROW_RMS, RN_DTYPE_BF16, x, nullptr, w, nullptr, eps, M, N, nullptr, y,
+               RN_SCHED_AUTO, 0, 0, stream, workspace);
+}
+
+int row_norm_fwd_ws(int op, int dtype, const void *x, const void *residual, const void *w,
+                    const void *b, float eps, int64_t M, int64_t N, void *h_out, void *y,
+                    void *workspace, int schedule, uint64_t wait_timeout_ns, int debug_flags,
+                    rn_stream_t stream) {
+    if (op < RN_OP_RMSNORM || op > RN_OP_LAYERNORM) return RN_ERR_ARG;
+    return run(op, dtype, x, residual, w, b, eps, M, N, h_out, y, schedule, wait_timeout_ns,
+               debug_flags, stream, workspace);
 }
 
 int row_norm_select_schedule(int op, int64_t M, int64_t N) {

@@ -455,6 +455,7 @@ struct BulkArgs {
     int stages;
     int debug;
     uint64_t timeout_ns;
+    unsigned long long *ws;  // dynamic unit order (two zeroed words), or nullptr: round-robin
 };
 
 // Per-warp partial sums of row rr sit at [rr * kRedStride + warp]: the lane
@@ -464,6 +465,7 @@ constexpr int kRedStride = 33;
 
 // Shared memory: [stages x (R rows of x [+ R rows of r])][full mbarriers]
 //                [empty mbarriers][partial sums 6 x R x 33 floats][flags: 4 ints]
+//                [unit of each stage: stages x int64 (dynamic unit order)]
 // (three double-buffered sets of partial sums; LayerNorm reduces up to four
 // quantities a row and has four sets, 8 x R x 33 floats)
 // `nin` is the number of row inputs streamed through the ring (1, or 2 with
@@ -473,7 +475,8 @@ constexpr int bulk_red_sets(bool ln) { return ln ? 8 : 6; }
 __host__ __device__ constexpr size_t bulk_smem_bytes(int stages, int R, int N, int nin = 1,
                                                      bool ln = false) {
     return static_cast<size_t>(stages) * nin * R * N * 2 + static_cast<size_t>(stages) * 16 +
-           static_cast<size_t>(bulk_red_sets(ln)) * R * kRedStride * 4 + 16;
+           static_cast<size_t>(bulk_red_sets(ln)) * R * kRedStride * 4 + 16 +
+           static_cast<size_t>(stages) * 8;
 }
 
 // NT consumer threads (N / 8 / VPR of them) plus one producer warp.
@@ -518,6 +521,8 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
     // before a named barrier, read after it); flags[2]: "someone gave up",
     // polled inside waits so nobody waits out a full timeout needlessly.
     volatile int *flags = reinterpret_cast<volatile int *>(red + bulk_red_sets(LN) * R * kRedStride);
+    // dynamic unit order: the unit each stage holds, -1 for "no more units"
+    volatile int64_t *unit_of = reinterpret_cast<volatile int64_t *>(flags + 4);
 
     const int nt = GENERIC ? static_cast<int>(blockDim.x) - 32 : NT;
     const int NW = nt / 32;
@@ -541,17 +546,32 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
     pdl_wait();
     __syncthreads();
 
+    // Unit order: round-robin (UnitSchedule), or with a workspace the dynamic
+    // order of DynUnits over units of R consecutive rows, for launches of six
+    // units a CTA and more (below that the CTAs would all reach the counter
+    // at once, and the short launch measured slower for it).
+    const int64_t total_units = (a.M + R - 1) / R;
+    const bool dyn = a.ws != nullptr && total_units >= 6 * static_cast<int64_t>(gridDim.x);
     const UnitSchedule sched(a.M, gridDim.x, R);
     const int64_t bid = blockIdx.x;
-    const int64_t n_units = sched.units(bid);
+    const int64_t n_units = dyn ? INT64_MAX : sched.units(bid);
+    const DynUnits du(a.ws, static_cast<int64_t>(gridDim.x), bid, total_units, S);
 
     if (warp == NW) {
         // ---- producer ----
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             int64_t k = 0;
+            bool marked = false;                   // the "no more units" stage was armed
+            int64_t u_cur = dyn ? du.first(0) : 0;  // the unit of iteration k (dynamic order)
             for (; k < n_units; ++k) {
                 const int s = static_cast<int>(k % S);
+                // the unit of iteration k + 1: static, or fetched now and first
+                // read an iteration later, after two empty waits and a copy
+                // issue have hidden the round trip
+                int64_t u_after = 0;
+                if (dyn) u_after = k + 1 < du.lead ? du.first(k + 1) : du.fetch();
+                const int64_t u = u_cur;
                 if (k >= S) {
                     const uint32_t par = static_cast<uint32_t>((k / S - 1) & 1);
                     if (!mbar_wait_bounded(&empty[s], par, a.timeout_ns, &flags[2])) {
@@ -562,7 +582,20 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                 }
                 int64_t r0;
                 int rows;
-                sched.unit(bid, k, &r0, &rows);
+                if (dyn) {
+                    if (u >= total_units) {
+                        unit_of[s] = -1;  // a stage with no bytes: the consumers stop here
+                        mbar_arrive(&full[s]);
+                        marked = true;
+                        break;
+                    }
+                    unit_of[s] = u;
+                    r0 = u * R;
+                    rows = static_cast<int>(a.M - r0 < R ? a.M - r0 : R);
+                    u_cur = u_after;
+                } else {
+                    sched.unit(bid, k, &r0, &rows);
+                }
                 const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
                 mbar_arrive_expect_tx(&full[s], bytes * NIN);
                 if (!(a.debug & 1)) {
@@ -572,11 +605,15 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                         bulk_copy_g2s(dst + row_bytes * R, a.r + r0 * N, bytes, &full[s], pol);
                 }
             }
+            if (dyn) du.finish();
             // Drain: every copy issued into this CTA's ring lands before the
-            // CTA may exit.  The last use of each stage is among the last S.
+            // CTA may exit.  The last use of each stage is among the last S
+            // (the last S - 1 when the stop marker re-armed stage k % S, whose
+            // previous unit the consumers had already released).
             const int64_t issued = k;
+            const int64_t first_kk = issued - S + (marked ? 1 : 0);
             const uint64_t t0 = globaltimer_ns();
-            for (int64_t kk = (issued > S ? issued - S : 0); kk < issued; ++kk) {
+            for (int64_t kk = (first_kk > 0 ? first_kk : 0); kk < issued; ++kk) {
                 const uint64_t spent = globaltimer_ns() - t0;
                 const uint64_t budget = spent < a.timeout_ns ? a.timeout_ns - spent : 0;
                 if (!mbar_wait_bounded(&full[kk % S], static_cast<uint32_t>((kk / S) & 1), budget,
@@ -620,9 +657,9 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
     }
 
     for (int64_t k = 0; k < n_units; ++k) {
-        int64_t r0;
-        int rows;
-        sched.unit(bid, k, &r0, &rows);
+        int64_t r0 = 0;
+        int rows = 0;
+        if (!dyn) sched.unit(bid, k, &r0, &rows);
         // Keep the weights packed (16-bit) across rows: without this the
         // compiler hoists their fp32 widening out of the loop and doubles
         // the register footprint.
@@ -640,13 +677,23 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
         const uint32_t par = static_cast<uint32_t>((k / S) & 1);
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], par, a.timeout_ns, &flags[2]));
+        // Dynamic order: the stage names its unit; the stop marker is a unit
+        // with no rows, which still goes through the barrier below, so every
+        // consumer warp leaves at the same unit.
+        bool last = false;
+        if (dyn && ok) {
+            const int64_t u = unit_of[s];
+            last = u < 0;
+            r0 = last ? 0 : u * R;
+            rows = last ? 0 : static_cast<int>(a.M - r0 < R ? a.M - r0 : R);
+        }
         const uint8_t *st = ring + static_cast<size_t>(s) * stage_bytes;
         uint4 xv[R][VPR];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr)
 #pragma unroll
             for (int j = 0; j < VPR; ++j)
-                xv[rr][j] = (ok && live(tid, j))
+                xv[rr][j] = (ok && !last && live(tid, j))
                                 ? ld_shared16(st + rr * row_bytes + 16u * (tid + j * nt))
                                 : make_uint4(0u, 0u, 0u, 0u);
         if constexpr (ADD) {
@@ -656,7 +703,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
 #pragma unroll
                 for (int j = 0; j < VPR; ++j)
                     xv[rr][j] = add8<E>(xv[rr][j],
-                                     (ok && live(tid, j))
+                                     (ok && !last && live(tid, j))
                                          ? ld_shared16(st + (R + rr) * row_bytes + 16u * (tid + j * nt))
                                          : make_uint4(0u, 0u, 0u, 0u));
             if (ok) {
@@ -711,7 +758,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                 }
             }
             named_bar_sync(1, nt);
-            if (flags[k & 1]) break;  // same decision in every consumer warp
+            if (flags[k & 1] || last) break;  // same decision in every consumer warp
             // lane rr finishes row rr's statistics once; shuffles hand them out
             float my_mean = 0.f, my_rstd = 0.f, my_ncr = 0.f;
             bool my_exact = false;
@@ -792,7 +839,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                 for (int rr = 0; rr < R; ++rr) rb[rr * kRedStride + warp] = ss[rr];
             }
             named_bar_sync(1, nt);
-            if (flags[k & 1]) break;  // same decision in every consumer warp
+            if (flags[k & 1] || last) break;  // same decision in every consumer warp
             // Lane rr finishes row rr's sum and scale once; a shuffle hands it
             // to the warp (instead of every thread redoing all R rows).
             float my_scale = 0.f;
@@ -833,6 +880,7 @@ struct RowJob {
     uint16_t *h;
     const uint16_t *b;  // LayerNorm bias (may be null)
     int l2;             // L2Norm instead of RMSNorm (w may be null: unit weights)
+    unsigned long long *ws = nullptr;  // workspace: dynamic unit order on the ring
 };
 
 template <class E, bool ADD, bool LN>
@@ -1127,7 +1175,7 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     if (stages < 2) return RN_ERR_SHAPE;
     const size_t smem = bulk_smem_bytes(stages, geo.R, N, NIN, LN);
     BulkArgs a{j.x, j.w, j.y, j.r, j.h, j.b, j.l2, j.M, N, j.eps, stages, debug_flags & 1,
-               timeout_ns ? timeout_ns : 2000000000ull};
+               timeout_ns ? timeout_ns : 2000000000ull, j.ws};
     const int sm = dev.sm_count, c = ctas_per_sm;
     if (geo.generic) {
         if constexpr (ADD || LN) {  // at most 256 consumers
@@ -1225,11 +1273,13 @@ static int rows_run(const RowCall &c) {
     const bool add = c.op == ROW_ADD_RMS;
     if (!c.x || !c.y || (need_w && !c.w) || (add && (!c.r || !c.h))) return RN_ERR_NULL;
     if (!aligned16(c.x) || !aligned16(c.y) || (c.w && !aligned16(c.w)) ||
-        (add && (!aligned16(c.r) || !aligned16(c.h))) || (c.op == ROW_LN && c.b && !aligned16(c.b)))
+        (add && (!aligned16(c.r) || !aligned16(c.h))) ||
+        (c.op == ROW_LN && c.b && !aligned16(c.b)) || (c.workspace && !aligned16(c.workspace)))
         return RN_ERR_ALIGN;
     if (add && c.h == c.y) return RN_ERR_ARG;  // two different outputs
     RowJob j{c.x, c.op == ROW_L2 ? nullptr : c.w, c.eps, c.M, static_cast<int>(c.N), c.y,
-             nullptr, nullptr, nullptr, c.op == ROW_L2 ? 1 : 0};
+             nullptr, nullptr, nullptr, c.op == ROW_L2 ? 1 : 0,
+             static_cast<unsigned long long *>(c.workspace)};
     if (add) {
         j.r = c.r;
         j.h = c.h;

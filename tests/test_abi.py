@@ -231,3 +231,17 @@ def test_binding_rejects_mixed_and_unsupported_dtypes():
     with pytest.raises((TypeError, ValueError)):
         binding.rmsnorm_fwd(torch.zeros(2, 8, dtype=torch.float16),
                             torch.zeros(8, dtype=torch.bfloat16), 1e-6)
+
+
+def test_workspace_forms_checks(lib):
+    # the header's workspace size is the binding's
+    text = open(HEADER).read()
+    assert int(re.search(r"#define RN_WORKSPACE_BYTES (\d+)", text).group(1)) == \
+        binding.RN_WORKSPACE_BYTES
+    # a misaligned workspace is refused before anything is launched
+    assert lib.rmsnorm_fwd_ws(P, P, 1e-6, 4, 64, P, MISALIGNED, None) == binding.RN_ERR_ALIGN
+    assert lib.rmsnorm_fwd_ws(P, P, 1e-6, 4, 7, P, P, None) == binding.RN_ERR_SHAPE
+    assert lib.rmsnorm_fwd_ws(P, P, 1e-6, 0, 64, P, P, None) == binding.RN_OK
+    assert lib.row_norm_fwd_ws(9, 0, P, P, P, P, 1e-6, 4, 64, P, P, P, 0, 0, 0, None) == binding.RN_ERR_ARG
+    assert lib.row_norm_fwd_ws(0, 0, P, None, P, None, 1e-6, 4, 64, None, P, MISALIGNED, 0, 0, 0,
+                               None) == binding.RN_ERR_ALIGN

@@ -165,10 +165,16 @@ def test_wait_timeout_reports_status_and_context_survives():
 # ---------------------------------------------------------------------------
 
 def _check_full_size(M, N, eps, outlier_frac, seed=0):
-    """The launch the bench times, every element against the oracle."""
+    """The launch the bench times (with a workspace: the dynamic unit order),
+    every element against the oracle; the fixed order gives the same bits."""
     x, w = rmsnorm_inputs(M, N, outlier_frac=outlier_frac, device="cuda", seed=seed)
-    y = binding.rmsnorm_fwd(x, w, eps)
+    ws = binding.new_workspace()
+    y = binding.rmsnorm_fwd(x, w, eps, workspace=ws)
+    y_fixed = binding.rmsnorm_fwd(x, w, eps)
     torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_fixed.view(torch.int16))
+    assert int(ws.count_nonzero()) == 0
+    del y_fixed
     xb, wb, got = bf16_bits(x), bf16_bits(w), bf16_bits(y)
     del x, y
     assert_full_parity(got, lambda a, b: (None, oracle.rmsnorm(xb[a:b], wb, eps)),
