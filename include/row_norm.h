@@ -449,6 +449,39 @@ int row_norm_fwd_ws(int op, int dtype, const void *x, const void *residual,
                     uint64_t wait_timeout_ns, int debug_flags, rn_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm without any caller allocation                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of the library's own scratch array behind rmsnorm_fwd_noalloc (one
+ * per device that loads the library, held until the process exits). */
+#define RN_NOALLOC_SCRATCH_BYTES 256
+
+/* rmsnorm_fwd_ws with the workspace taken from a fixed scratch array of
+ * RN_NOALLOC_SCRATCH_BYTES declared inside the library, so that the caller
+ * allocates nothing at all.  This is for callers that cannot hand the library
+ * a buffer: a plug-in running inside a host framework that owns the device's
+ * memory pool and gives the plug-in no way to draw from it, or a serving
+ * process that forbids every device allocation after start-up so that its
+ * memory use stays fixed and no allocator call (which may synchronise the
+ * device) lands on its hot path.  The pages describe no such entry point;
+ * it exists for these callers only.
+ *   - Same arguments, limits, results and errors as rmsnorm_fwd; the scratch
+ *     needed is the same few bytes for every M and N, so no size is refused
+ *     for lack of scratch (sizes outside rmsnorm_fwd's limits give
+ *     RN_ERR_SHAPE).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  RN_ERR_DEVICE if the lookup fails.
+ *   - Each call clears the counters it needs (a cudaMemsetAsync of the
+ *     scratch on `stream`) before its kernel.  Calls no allocation routine.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents: calls whose kernels may overlap on the GPU (different
+ *     streams, not ordered) race on it and can compute wrong rows.  Order
+ *     them, or give each stream rmsnorm_fwd_ws and a workspace of its own. */
+int rmsnorm_fwd_noalloc(const rn_bf16 *x, const rn_bf16 *w, float eps,
+                        int64_t M, int64_t N, rn_bf16 *y, rn_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status word                                                                */
 /* ------------------------------------------------------------------------ */
 

@@ -111,6 +111,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.row_norm_fwd_ws.argtypes = [i32, i32, vp, vp, vp, vp, f32, i64, i64, vp, vp, vp, i32,
                                       u64, i32, vp]
         L.row_norm_fwd_ws.restype = i32
+        L.rmsnorm_fwd_noalloc.argtypes = [vp, vp, f32, i64, i64, vp, vp]
+        L.rmsnorm_fwd_noalloc.restype = i32
         L.add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, vp]
         L.add_rmsnorm_fwd.restype = i32
         L.add_rmsnorm_fwd_sched.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp, i32, u64, i32, vp]
@@ -276,6 +278,27 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: torch.Tensor | 
         rc = L.rmsnorm_fwd_sched(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
                                  schedule, wait_timeout_ns, debug_flags, _stream(stream))
     _check(rc, "rmsnorm_fwd")
+    return y
+
+
+def rmsnorm_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, eps: float,
+                        y: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:
+    """rmsnorm_fwd (bf16) for callers that cannot allocate device memory: the
+    library's own scratch array replaces the workspace.  Calls that may run at
+    the same time on one GPU race on that array; see include/row_norm.h."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1]:
+        raise ValueError("x must be [M, N] and w [N]")
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", torch.bfloat16)
+        if y.shape != x.shape:
+            raise ValueError("y must have x's shape")
+    M, N = x.shape
+    _check(load().rmsnorm_fwd_noalloc(x.data_ptr(), w.data_ptr(), eps, M, N, y.data_ptr(),
+                                      _stream(stream)), "rmsnorm_fwd_noalloc")
     return y
 
 
