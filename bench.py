@@ -234,21 +234,38 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(busy)}
 
 
-def traffic_per_launch(kernel: str, workload: str):
-    """DRAM bytes per launch recorded from an ncu capture (profiles/), or None
-    when no capture matches or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "row_normalization_gb300", "csrc",
-                       "row_kernels.cuh" if kernel.startswith("rms") else "qk_norm_rope.cu")
+COUNTERS_FILE = os.path.join(ROOT, "profiles", "dram_counters.txt")
+
+
+def kernel_source_digest(kernel: str) -> str:
+    """sha256[:16] of the sources a kernel is compiled from (its file and the
+    shared device helpers), which keys the recorded ncu counters."""
+    csrc = os.path.join(ROOT, "row_normalization_gb300", "csrc")
+    files = ["row_kernels.cuh" if kernel.startswith("rms") else "qk_norm_rope.cu",
+             "rn_common.cuh"]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_counters(kernel: str, workload: str):
+    """The ncu DRAM counters recorded for one launch (profiles/dram_counters.txt):
+    dram__bytes_read.sum, dram__bytes_write.sum and
+    dram__throughput.avg.pct_of_peak_sustained_elapsed, or None when no
+    capture matches or the kernel's sources changed since it was taken."""
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        with open(path) as fh:
+        digest = kernel_source_digest(kernel)
+        with open(COUNTERS_FILE) as fh:
             for line in fh:
                 if line.startswith("#") or "|" not in line:
                     continue
-                k, wl, nbytes, sha = [p.strip() for p in line.split("|")[:4]]
+                k, wl, rd, wr, pct, sha = [p.strip() for p in line.split("|")[:6]]
                 if k == kernel and wl == workload and sha == digest:
-                    return int(float(nbytes))
+                    return {"dram_bytes_read": int(float(rd)), "dram_bytes_write": int(float(wr)),
+                            "dram_throughput_pct_of_peak": float(pct),
+                            "source": "profiles/dram_counters.txt (ncu, one pass, cold caches)"}
     except OSError:
         return None
     return None
@@ -606,13 +623,22 @@ def run_ours(args) -> int:
                                                   / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
     for p in per_shape:
         p["frac_of_measured"] = round(p["gbs"] / hbm_peak, 4)
+        wl = (f"{p['op']} M={p['M']} N={p['N']}" if p["op"] != "qk_norm_rope"
+              else f"qk_norm_rope T={p['T']} r={p['rotary_dim']}")
+        p["ncu"] = ncu_counters(p["kernel"], wl)
     dom = max(per_shape, key=lambda p: p["us"])
     dom_wl = (f"{dom['op']} M={dom['M']} N={dom['N']}" if dom["op"] != "qk_norm_rope"
               else f"qk_norm_rope T={dom['T']} r={dom['rotary_dim']}")
     achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
+    dom_ncu = ncu_counters(dom["kernel"], dom_wl)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-                "traffic": traffic_per_launch(dom["kernel"], dom_wl),
+                "traffic": (dom_ncu["dram_bytes_read"] + dom_ncu["dram_bytes_write"]
+                            if dom_ncu else None),
+                "dram_bytes_read": dom_ncu["dram_bytes_read"] if dom_ncu else None,
+                "dram_bytes_write": dom_ncu["dram_bytes_write"] if dom_ncu else None,
+                "dram_throughput_pct_of_peak": (dom_ncu["dram_throughput_pct_of_peak"]
+                                                if dom_ncu else None),
                 "kernel": dom["kernel"], "launch": dom_wl,
                 "algorithmic_bytes_per_launch": dom["bytes"]}
 
