@@ -419,7 +419,8 @@ int rope_cos_sin_table_bf16(double theta, int64_t max_pos, int rotary_dim,
  * each CTA takes about 70% of its share in the fixed order and every later
  * unit from a counter in the workspace: CTAs on faster SMs take more units
  * and all finish within about a stage of each other.  Launches of fewer
- * than six units a CTA keep the fixed order.  The outputs are bit-identical
+ * than six units a CTA keep the fixed order, and so does LayerNorm, whose
+ * heavier per-row work measured mixed with the dynamic one.  The outputs are bit-identical
  * either way (a row gets the same arithmetic whichever CTA takes it).  (The
  * fused Q/K token ring measured no gain from this order and takes no
  * workspace.)
