@@ -502,9 +502,7 @@ constexpr int bulk_max_threads() {
 template <int VPR, int NT, bool LN>
 constexpr int bulk_min_ctas() { return ((LN && NT == 0 && VPR <= 2) || NT == -2) ? 2 : 1; }
 
-// DYN: the dynamic unit order (a.ws holds the counters), built separately so
-// that the round-robin build carries none of its bookkeeping.
-template <class E, int VPR, int R, int NT, bool ADD, bool LN, bool DYN>
+template <class E, int VPR, int R, int NT, bool ADD, bool LN>
 __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<VPR, NT, LN>())
     rms_persistent_bulk_kernel(const BulkArgs a) {
     constexpr bool GENERIC = NT <= 0;
@@ -548,10 +546,15 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
     pdl_wait();
     __syncthreads();
 
-    // Unit order: round-robin (UnitSchedule), or in the DYN build the dynamic
-    // order of DynUnits over units of R consecutive rows.
-    constexpr bool dyn = DYN;
+    // Unit order: round-robin (UnitSchedule), or with a workspace the dynamic
+    // order of DynUnits over units of R consecutive rows, for launches of six
+    // units a CTA and more (below that the CTAs would all reach the counter
+    // at once, and the short launch measured slower for it).  LayerNorm is
+    // built without the dynamic order: its heavier consumers measured mixed
+    // with it (+4% at 8192 x 12288, -5% at 32768 x 4096), and its run-time
+    // checks alone cost LayerNorm's instruction-bound consumers about 4%.
     const int64_t total_units = (a.M + R - 1) / R;
+    const bool dyn = !LN && a.ws != nullptr && total_units >= 6 * static_cast<int64_t>(gridDim.x);
     const UnitSchedule sched(a.M, gridDim.x, R);
     const int64_t bid = blockIdx.x;
     const int64_t n_units = dyn ? INT64_MAX : sched.units(bid);
@@ -570,7 +573,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                 // read an iteration later, after two empty waits and a copy
                 // issue have hidden the round trip
                 int64_t u_after = 0;
-                if constexpr (dyn) u_after = k + 1 < du.lead ? du.first(k + 1) : du.fetch();
+                if (dyn) u_after = k + 1 < du.lead ? du.first(k + 1) : du.fetch();
                 const int64_t u = u_cur;
                 if (k >= S) {
                     const uint32_t par = static_cast<uint32_t>((k / S - 1) & 1);
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                 }
                 int64_t r0;
                 int rows;
-                if constexpr (dyn) {
+                if (dyn) {
                     if (u >= total_units) {
                         unit_of[s] = -1;  // a stage with no bytes: the consumers stop here
                         mbar_arrive(&full[s]);
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
                         bulk_copy_g2s(dst + row_bytes * R, a.r + r0 * N, bytes, &full[s], pol);
                 }
             }
-            if constexpr (dyn) du.finish();
+            if (dyn) du.finish();
             // Drain: every copy issued into this CTA's ring lands before the
             // CTA may exit.  The last use of each stage is among the last S
             // (the last S - 1 when the stop marker re-armed stage k % S, whose
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
     for (int64_t k = 0; k < n_units; ++k) {
         int64_t r0 = 0;
         int rows = 0;
-        if constexpr (!dyn) sched.unit(bid, k, &r0, &rows);
+        if (!dyn) sched.unit(bid, k, &r0, &rows);
         // Keep the weights packed (16-bit) across rows: without this the
         // compiler hoists their fp32 widening out of the loop and doubles
         // the register footprint.
@@ -681,13 +684,11 @@ __global__ void __launch_bounds__(bulk_max_threads<VPR, R, NT>(), bulk_min_ctas<
         // with no rows, which still goes through the barrier below, so every
         // consumer warp leaves at the same unit.
         bool last = false;
-        if constexpr (dyn) {
-            if (ok) {
-                const int64_t u = unit_of[s];
-                last = u < 0;
-                r0 = last ? 0 : u * R;
-                rows = last ? 0 : static_cast<int>(a.M - r0 < R ? a.M - r0 : R);
-            }
+        if (dyn && ok) {
+            const int64_t u = unit_of[s];
+            last = u < 0;
+            r0 = last ? 0 : u * R;
+            rows = last ? 0 : static_cast<int>(a.M - r0 < R ? a.M - r0 : R);
         }
         const uint8_t *st = ring + static_cast<size_t>(s) * stage_bytes;
         uint4 xv[R][VPR];
@@ -1052,12 +1053,12 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
 // `nt` consumers and `smem` bytes of dynamic shared memory (registers, shared
 // memory and threads all counted), or -1 when the runtime cannot say.  Opts
 // the instantiation into `smem_cap` bytes of shared memory on first use.
-template <class E, int VPR, int R, int NT, bool ADD, bool LN, bool DYN = false>
+template <class E, int VPR, int R, int NT, bool ADD, bool LN>
 static int bulk_fit(int nt, size_t smem, int smem_cap) {
     static std::atomic<int> attr_done[kMaxDevices];
     // last answer per device: (consumers << 20 | smem) << 8 | CTAs, plus bit 63
     static std::atomic<uint64_t> cache[kMaxDevices];
-    const auto kernel = rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN, DYN>;
+    const auto kernel = rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>;
     const int dev = current_device_index();
     if (dev < 0 || dev >= kMaxDevices) return -1;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
@@ -1084,12 +1085,7 @@ static int bulk_fit(int nt, size_t smem, int smem_cap) {
 // Launches one instantiation of the ring on min(M, SMs x ctas) CTAs.  A
 // request for more than one CTA per SM is clamped to what the SM holds at
 // once: CTAs beyond that would run as a second wave behind the first instead
-// of beside it.  With a workspace, RMSNorm, L2Norm and the fused add take the
-// dynamic-order build for launches of six units a CTA and more (below that
-// the CTAs would all reach the counter at once, and the short launch measured
-// slower for it), if it fits as many CTAs an SM.  LayerNorm keeps the fixed
-// order: its heavier consumers measured mixed with the dynamic one (+4% at
-// 8192 x 12288, -5% at 32768 x 4096).
+// of beside it.
 template <class E, int VPR, int R, int NT, bool ADD, bool LN>
 static int launch_bulk_inst(const BulkArgs &a, int sm_count, int ctas, size_t smem, int smem_cap,
                             cudaStream_t st, int nt = NT) {
@@ -1099,14 +1095,7 @@ static int launch_bulk_inst(const BulkArgs &a, int sm_count, int ctas, size_t sm
     if (ctas > fit) ctas = fit;
     int64_t grid = static_cast<int64_t>(sm_count) * ctas;
     if (grid > a.M) grid = a.M;
-    if constexpr (!LN) {
-        const int64_t units = (a.M + R - 1) / R;
-        if (a.ws && units >= 6 * grid &&
-            bulk_fit<E, VPR, R, NT, ADD, LN, true>(nt, smem, smem_cap) >= ctas)
-            return launch_pdl(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN, true>,
-                              dim3(static_cast<unsigned>(grid)), dim3(nt + 32), smem, st, a);
-    }
-    return launch_pdl(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN, false>,
+    return launch_pdl(rms_persistent_bulk_kernel<E, VPR, R, NT, ADD, LN>,
                       dim3(static_cast<unsigned>(grid)), dim3(nt + 32), smem, st, a);
 }
 
