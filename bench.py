@@ -342,20 +342,45 @@ def launch_qk(binding, c):
                              c["r"], QK_EPS, schedule=FORCE["qk"])
 
 
-def launch_step(binding, rms, qk, events=None):
-    """Enqueue one step; optionally record an event before every launch."""
+def launch_step(binding, rms, qk, events=None, skip=None):
+    """Enqueue one step; optionally record an event before every launch, or
+    leave out launch number `skip`."""
     k = 0
     for c in rms:
         if events is not None:
             events[k].record()
+        if k != skip:
+            launch_row(binding, c)
         k += 1
-        launch_row(binding, c)
     for c in qk:
         if events is not None:
             events[k].record()
+        if k != skip:
+            launch_qk(binding, c)
         k += 1
-        launch_qk(binding, c)
     return k
+
+
+def marginal_ms(torch, binding, rms, qk, n_launch: int, steps: int, rounds: int = 3) -> list:
+    """What each launch adds to the step in context: the time of `steps`
+    whole steps minus that of the same steps without the launch, both timed
+    as pass A times (one event pair, launches overlapping their gaps),
+    interleaved, median of `rounds`; milliseconds per step."""
+    def timed(skip):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            launch_step(binding, rms, qk, skip=skip)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    out = []
+    for i in range(n_launch):
+        diffs = [timed(None) - timed(i) for _ in range(rounds)]
+        out.append(statistics.median(diffs))
+    return out
 
 
 def graph_ms(torch, launch, reps: int) -> float:
@@ -621,8 +646,13 @@ def run_ours(args) -> int:
                           "gbs": round(b / (per_launch_ms[k] * 1e-3) / 1e9, 1),
                           "gbs_counting_v": round((b + qk_v_bytes(QK_T))
                                                   / (per_launch_ms[k] * 1e-3) / 1e9, 1)})
-    for p in per_shape:
+    marg = marginal_ms(torch, binding, rms, qk, n_launch, args.marginal_steps) \
+        if args.marginal_steps > 0 else None
+    for k, p in enumerate(per_shape):
         p["frac_of_measured"] = round(p["gbs"] / hbm_peak, 4)
+        if marg is not None and marg[k] > 0:
+            p["marginal_us"] = round(marg[k] * 1e3, 2)
+            p["marginal_frac_of_measured"] = round(p["bytes"] / (marg[k] * 1e-3) / 1e9 / hbm_peak, 4)
         wl = (f"{p['op']} M={p['M']} N={p['N']}" if p["op"] != "qk_norm_rope"
               else f"qk_norm_rope T={p['T']} r={p['rotary_dim']}")
         p["ncu"] = ncu_counters(p["kernel"], wl)
@@ -685,7 +715,9 @@ def run_ours(args) -> int:
         "timing": ("value and ms_per_step: K steps with one event pair around them "
                    "(launches overlap their gaps through programmatic dependent launch); "
                    "per_shape and roofline: a second pass of the same K steps with an event "
-                   "before every launch, which serialises the launches"),
+                   "before every launch, which serialises the launches; per_shape marginal_us: "
+                   "the step's time minus that of the step without the launch, both timed "
+                   "like the value (what the launch costs in context)"),
         "per_shape": per_shape,
         "steady_per_shape": steady,
         "configs": configs,
@@ -942,6 +974,8 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--marginal-steps", type=int, default=200,
+                    help="steps per timing of each launch's marginal cost in the step (0: skip)")
     ap.add_argument("--steady-reps", type=int, default=50,
                     help="back-to-back launches per shape for steady_per_shape (0: skip)")
     ap.add_argument("--only", default="", help="profile a subset, e.g. rms:8192x16384")
