@@ -310,9 +310,15 @@ enum {
     RN_QK_TWO_HEADS = 2,       /* 16 lanes per head                      */
     RN_QK_FOUR_HEADS = 4,      /* 8 lanes per head                       */
     RN_QK_PERSISTENT = 8,      /* 8 lanes per head, persistent grid       */
-    RN_QK_BULK = 16            /* persistent CTAs stream whole tokens'
+    RN_QK_BULK = 16,           /* persistent CTAs stream whole tokens'
                                   query/key regions and cos/sin rows
                                   through a bulk-copy shared-memory ring */
+    RN_QK_PAIRS = 32           /* 8 lanes per head, two heads of a token
+                                  per 8 lanes sharing one cos/sin slice,
+                                  grid of two whole waves; results
+                                  bit-identical to RN_QK_FOUR_HEADS.  Not
+                                  for D 64 with rotary_dim 16
+                                  (RN_ERR_SHAPE when forced)              */
 };
 
 /* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*).

@@ -41,6 +41,7 @@ RN_QK_TWO_HEADS = 2
 RN_QK_FOUR_HEADS = 4
 RN_QK_PERSISTENT = 8
 RN_QK_BULK = 16
+RN_QK_PAIRS = 32
 
 RN_ROPE_NEOX = 0
 RN_ROPE_GPTJ = 1
@@ -54,6 +55,7 @@ RN_OP_ADD_RMSNORM = 2
 RN_OP_LAYERNORM = 3
 
 RN_WORKSPACE_BYTES = 256
+RN_NOALLOC_SCRATCH_BYTES = 256  # the fixed scratch array of rmsnorm_fwd_noalloc
 
 _ROW_DTYPES = {torch.bfloat16: RN_DTYPE_BF16, torch.float16: RN_DTYPE_F16}
 

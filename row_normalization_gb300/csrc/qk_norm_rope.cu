@@ -282,6 +282,199 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
     }
 }
 
+// NW consecutive 32-bit words (2*NW bf16) into registers, still packed.  The
+// pointer is aligned to the widest of 16/8/4 bytes that divides 4*NW.
+template <int NW>
+__device__ __forceinline__ void load_words(const uint16_t *p, uint32_t (&o)[NW]) {
+    if constexpr (NW % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < NW / 4; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(p + 8 * k);
+            o[4 * k + 0] = v.x; o[4 * k + 1] = v.y; o[4 * k + 2] = v.z; o[4 * k + 3] = v.w;
+        }
+    } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+        for (int k = 0; k < NW / 2; ++k) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(p + 4 * k);
+            o[2 * k + 0] = v.x; o[2 * k + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) o[k] = *reinterpret_cast<const uint32_t *>(p + 2 * k);
+    }
+}
+
+// The same operation as qk_norm_rope_kernel at 8 lanes per head, with two
+// heads per 8-lane group and round: heads j and j + 4 of the warp's eight.
+// The launch is bound by how many bytes are in flight, and two thirds of a
+// lane's in-flight registers in qk_norm_rope_kernel hold its cos/sin slice,
+// which the four heads of a warp load alike (they belong to one token).  Here
+// the warp's eight heads belong to one token whenever the normed heads per
+// token are a multiple of 8, so one cos/sin slice serves both of a group's
+// heads (a second row is read only when the two tokens differ), and the heads
+// stay packed bf16 until they are reduced.  Twice the heads in flight a warp
+// for a quarter more registers; the arithmetic is qk_norm_rope_kernel's, in
+// its order, so the results are bit-identical to it.
+template <int D, int R, int STYLE, bool TB>
+__global__ void __launch_bounds__(256) qk_pair_kernel(const QkArgs a) {
+    constexpr int LPH = 8;
+    constexpr int H2 = R / 2;
+    constexpr int A = H2 / LPH;
+    constexpr int B = (D - R) / LPH;
+    static_assert(A * LPH == H2 && B * LPH == D - R && A % 2 == 0 && B % 2 == 0, "bad layout");
+    constexpr int U1 = STYLE == 0 ? A / 2 : A;  // words: STYLE 0 first half; STYLE 1 pairs (x1, x2)
+    constexpr int U2 = STYLE == 0 ? A / 2 : 1;  // words: STYLE 0 second half
+    constexpr int U3 = B > 0 ? B / 2 : 1;       // words: tail
+    pdl_trigger();
+    pdl_wait();
+
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPH;
+    const int grp = lane / LPH;
+    const uint32_t hpt = static_cast<uint32_t>(a.Hq + a.Hkv);  // normed heads per token
+    const uint32_t total = static_cast<uint32_t>(a.T) * hpt;   // host: < 2^31
+    const int64_t W = static_cast<int64_t>(a.Hq + 2 * a.Hkv) * D;
+    const uint64_t warp0 = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
+
+    for (uint64_t base = warp0 * 8; base < total; base += nwarps * 8) {
+        uint32_t th[2], hh[2];
+        bool act[2];
+        uint16_t *head[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t g = static_cast<uint32_t>(base) + grp + 4 * j;
+            act[j] = g < total;
+            th[j] = act[j] ? g / hpt : 0u;
+            hh[j] = act[j] ? g - th[j] * hpt : 0u;
+            head[j] = a.qkv + static_cast<int64_t>(th[j]) * W + static_cast<int64_t>(hh[j]) * D;
+        }
+        int64_t p = act[0] ? __ldg(a.pos + th[0]) : 0;
+        uint32_t u1[2][U1], u2[2][U2], u3[2][U3];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (act[j]) {
+                if constexpr (STYLE == 0) {
+                    load_words<U1>(head[j] + sub * A, u1[j]);
+                    load_words<U2>(head[j] + H2 + sub * A, u2[j]);
+                } else {
+                    load_words<U1>(head[j] + sub * 2 * A, u1[j]);
+                }
+                if constexpr (B > 0) load_words<U3>(head[j] + R + sub * B, u3[j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < U1; ++i) u1[j][i] = 0u;
+#pragma unroll
+                for (int i = 0; i < U2; ++i) u2[j][i] = 0u;
+#pragma unroll
+                for (int i = 0; i < U3; ++i) u3[j][i] = 0u;
+            }
+        }
+        // a rejected position: read but never written (as qk_norm_rope_kernel)
+        auto accept = [&](int64_t &pp, bool active) {
+            bool ok = active;
+            if (a.max_pos > 0 && active && (pp < 0 || pp >= a.max_pos)) {
+                ok = false;
+                if (sub == 0) atomicOr(a.err, RN_STATUS_BAD_POSITION);
+            }
+            if (!ok) pp = 0;
+            return ok;
+        };
+        float c[A], s[A];
+        auto load_cs = [&](int64_t pp) {
+            if constexpr (TB) {
+                const uint16_t *cs = static_cast<const uint16_t *>(a.cos_sin) + pp * R;
+                load_bf<A>(cs + sub * A, c);
+                load_bf<A>(cs + H2 + sub * A, s);
+            } else {
+                const float *cs = static_cast<const float *>(a.cos_sin) + pp * R;
+                load_f32<A>(cs + sub * A, c);
+                load_f32<A>(cs + H2 + sub * A, s);
+            }
+        };
+        const bool ok0 = accept(p, act[0]);
+        load_cs(p);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            bool ok = ok0;
+            if (j == 1 && (th[1] != th[0] || !act[1])) {  // the second head is another token's
+                int64_t p1 = act[1] ? __ldg(a.pos + th[1]) : 0;
+                ok = accept(p1, act[1]);
+                load_cs(p1);
+            }
+            float x1[A], x2[A];
+#pragma unroll
+            for (int i = 0; i < A; ++i) {
+                if constexpr (STYLE == 0) {
+                    x1[i] = (i & 1) ? bf_hi(u1[j][i / 2]) : bf_lo(u1[j][i / 2]);
+                    x2[i] = (i & 1) ? bf_hi(u2[j][i / 2]) : bf_lo(u2[j][i / 2]);
+                } else {
+                    x1[i] = bf_lo(u1[j][i]);
+                    x2[i] = bf_hi(u1[j][i]);
+                }
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < A; ++i) ss = fmaf(x2[i], x2[i], fmaf(x1[i], x1[i], ss));
+            if constexpr (B > 0) {
+#pragma unroll
+                for (int i = 0; i < U3; ++i) {
+                    const float lo = bf_lo(u3[j][i]), hi = bf_hi(u3[j][i]);
+                    ss = fmaf(hi, hi, fmaf(lo, lo, ss));
+                }
+            }
+            ss = group_sum<LPH>(ss);
+            const float rstd = __frsqrt_rn(ss / static_cast<float>(D) + a.eps);
+            const uint16_t *wp = (hh[j] < static_cast<uint32_t>(a.Hq)) ? a.wq : a.wk;
+            float w1[A], w2[A];
+            if constexpr (STYLE == 0) {
+                load_bf<A>(wp + sub * A, w1);
+                load_bf<A>(wp + H2 + sub * A, w2);
+            } else {
+                float wr[2 * A];
+                load_bf<2 * A>(wp + sub * 2 * A, wr);
+#pragma unroll
+                for (int i = 0; i < A; ++i) {
+                    w1[i] = wr[2 * i];
+                    w2[i] = wr[2 * i + 1];
+                }
+            }
+            float o1[A], o2[A];
+#pragma unroll
+            for (int i = 0; i < A; ++i) {
+                const float n1 = x1[i] * rstd * w1[i];
+                const float n2 = x2[i] * rstd * w2[i];
+                o1[i] = n1 * c[i] - n2 * s[i];
+                o2[i] = n2 * c[i] + n1 * s[i];
+            }
+            if (ok) {
+                if constexpr (STYLE == 0) {
+                    store_bf<A>(head[j] + sub * A, o1);
+                    store_bf<A>(head[j] + H2 + sub * A, o2);
+                } else {
+                    float orr[2 * A];
+#pragma unroll
+                    for (int i = 0; i < A; ++i) {
+                        orr[2 * i] = o1[i];
+                        orr[2 * i + 1] = o2[i];
+                    }
+                    store_bf<2 * A>(head[j] + sub * 2 * A, orr);
+                }
+            }
+            if constexpr (B > 0) {
+                float w3[B], x3[B];
+                load_bf<B>(wp + R + sub * B, w3);
+#pragma unroll
+                for (int i = 0; i < U3; ++i) {
+                    x3[2 * i] = bf_lo(u3[j][i]) * rstd * w3[2 * i];
+                    x3[2 * i + 1] = bf_hi(u3[j][i]) * rstd * w3[2 * i + 1];
+                }
+                if (ok) store_bf<B>(head[j] + R + sub * B, x3);
+            }
+        }
+    }
+}
+
 // ---- persistent schedule: tokens streamed through a bulk-copy ring -------------
 //
 // One CTA per SM: 16 consumer warps (8 for 256-wide heads) and 1 producer warp.  A unit is `tps`
@@ -752,6 +945,33 @@ static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const De
                       dim3(kThreads), 0, st, a);
 }
 
+// Two heads per 8-lane group (qk_pair_kernel) on a grid of two whole waves:
+// SMs x twice the CTAs an SM holds at once.  Grids that are not a whole
+// number of waves measured 3-10% slower at 2048-4096 tokens, and one wave
+// loses at 4096 tokens: with two, the second wave's CTAs take the place of
+// whichever finish first, which evens out the SMs' unequal rates.
+template <int D, int R, int STYLE, bool TB>
+static int launch_qk_pairs(const QkArgs &a, cudaStream_t st, const DeviceInfo &dev) {
+    static std::atomic<int> fit_cache[kMaxDevices];
+    const int dev_idx = current_device_index();
+    if (dev_idx < 0 || dev_idx >= kMaxDevices) return RN_ERR_DEVICE;
+    int fit = fit_cache[dev_idx].load(std::memory_order_acquire);
+    if (fit <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qk_pair_kernel<D, R, STYLE, TB>,
+                                                          256, 0) != cudaSuccess || fit <= 0) {
+            cudaGetLastError();
+            return RN_ERR_DEVICE;
+        }
+        fit_cache[dev_idx].store(fit, std::memory_order_release);
+    }
+    const uint64_t total = static_cast<uint64_t>(a.T) * static_cast<uint64_t>(a.Hq + a.Hkv);
+    uint64_t blocks = (total + 63) / 64;  // 8 warps x 8 heads a round
+    const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * 2 * static_cast<uint64_t>(fit);
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(qk_pair_kernel<D, R, STYLE, TB>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(256), 0, st, a);
+}
+
 // Largest lanes-per-head <= the request that tiles both rotary halves and
 // the tail of this (D, rotary_dim); 8 always does.
 template <int D, int R, int STYLE, bool TB>
@@ -844,6 +1064,17 @@ static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic
         if (rc != RN_ERR_SHAPE || !automatic) return rc;
         persistent = true;  // a token too wide for the ring: the warp grid serves it
     }
+    if (schedule == RN_QK_PAIRS) {
+        // layouts with a whole number of words a lane in every part
+#define RN_QK_PAIRS_GO(D_, R_) \
+    if (D == (D_) && r == (R_)) return launch_qk_pairs<D_, R_, STYLE, TB>(a, st, dev);
+        RN_QK_PAIRS_GO(64, 64) RN_QK_PAIRS_GO(64, 32)
+        RN_QK_PAIRS_GO(128, 128) RN_QK_PAIRS_GO(128, 64) RN_QK_PAIRS_GO(128, 32)
+        RN_QK_PAIRS_GO(256, 256) RN_QK_PAIRS_GO(256, 128) RN_QK_PAIRS_GO(256, 64)
+#undef RN_QK_PAIRS_GO
+        // (64, 16) has one element a lane per half: the warp grid serves it
+        if (!automatic) return RN_ERR_SHAPE;
+    }
 #define RN_QK_GO(D_, R_)                                                               \
     if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_, STYLE, TB>(a, lph, persistent, st, dev);
     RN_QK_GO(64, 64) RN_QK_GO(64, 32) RN_QK_GO(64, 16)
@@ -885,6 +1116,7 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
         case RN_QK_FOUR_HEADS: lph = 8; break;
         case RN_QK_PERSISTENT: lph = 8; persistent = true; break;
         case RN_QK_BULK: lph = 8; break;
+        case RN_QK_PAIRS: lph = 8; persistent = true; break;
         default: return RN_ERR_ARG;
     }
     const DeviceInfo *dev = current_device_info();

@@ -245,3 +245,14 @@ def test_workspace_forms_checks(lib):
     assert lib.row_norm_fwd_ws(9, 0, P, P, P, P, 1e-6, 4, 64, P, P, P, 0, 0, 0, None) == binding.RN_ERR_ARG
     assert lib.row_norm_fwd_ws(0, 0, P, None, P, None, 1e-6, 4, 64, None, P, MISALIGNED, 0, 0, 0,
                                None) == binding.RN_ERR_ALIGN
+
+
+def test_header_constants_are_the_bindings():
+    # every enum value and #define the header gives a caller is in the binding,
+    # with the same value
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    consts = {n: int(v) for n, v in re.findall(r"\b(RN_[A-Z0-9_]+)\s*=\s*(-?\d+)u?\b", text)}
+    consts.update({n: int(v) for n, v in re.findall(r"#define\s+(RN_[A-Z0-9_]+)\s+(\d+)\b", text)})
+    assert {"RN_QK_PAIRS", "RN_SCHED_PERSIST_BULK", "RN_ERR_ARG", "RN_OP_LAYERNORM"} <= set(consts)
+    for name, value in consts.items():
+        assert getattr(binding, name) == value, name

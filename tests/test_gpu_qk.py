@@ -23,7 +23,10 @@ from tests.parity import assert_parity
 pytestmark = pytest.mark.gpu
 
 QK_SCHEDULES = [binding.RN_QK_AUTO, binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_TWO_HEADS,
-                binding.RN_QK_FOUR_HEADS, binding.RN_QK_PERSISTENT, binding.RN_QK_BULK]
+                binding.RN_QK_FOUR_HEADS, binding.RN_QK_PERSISTENT, binding.RN_QK_BULK,
+                binding.RN_QK_PAIRS]
+# schedules that do not take D 64 with rotary 16 (one element a lane per half)
+NOT_64_16 = (binding.RN_QK_BULK, binding.RN_QK_PAIRS)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,7 +75,7 @@ LAYOUTS = [(64, 64), (64, 32), (64, 16), (128, 128), (128, 64), (128, 32),
 @pytest.mark.parametrize("schedule", QK_SCHEDULES)
 @pytest.mark.parametrize("D,r", LAYOUTS)
 def test_layouts_every_schedule(D, r, schedule):
-    if schedule == binding.RN_QK_BULK and (D, r) == (64, 16):
+    if schedule in NOT_64_16 and (D, r) == (64, 16):
         # one element per lane per rotary half: only the warp schedules take it
         with pytest.raises(binding.RowNormError) as ei:
             run_case(5, 4, 2, D, r, positions="uniform", max_pos=97, schedule=schedule)
@@ -83,7 +86,7 @@ def test_layouts_every_schedule(D, r, schedule):
     assert_parity(got, want, f"D={D} r={r} sched={schedule}")
 
 
-@pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_BULK])
+@pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_BULK, binding.RN_QK_PAIRS])
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (1, 0), (0, 2), (7, 3), (1, 1), (64, 0)])
 @pytest.mark.parametrize("T", [1, 2, 3, 33, 1000])
 def test_head_counts_ragged(T, Hq, Hkv, schedule):
@@ -103,6 +106,20 @@ def test_bulk_ring_many_units_every_layout(D, r):
         got, want = run_case(777, 8, 2, D, r, positions="uniform", max_pos=9000,
                              schedule=binding.RN_QK_BULK, seed=stages, debug_flags=stages << 8)
         assert_parity(got, want, f"bulk D={D} r={r} stages={stages}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 2), (12, 4), (5, 2)])
+@pytest.mark.parametrize("D,r", [lr for lr in LAYOUTS if lr != (64, 16)])
+def test_pairs_many_rounds_every_layout(D, r, Hq, Hkv):
+    # Two heads per 8-lane group.  With 40 or 16 normed heads a token (a
+    # multiple of 8) both heads of a group are always one token's; with 10 or
+    # 7 they straddle two tokens in some rounds, which reads a second cos/sin
+    # row.  About 200 000 heads: several rounds a warp on the two-wave grid,
+    # the last one ragged.
+    T = 200_000 // (Hq + Hkv) + 1
+    got, want = run_case(T, Hq, Hkv, D, r, positions="uniform", max_pos=9000,
+                         schedule=binding.RN_QK_PAIRS, seed=D * 5 + r + Hq, device_inputs=True)
+    assert_parity(got, want, f"pairs D={D} r={r} Hq={Hq} Hkv={Hkv}")
 
 
 def test_bulk_wait_timeout_reports_status_and_context_survives():
@@ -144,8 +161,11 @@ def test_schedules_agree_at_scale():
                        schedule=binding.RN_QK_FOUR_HEADS, device_inputs=True)
     b, _ = run_case(4096, 32, 8, 128, 64, positions="uniform", max_pos=131072,
                     schedule=binding.RN_QK_PERSISTENT, device_inputs=True)
+    c, _ = run_case(4096, 32, 8, 128, 64, positions="uniform", max_pos=131072,
+                    schedule=binding.RN_QK_PAIRS, device_inputs=True)
     assert_parity(a, want, "four heads")
     assert np.array_equal(a, b)  # same lane layout and arithmetic: bit-identical
+    assert np.array_equal(a, c)
 
 
 @pytest.mark.parametrize("T", [9, 3000])
@@ -183,6 +203,33 @@ def test_checked_positions_skip_bad_tokens(T):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (32, 8)])
+def test_pairs_checked_positions(Hq, Hkv):
+    # The pairs schedule checks the second head's position on its own when it
+    # belongs to another token: with 6 heads a token a group often holds one
+    # head of a rejected token and one of an accepted one.
+    T, D, r, max_pos = 3000, 128, 128, 64
+    qkv, wq, wk, pos = qkv_inputs(T, Hq, Hkv, D, positions="uniform", max_pos=max_pos, seed=41)
+    bad = [0, 1, 3, 700, 701, 2998]
+    for i, t in enumerate(bad):
+        pos[t] = -1 - i if i % 2 else max_pos + i
+    table = oracle_table(1e6, max_pos, r)
+    good_pos = pos.clone()
+    good_pos[bad] = 0
+    want = oracle.qk_norm_rope(bf16_bits(qkv), bf16_bits(wq), bf16_bits(wk), table,
+                               good_pos.numpy(), Hq, Hkv, D, r, 1e-6).reshape(T, -1)
+    q = qkv.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), torch.from_numpy(table).cuda(),
+                                pos.cuda(), Hq, Hkv, D, r, 1e-6, max_pos=max_pos, err_flag=err,
+                                schedule=binding.RN_QK_PAIRS)
+    got = bf16_bits(q).reshape(T, -1)
+    assert int(err.item()) & binding.RN_STATUS_BAD_POSITION
+    assert np.array_equal(got[bad], bf16_bits(qkv).reshape(T, -1)[bad]), "rejected tokens touched"
+    ok_rows = [t for t in range(T) if t not in bad]
+    assert_parity(got[ok_rows], want[ok_rows], f"pairs checked Hq={Hq} Hkv={Hkv}")
+
+
 def test_empty_tokens_is_noop():
     q = torch.empty(0, 48 * 128, dtype=torch.bfloat16, device="cuda")
     w = torch.ones(128, dtype=torch.bfloat16, device="cuda")
@@ -204,7 +251,8 @@ def test_table_builder_matches_oracle(theta, max_pos, r):
     assert np.mean(got == ref) > 0.999
 
 
-@pytest.mark.parametrize("schedule", [binding.RN_QK_FOUR_HEADS, binding.RN_QK_BULK])
+@pytest.mark.parametrize("schedule", [binding.RN_QK_FOUR_HEADS, binding.RN_QK_BULK,
+                                      binding.RN_QK_PAIRS])
 def test_positions_view_at_8_byte_offset(schedule):
     # positions only need 8-byte alignment: a view one int64 into a buffer works
     T, Hq, Hkv, D, r = 2049, 4, 2, 128, 64
@@ -227,15 +275,15 @@ def test_positions_view_at_8_byte_offset(schedule):
 @pytest.mark.parametrize("schedule", QK_SCHEDULES)
 @pytest.mark.parametrize("D,r", LAYOUTS)
 def test_gptj_layouts_every_schedule(D, r, schedule):
-    if schedule == binding.RN_QK_BULK and (D, r) == (64, 16):
-        return  # the ring does not take this layout (warp schedules do)
+    if schedule in NOT_64_16 and (D, r) == (64, 16):
+        return  # the ring and the pairs do not take this layout (warp schedules do)
     got, want = run_case(5, 4, 2, D, r, positions="uniform", max_pos=97, schedule=schedule,
                          seed=D + r + 1, style=binding.RN_ROPE_GPTJ)
     assert_parity(got, want, f"gptj D={D} r={r} sched={schedule}")
 
 
 @pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_FOUR_HEADS,
-                                      binding.RN_QK_BULK])
+                                      binding.RN_QK_BULK, binding.RN_QK_PAIRS])
 @pytest.mark.parametrize("r", [128, 64])
 def test_gptj_many_tokens_full_compare(r, schedule):
     got, want = run_case(4096, 32, 8, 128, r, positions="uniform", max_pos=131072,
@@ -276,8 +324,8 @@ def test_gptj_checked_positions():
 @pytest.mark.parametrize("schedule", QK_SCHEDULES)
 @pytest.mark.parametrize("D,r", LAYOUTS)
 def test_bf16_table_layouts_every_schedule(D, r, schedule, style):
-    if schedule == binding.RN_QK_BULK and (D, r) == (64, 16):
-        return  # the ring does not take this layout (warp schedules do)
+    if schedule in NOT_64_16 and (D, r) == (64, 16):
+        return  # the ring and the pairs do not take this layout (warp schedules do)
     got, want = run_case(7, 4, 2, D, r, positions="uniform", max_pos=211, schedule=schedule,
                          seed=D + 3 * r + style, style=style, bf16_table=True)
     assert_parity(got, want, f"bf16 table D={D} r={r} sched={schedule} style={style}")
@@ -285,11 +333,11 @@ def test_bf16_table_layouts_every_schedule(D, r, schedule, style):
 
 @pytest.mark.parametrize("style", [binding.RN_ROPE_NEOX, binding.RN_ROPE_GPTJ])
 @pytest.mark.parametrize("schedule", [binding.RN_QK_AUTO, binding.RN_QK_PERSISTENT,
-                                      binding.RN_QK_BULK])
+                                      binding.RN_QK_BULK, binding.RN_QK_PAIRS])
 @pytest.mark.parametrize("r", [128, 64])
 def test_bf16_table_many_tokens_full_compare(r, schedule, style):
-    # 16384 tokens (4096 for the warp grid), uniform positions over 131072
-    T = 4096 if schedule == binding.RN_QK_PERSISTENT else 16384
+    # 16384 tokens (4096 for the warp grids), uniform positions over 131072
+    T = 4096 if schedule in (binding.RN_QK_PERSISTENT, binding.RN_QK_PAIRS) else 16384
     got, want = run_case(T, 32, 8, 128, r, positions="uniform", max_pos=131072,
                          device_inputs=True, seed=17 + r, schedule=schedule, style=style,
                          bf16_table=True)
@@ -308,7 +356,7 @@ def test_bf16_table_checked_positions():
     ok_rows = good.numpy()
     want[ok_rows] = oracle.qk_norm_rope(bf16_bits(qkv[good]), bf16_bits(wq), bf16_bits(wk), table,
                                         pos[good].numpy(), Hq, Hkv, D, r, 1e-6)
-    for schedule in (binding.RN_QK_FOUR_HEADS, binding.RN_QK_BULK):
+    for schedule in (binding.RN_QK_FOUR_HEADS, binding.RN_QK_BULK, binding.RN_QK_PAIRS):
         q = qkv.cuda()
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         binding.qk_norm_rope_fwd_ex(q, wq.cuda(), wk.cuda(), dev_table, pos.cuda(), Hq, Hkv, D, r,
