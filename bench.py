@@ -277,7 +277,7 @@ def ncu_counters(kernel: str, workload: str):
 
 RMS_KERNELS = {1: "rms_warp_rows_kernel", 2: "rms_cta_rows_kernel", 3: "rms_persistent_bulk_kernel"}
 QK_KERNELS = {1: "qk_norm_rope_kernel", 2: "qk_norm_rope_kernel", 4: "qk_norm_rope_kernel",
-              8: "qk_norm_rope_kernel", 16: "qk_persistent_bulk_kernel"}
+              8: "qk_norm_rope_kernel", 16: "qk_persistent_bulk_kernel", 32: "qk_pair_kernel"}
 
 
 def table_dtype(torch):
@@ -460,7 +460,9 @@ def config_points(torch, binding, inputs, hbm_peak: float) -> dict:
 
         ms = graph_ms(torch, fn, 100 if latency else 20)
         b = qk_bytes(T, r)
-        pt = {"T": T, "rotary_dim": r, "positions": positions, "us": round(ms * 1e3, 2),
+        qs = binding.qk_norm_rope_select_schedule(T, D, r)
+        pt = {"T": T, "rotary_dim": r, "positions": positions,
+              "kernel": QK_KERNELS.get(qs, str(qs)), "us": round(ms * 1e3, 2),
               "gbs": round(b / (ms * 1e-3) / 1e9, 1),
               "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
         if latency:
@@ -639,7 +641,7 @@ def run_ours(args) -> int:
     for j, c in enumerate(qk):
         k = len(rms) + j
         b = qk_bytes(QK_T, c["r"])
-        qs = FORCE["qk"] or binding.qk_norm_rope_select_schedule(QK_T)
+        qs = FORCE["qk"] or binding.qk_norm_rope_select_schedule(QK_T, D, c["r"])
         per_shape.append({"op": "qk_norm_rope", "T": QK_T, "rotary_dim": c["r"],
                           "kernel": QK_KERNELS.get(qs, str(qs)),
                           "us": round(per_launch_ms[k] * 1e3, 2), "bytes": b,

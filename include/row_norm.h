@@ -315,10 +315,12 @@ enum {
                                   through a bulk-copy shared-memory ring */
     RN_QK_PAIRS = 32           /* 8 lanes per head, two heads of a token
                                   per 8 lanes sharing one cos/sin slice,
-                                  grid of two whole waves; results
-                                  bit-identical to RN_QK_FOUR_HEADS.  Not
-                                  for D 64 with rotary_dim 16
-                                  (RN_ERR_SHAPE when forced)              */
+                                  grid of two whole waves.  Results
+                                  bit-identical to RN_QK_BULK for neox
+                                  heads up to 128 wide with an fp32 table,
+                                  to RN_QK_FOUR_HEADS otherwise.  Not for
+                                  D 64 with rotary_dim 16 (RN_ERR_SHAPE
+                                  when forced)                            */
 };
 
 /* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*).
@@ -368,12 +370,17 @@ int qk_norm_rope_fwd_ex_bf16_table(rn_bf16 *qkv, const rn_bf16 *wq,
                                    uint64_t wait_timeout_ns, int debug_flags,
                                    rn_stream_t stream);
 
-/* The schedule (RN_QK_*) that qk_norm_rope_fwd picks for T tokens (RN_ERR_SHAPE
- * if T < 0).  When it picks RN_QK_BULK for a layout the ring cannot hold
- * (D = 64 with rotary_dim = 16, or a token wider than the ring's shared
- * memory) qk_norm_rope_fwd runs RN_QK_PERSISTENT instead.  Host-only query:
- * launches nothing. */
+/* The schedule (RN_QK_*) that qk_norm_rope_fwd picks for T tokens of heads
+ * with D = 128 and rotary_dim = 128 (RN_ERR_SHAPE if T < 0).  Host-only
+ * query: launches nothing. */
 int qk_norm_rope_select_schedule(int64_t T);
+
+/* The same for any layout: the pick depends on T, D and rotary_dim (measured
+ * per layout).  RN_ERR_SHAPE if T < 0 or (D, rotary_dim) is not a layout
+ * qk_norm_rope_fwd takes.  When it picks RN_QK_BULK for a token wider than the
+ * ring's shared memory, qk_norm_rope_fwd runs RN_QK_PERSISTENT instead.
+ * Host-only query: launches nothing. */
+int qk_norm_rope_select_schedule_ex(int64_t T, int D, int rotary_dim);
 
 /* cos_sin[p, i] = cos(p * f_i), cos_sin[p, r/2 + i] = sin(p * f_i),
  * f_i = theta^(-2i/r), for p < max_pos, i < r/2 (r = rotary_dim, even, > 0).

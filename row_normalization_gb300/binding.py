@@ -135,6 +135,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.rmsnorm_select_schedule.restype = i32
         L.qk_norm_rope_select_schedule.argtypes = [i64]
         L.qk_norm_rope_select_schedule.restype = i32
+        L.qk_norm_rope_select_schedule_ex.argtypes = [i64, i32, i32]
+        L.qk_norm_rope_select_schedule_ex.restype = i32
         L.rmsnorm_fwd_f16.argtypes = [vp, vp, f32, i64, i64, vp, vp]
         L.rmsnorm_fwd_f16.restype = i32
         L.l2norm_fwd_f16.argtypes = [vp, f32, i64, i64, vp, vp]
@@ -601,11 +603,11 @@ def add_rmsnorm_select_schedule(M: int, N: int) -> int:
     return rc
 
 
-def qk_norm_rope_select_schedule(T: int) -> int:
-    """The RN_QK_* schedule qk_norm_rope_fwd picks for T tokens."""
-    rc = int(load().qk_norm_rope_select_schedule(int(T)))
+def qk_norm_rope_select_schedule(T: int, head_dim: int = 128, rotary_dim: int = 128) -> int:
+    """The RN_QK_* schedule qk_norm_rope_fwd picks for T tokens of this layout."""
+    rc = int(load().qk_norm_rope_select_schedule_ex(int(T), int(head_dim), int(rotary_dim)))
     if rc < 0:
-        raise RowNormError("qk_norm_rope_select_schedule", rc)
+        raise RowNormError("qk_norm_rope_select_schedule_ex", rc)
     return rc
 
 

@@ -282,199 +282,6 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const QkArgs a) {
     }
 }
 
-// NW consecutive 32-bit words (2*NW bf16) into registers, still packed.  The
-// pointer is aligned to the widest of 16/8/4 bytes that divides 4*NW.
-template <int NW>
-__device__ __forceinline__ void load_words(const uint16_t *p, uint32_t (&o)[NW]) {
-    if constexpr (NW % 4 == 0) {
-#pragma unroll
-        for (int k = 0; k < NW / 4; ++k) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(p + 8 * k);
-            o[4 * k + 0] = v.x; o[4 * k + 1] = v.y; o[4 * k + 2] = v.z; o[4 * k + 3] = v.w;
-        }
-    } else if constexpr (NW % 2 == 0) {
-#pragma unroll
-        for (int k = 0; k < NW / 2; ++k) {
-            const uint2 v = *reinterpret_cast<const uint2 *>(p + 4 * k);
-            o[2 * k + 0] = v.x; o[2 * k + 1] = v.y;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < NW; ++k) o[k] = *reinterpret_cast<const uint32_t *>(p + 2 * k);
-    }
-}
-
-// The same operation as qk_norm_rope_kernel at 8 lanes per head, with two
-// heads per 8-lane group and round: heads j and j + 4 of the warp's eight.
-// The launch is bound by how many bytes are in flight, and two thirds of a
-// lane's in-flight registers in qk_norm_rope_kernel hold its cos/sin slice,
-// which the four heads of a warp load alike (they belong to one token).  Here
-// the warp's eight heads belong to one token whenever the normed heads per
-// token are a multiple of 8, so one cos/sin slice serves both of a group's
-// heads (a second row is read only when the two tokens differ), and the heads
-// stay packed bf16 until they are reduced.  Twice the heads in flight a warp
-// for a quarter more registers; the arithmetic is qk_norm_rope_kernel's, in
-// its order, so the results are bit-identical to it.
-template <int D, int R, int STYLE, bool TB>
-__global__ void __launch_bounds__(256) qk_pair_kernel(const QkArgs a) {
-    constexpr int LPH = 8;
-    constexpr int H2 = R / 2;
-    constexpr int A = H2 / LPH;
-    constexpr int B = (D - R) / LPH;
-    static_assert(A * LPH == H2 && B * LPH == D - R && A % 2 == 0 && B % 2 == 0, "bad layout");
-    constexpr int U1 = STYLE == 0 ? A / 2 : A;  // words: STYLE 0 first half; STYLE 1 pairs (x1, x2)
-    constexpr int U2 = STYLE == 0 ? A / 2 : 1;  // words: STYLE 0 second half
-    constexpr int U3 = B > 0 ? B / 2 : 1;       // words: tail
-    pdl_trigger();
-    pdl_wait();
-
-    const int lane = threadIdx.x & 31;
-    const int sub = lane % LPH;
-    const int grp = lane / LPH;
-    const uint32_t hpt = static_cast<uint32_t>(a.Hq + a.Hkv);  // normed heads per token
-    const uint32_t total = static_cast<uint32_t>(a.T) * hpt;   // host: < 2^31
-    const int64_t W = static_cast<int64_t>(a.Hq + 2 * a.Hkv) * D;
-    const uint64_t warp0 = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
-
-    for (uint64_t base = warp0 * 8; base < total; base += nwarps * 8) {
-        uint32_t th[2], hh[2];
-        bool act[2];
-        uint16_t *head[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const uint32_t g = static_cast<uint32_t>(base) + grp + 4 * j;
-            act[j] = g < total;
-            th[j] = act[j] ? g / hpt : 0u;
-            hh[j] = act[j] ? g - th[j] * hpt : 0u;
-            head[j] = a.qkv + static_cast<int64_t>(th[j]) * W + static_cast<int64_t>(hh[j]) * D;
-        }
-        int64_t p = act[0] ? __ldg(a.pos + th[0]) : 0;
-        uint32_t u1[2][U1], u2[2][U2], u3[2][U3];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            if (act[j]) {
-                if constexpr (STYLE == 0) {
-                    load_words<U1>(head[j] + sub * A, u1[j]);
-                    load_words<U2>(head[j] + H2 + sub * A, u2[j]);
-                } else {
-                    load_words<U1>(head[j] + sub * 2 * A, u1[j]);
-                }
-                if constexpr (B > 0) load_words<U3>(head[j] + R + sub * B, u3[j]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < U1; ++i) u1[j][i] = 0u;
-#pragma unroll
-                for (int i = 0; i < U2; ++i) u2[j][i] = 0u;
-#pragma unroll
-                for (int i = 0; i < U3; ++i) u3[j][i] = 0u;
-            }
-        }
-        // a rejected position: read but never written (as qk_norm_rope_kernel)
-        auto accept = [&](int64_t &pp, bool active) {
-            bool ok = active;
-            if (a.max_pos > 0 && active && (pp < 0 || pp >= a.max_pos)) {
-                ok = false;
-                if (sub == 0) atomicOr(a.err, RN_STATUS_BAD_POSITION);
-            }
-            if (!ok) pp = 0;
-            return ok;
-        };
-        float c[A], s[A];
-        auto load_cs = [&](int64_t pp) {
-            if constexpr (TB) {
-                const uint16_t *cs = static_cast<const uint16_t *>(a.cos_sin) + pp * R;
-                load_bf<A>(cs + sub * A, c);
-                load_bf<A>(cs + H2 + sub * A, s);
-            } else {
-                const float *cs = static_cast<const float *>(a.cos_sin) + pp * R;
-                load_f32<A>(cs + sub * A, c);
-                load_f32<A>(cs + H2 + sub * A, s);
-            }
-        };
-        const bool ok0 = accept(p, act[0]);
-        load_cs(p);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            bool ok = ok0;
-            if (j == 1 && (th[1] != th[0] || !act[1])) {  // the second head is another token's
-                int64_t p1 = act[1] ? __ldg(a.pos + th[1]) : 0;
-                ok = accept(p1, act[1]);
-                load_cs(p1);
-            }
-            float x1[A], x2[A];
-#pragma unroll
-            for (int i = 0; i < A; ++i) {
-                if constexpr (STYLE == 0) {
-                    x1[i] = (i & 1) ? bf_hi(u1[j][i / 2]) : bf_lo(u1[j][i / 2]);
-                    x2[i] = (i & 1) ? bf_hi(u2[j][i / 2]) : bf_lo(u2[j][i / 2]);
-                } else {
-                    x1[i] = bf_lo(u1[j][i]);
-                    x2[i] = bf_hi(u1[j][i]);
-                }
-            }
-            float ss = 0.f;
-#pragma unroll
-            for (int i = 0; i < A; ++i) ss = fmaf(x2[i], x2[i], fmaf(x1[i], x1[i], ss));
-            if constexpr (B > 0) {
-#pragma unroll
-                for (int i = 0; i < U3; ++i) {
-                    const float lo = bf_lo(u3[j][i]), hi = bf_hi(u3[j][i]);
-                    ss = fmaf(hi, hi, fmaf(lo, lo, ss));
-                }
-            }
-            ss = group_sum<LPH>(ss);
-            const float rstd = __frsqrt_rn(ss / static_cast<float>(D) + a.eps);
-            const uint16_t *wp = (hh[j] < static_cast<uint32_t>(a.Hq)) ? a.wq : a.wk;
-            float w1[A], w2[A];
-            if constexpr (STYLE == 0) {
-                load_bf<A>(wp + sub * A, w1);
-                load_bf<A>(wp + H2 + sub * A, w2);
-            } else {
-                float wr[2 * A];
-                load_bf<2 * A>(wp + sub * 2 * A, wr);
-#pragma unroll
-                for (int i = 0; i < A; ++i) {
-                    w1[i] = wr[2 * i];
-                    w2[i] = wr[2 * i + 1];
-                }
-            }
-            float o1[A], o2[A];
-#pragma unroll
-            for (int i = 0; i < A; ++i) {
-                const float n1 = x1[i] * rstd * w1[i];
-                const float n2 = x2[i] * rstd * w2[i];
-                o1[i] = n1 * c[i] - n2 * s[i];
-                o2[i] = n2 * c[i] + n1 * s[i];
-            }
-            if (ok) {
-                if constexpr (STYLE == 0) {
-                    store_bf<A>(head[j] + sub * A, o1);
-                    store_bf<A>(head[j] + H2 + sub * A, o2);
-                } else {
-                    float orr[2 * A];
-#pragma unroll
-                    for (int i = 0; i < A; ++i) {
-                        orr[2 * i] = o1[i];
-                        orr[2 * i + 1] = o2[i];
-                    }
-                    store_bf<2 * A>(head[j] + sub * 2 * A, orr);
-                }
-            }
-            if constexpr (B > 0) {
-                float w3[B], x3[B];
-                load_bf<B>(wp + R + sub * B, w3);
-#pragma unroll
-                for (int i = 0; i < U3; ++i) {
-                    x3[2 * i] = bf_lo(u3[j][i]) * rstd * w3[2 * i];
-                    x3[2 * i + 1] = bf_hi(u3[j][i]) * rstd * w3[2 * i + 1];
-                }
-                if (ok) store_bf<B>(head[j] + R + sub * B, x3);
-            }
-        }
-    }
-}
-
 // ---- persistent schedule: tokens streamed through a bulk-copy ring -------------
 //
 // One CTA per SM: 16 consumer warps (8 for 256-wide heads) and 1 producer warp.  A unit is `tps`
@@ -655,6 +462,220 @@ __device__ __forceinline__ void qk_rotate(const uint32_t (&x1)[A2], const uint32
         qk_rotate_slice<A2, B2, TAIL>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
     else
         qk_rotate_slice_gptj<A2, B2, TAIL>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
+}
+
+// The same operation as qk_norm_rope_kernel at 8 lanes per head, with two
+// heads per 8-lane group and round: heads j and j + 4 of the warp's eight.
+// The launch is bound by the bytes in flight, and two thirds of a lane's
+// in-flight registers in qk_norm_rope_kernel hold its cos/sin slice, which the
+// four heads of a warp load alike (they belong to one token).  Here the warp's
+// eight heads belong to one token whenever the normed heads per token are a
+// multiple of 8, so one cos/sin slice serves both heads of a group (a second
+// row is read only when the two tokens differ), and the heads stay packed
+// bf16 until they are reduced: twice the heads in flight a warp for a quarter
+// more registers.
+//
+// Arithmetic: neox heads up to 128 wide with an fp32 table take the token
+// ring's (fp32 pairs, two accumulators, qk_rotate), and their results are
+// bit-identical to RN_QK_BULK; it measured 1% (rotary 128) to 8% (rotary 64)
+// faster at 2048-4096 tokens than the scalar form.  GPT-J pairs, bf16 tables
+// and 256-wide heads keep qk_norm_rope_kernel's scalar form (bit-identical to
+// RN_QK_FOUR_HEADS), where the packed one measured 1-5% slower: more
+// registers, or spills under the three-CTA bound.
+template <int D, int R, int STYLE, bool TB>
+__global__ void __launch_bounds__(256, D >= 256 ? 2 : 3) qk_pair_kernel(const QkArgs a) {
+    constexpr int LPH = 8;
+    constexpr int H2 = R / 2;
+    constexpr int A = H2 / LPH;
+    constexpr int B = (D - R) / LPH;
+    constexpr int A2 = A / 2;
+    constexpr int B2 = B > 0 ? B / 2 : 1;
+    constexpr bool PACKED = STYLE == 0 && D <= 128 && !TB;
+    static_assert(A * LPH == H2 && B * LPH == D - R && A % 2 == 0 && B % 2 == 0, "bad layout");
+    pdl_trigger();
+    pdl_wait();
+
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPH;
+    const int grp = lane / LPH;
+    // the lane's two rotary pieces: neox A elements of each half, GPT-J 2A
+    // contiguous elements (two A-runs)
+    const int off1 = STYLE == 0 ? sub * A : sub * 2 * A;
+    const int off2 = STYLE == 0 ? H2 + sub * A : sub * 2 * A + A;
+    const uint32_t hpt = static_cast<uint32_t>(a.Hq + a.Hkv);  // normed heads per token
+    const uint32_t total = static_cast<uint32_t>(a.T) * hpt;   // host: < 2^31
+    const int64_t W = static_cast<int64_t>(a.Hq + 2 * a.Hkv) * D;
+    const uint64_t warp0 = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
+
+    for (uint64_t base = warp0 * 8; base < total; base += nwarps * 8) {
+        uint32_t th[2], hh[2];
+        bool act[2];
+        uint16_t *head[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t g = static_cast<uint32_t>(base) + grp + 4 * j;
+            act[j] = g < total;
+            th[j] = act[j] ? g / hpt : 0u;
+            hh[j] = act[j] ? g - th[j] * hpt : 0u;
+            head[j] = a.qkv + static_cast<int64_t>(th[j]) * W + static_cast<int64_t>(hh[j]) * D;
+        }
+        int64_t p = act[0] ? __ldg(a.pos + th[0]) : 0;
+        uint32_t x1[2][A2], x2[2][A2], x3[2][B2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (act[j]) {
+                load_words<A>(head[j] + off1, x1[j]);
+                load_words<A>(head[j] + off2, x2[j]);
+                if constexpr (B > 0) load_words<B>(head[j] + R + sub * B, x3[j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < A2; ++i) x1[j][i] = x2[j][i] = 0u;
+#pragma unroll
+                for (int i = 0; i < B2; ++i) x3[j][i] = 0u;
+            }
+        }
+        // a rejected position: read but never written (as qk_norm_rope_kernel)
+        auto accept = [&](int64_t &pp, bool active) {
+            bool ok = active;
+            if (a.max_pos > 0 && active && (pp < 0 || pp >= a.max_pos)) {
+                ok = false;
+                if (sub == 0) atomicOr(a.err, RN_STATUS_BAD_POSITION);
+            }
+            if (!ok) pp = 0;
+            return ok;
+        };
+        float c[A], sn[A];
+        auto load_cs = [&](int64_t pp) {
+            if constexpr (TB) {
+                const uint16_t *cs = static_cast<const uint16_t *>(a.cos_sin) + pp * R;
+                load_bf<A>(cs + sub * A, c);
+                load_bf<A>(cs + H2 + sub * A, sn);
+            } else {
+                const float *cs = static_cast<const float *>(a.cos_sin) + pp * R;
+                load_f32<A>(cs + sub * A, c);
+                load_f32<A>(cs + H2 + sub * A, sn);
+            }
+        };
+        const bool ok0 = accept(p, act[0]);
+        load_cs(p);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            bool ok = ok0;
+            if (j == 1 && (th[1] != th[0] || !act[1])) {  // the second head is another token's
+                int64_t p1 = act[1] ? __ldg(a.pos + th[1]) : 0;
+                ok = accept(p1, act[1]);
+                load_cs(p1);
+            }
+            const uint16_t *wp = (hh[j] < static_cast<uint32_t>(a.Hq)) ? a.wq : a.wk;
+            if constexpr (PACKED) {
+                float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < A2; ++i) {
+                    const float2 u = bf2f(x1[j][i]);
+                    const float2 v = bf2f(x2[j][i]);
+                    acc = __ffma2_rn(u, u, acc);
+                    acc2 = __ffma2_rn(v, v, acc2);
+                }
+                if constexpr (B > 0) {
+#pragma unroll
+                    for (int i = 0; i < B2; ++i) {
+                        const float2 u = bf2f(x3[j][i]);
+                        if (i & 1)
+                            acc2 = __ffma2_rn(u, u, acc2);
+                        else
+                            acc = __ffma2_rn(u, u, acc);
+                    }
+                }
+                const float ss = group_sum<LPH>((acc.x + acc.y) + (acc2.x + acc2.y));
+                // D is a power of two: multiplying by 1/D is the exact division.
+                const float rstd = __frsqrt_rn(ss * (1.0f / static_cast<float>(D)) + a.eps);
+                uint32_t w1[A2], w2[A2], w3[B2];
+                load_words<A>(wp + off1, w1);
+                load_words<A>(wp + off2, w2);
+                if constexpr (B > 0) load_words<B>(wp + R + sub * B, w3);
+                uint32_t o1[A2], o2[A2], o3[B2];
+                qk_rotate<STYLE, A2, B2, (B > 0)>(x1[j], x2[j], x3[j], w1, w2, w3, c, sn, rstd, o1,
+                                                 o2, o3);
+                if (ok) {
+                    store_words<A>(head[j] + off1, o1);
+                    store_words<A>(head[j] + off2, o2);
+                    if constexpr (B > 0) store_words<B>(head[j] + R + sub * B, o3);
+                }
+            } else {
+                // qk_norm_rope_kernel's arithmetic, element by element
+                float e1[A], e2[A];
+#pragma unroll
+                for (int i = 0; i < A; ++i) {
+                    if constexpr (STYLE == 0) {
+                        e1[i] = (i & 1) ? bf_hi(x1[j][i / 2]) : bf_lo(x1[j][i / 2]);
+                        e2[i] = (i & 1) ? bf_hi(x2[j][i / 2]) : bf_lo(x2[j][i / 2]);
+                    } else {  // word i of the lane's 2A-run is the pair (x1, x2) of element i
+                        const uint32_t w = i < A2 ? x1[j][i] : x2[j][i - A2];
+                        e1[i] = bf_lo(w);
+                        e2[i] = bf_hi(w);
+                    }
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < A; ++i) ss = fmaf(e2[i], e2[i], fmaf(e1[i], e1[i], ss));
+                if constexpr (B > 0) {
+#pragma unroll
+                    for (int i = 0; i < B2; ++i) {
+                        const float lo = bf_lo(x3[j][i]), hi = bf_hi(x3[j][i]);
+                        ss = fmaf(hi, hi, fmaf(lo, lo, ss));
+                    }
+                }
+                ss = group_sum<LPH>(ss);
+                const float rstd = __frsqrt_rn(ss / static_cast<float>(D) + a.eps);
+                float w1[A], w2[A];
+                if constexpr (STYLE == 0) {
+                    load_bf<A>(wp + sub * A, w1);
+                    load_bf<A>(wp + H2 + sub * A, w2);
+                } else {
+                    float wr[2 * A];
+                    load_bf<2 * A>(wp + sub * 2 * A, wr);
+#pragma unroll
+                    for (int i = 0; i < A; ++i) {
+                        w1[i] = wr[2 * i];
+                        w2[i] = wr[2 * i + 1];
+                    }
+                }
+                float o1[A], o2[A];
+#pragma unroll
+                for (int i = 0; i < A; ++i) {
+                    const float n1 = e1[i] * rstd * w1[i];
+                    const float n2 = e2[i] * rstd * w2[i];
+                    o1[i] = n1 * c[i] - n2 * sn[i];
+                    o2[i] = n2 * c[i] + n1 * sn[i];
+                }
+                if (ok) {
+                    if constexpr (STYLE == 0) {
+                        store_bf<A>(head[j] + sub * A, o1);
+                        store_bf<A>(head[j] + H2 + sub * A, o2);
+                    } else {
+                        float orr[2 * A];
+#pragma unroll
+                        for (int i = 0; i < A; ++i) {
+                            orr[2 * i] = o1[i];
+                            orr[2 * i + 1] = o2[i];
+                        }
+                        store_bf<2 * A>(head[j] + sub * 2 * A, orr);
+                    }
+                }
+                if constexpr (B > 0) {
+                    float w3[B], e3[B];
+                    load_bf<B>(wp + R + sub * B, w3);
+#pragma unroll
+                    for (int i = 0; i < B2; ++i) {
+                        e3[2 * i] = bf_lo(x3[j][i]) * rstd * w3[2 * i];
+                        e3[2 * i + 1] = bf_hi(x3[j][i]) * rstd * w3[2 * i + 1];
+                    }
+                    if (ok) store_bf<B>(head[j] + R + sub * B, e3);
+                }
+            }
+        }
+    }
 }
 
 template <int D, int R, int STYLE, bool TB>
@@ -1035,16 +1056,42 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
                       dim3(qk_bulk_consumers<D>() + 32), smem, st, b);
 }
 
-// Schedule by token count (measured on GB300, back-to-back launches): one
-// head per warp for 1-2 tokens, two heads per warp through 256 tokens, four
-// heads per warp on a persistent grid through 4096 tokens (5-15% ahead of the
-// ring there), and the bulk-copy token ring beyond (ahead from 6144 tokens),
-// where its deeper prefetch pays for its longer start-up.
-static int auto_qk_schedule(int64_t T) {
+// Schedule by token count and layout (measured on GB300 in steady state,
+// back-to-back launches, positions uniform over 131072 rows): one head per
+// warp for 1-2 tokens, two heads per warp through 256 tokens, then four
+// heads per warp on a persistent grid until the token count reaches the
+// layout's `pairs_from`, two heads per 8-lane group (qk_pair_kernel) from
+// there, and the bulk-copy token ring above `ring_above` tokens, where its
+// deeper prefetch pays for its longer start-up.  At D 128 the pairs lead the
+// four-heads grid by 3-15% from 1024 to 4096 tokens at rotary 128 and 64
+// (except within 2% either way at 1536 tokens, rotary 64), and from 1792 at
+// rotary 32, where the four-heads grid leads by 4-7% up to 1024.  The ring
+// leads from 6144 tokens.  At D 64, and at
+// D 256 with full rotary, the ring stays behind the pairs at every count up to
+// 65536 (its tokens are small or its stages hold few of them); at D 256 with
+// rotary 64 the four-heads grid leads both everywhere.
+struct QkRule {
+    int D, r;
+    int64_t pairs_from;  // 0: never
+    int64_t ring_above;  // 0: never
+};
+static constexpr QkRule kQkRules[] = {
+    {64, 64, 1280, 0},      {64, 32, 1280, 0},      {64, 16, 0, 0},
+    {128, 128, 1024, 4096}, {128, 64, 1024, 4096}, {128, 32, 1792, 4096},
+    {256, 256, 1792, 0},    {256, 128, 1792, 4096}, {256, 64, 0, 0},
+};
+
+// RN_ERR_SHAPE for a layout no schedule serves.
+static int auto_qk_schedule(int64_t T, int D, int r) {
+    const QkRule *rule = nullptr;
+    for (const QkRule &q : kQkRules)
+        if (q.D == D && q.r == r) rule = &q;
+    if (!rule) return RN_ERR_SHAPE;
     if (T <= 2) return RN_QK_HEAD_PER_WARP;
     if (T <= 256) return RN_QK_TWO_HEADS;
-    if (T <= 4096) return RN_QK_PERSISTENT;
-    return RN_QK_BULK;
+    if (rule->ring_above > 0 && T > rule->ring_above) return RN_QK_BULK;
+    if (rule->pairs_from > 0 && T >= rule->pairs_from) return RN_QK_PAIRS;
+    return RN_QK_PERSISTENT;
 }
 
 template <int STYLE, bool TB>
@@ -1106,9 +1153,8 @@ static int qk_dispatch(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf16 *wk,
     bool persistent = false;
     const bool automatic = schedule == RN_QK_AUTO;
     if (automatic) {
-        schedule = auto_qk_schedule(T);
-        // (64, 16) has one element per lane per half: the warp grid serves it
-        if (schedule == RN_QK_BULK && D == 64 && rotary_dim == 16) schedule = RN_QK_PERSISTENT;
+        schedule = auto_qk_schedule(T, D, rotary_dim);
+        if (schedule < 0) return schedule;
     }
     switch (schedule) {
         case RN_QK_HEAD_PER_WARP: lph = 32; break;
@@ -1208,7 +1254,12 @@ int qk_norm_rope_fwd_ex_bf16_table(rn_bf16 *qkv, const rn_bf16 *wq, const rn_bf1
 
 int qk_norm_rope_select_schedule(int64_t T) {
     if (T < 0) return RN_ERR_SHAPE;
-    return rn::auto_qk_schedule(T);
+    return rn::auto_qk_schedule(T, 128, 128);
+}
+
+int qk_norm_rope_select_schedule_ex(int64_t T, int D, int rotary_dim) {
+    if (T < 0) return RN_ERR_SHAPE;
+    return rn::auto_qk_schedule(T, D, rotary_dim);
 }
 
 }  // extern "C"

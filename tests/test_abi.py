@@ -256,3 +256,29 @@ def test_header_constants_are_the_bindings():
     assert {"RN_QK_PAIRS", "RN_SCHED_PERSIST_BULK", "RN_ERR_ARG", "RN_OP_LAYERNORM"} <= set(consts)
     for name, value in consts.items():
         assert getattr(binding, name) == value, name
+
+
+def test_qk_schedule_selection_by_layout(lib):
+    # host-only: the automatic pick by token count and layout, at its boundaries
+    sel = binding.qk_norm_rope_select_schedule
+    assert [sel(T) for T in (1, 2, 3, 256, 257, 1023, 1024, 4096, 4097)] == [
+        binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_TWO_HEADS,
+        binding.RN_QK_TWO_HEADS, binding.RN_QK_PERSISTENT, binding.RN_QK_PERSISTENT,
+        binding.RN_QK_PAIRS, binding.RN_QK_PAIRS, binding.RN_QK_BULK]
+    assert sel(1023, 128, 64) == binding.RN_QK_PERSISTENT and sel(1024, 128, 64) == binding.RN_QK_PAIRS
+    assert sel(1791, 128, 32) == binding.RN_QK_PERSISTENT and sel(1792, 128, 32) == binding.RN_QK_PAIRS
+    assert lib.qk_norm_rope_select_schedule(3000) == sel(3000, 128, 128)
+    for r in (128, 64, 32):
+        assert sel(1 << 20, 128, r) == binding.RN_QK_BULK
+    # the ring never: 64-wide heads and 256-wide with full rotary take the pairs
+    for D, r in ((64, 64), (64, 32), (256, 256)):
+        assert sel(1 << 20, D, r) == binding.RN_QK_PAIRS
+    assert sel(1279, 64, 64) == binding.RN_QK_PERSISTENT and sel(1280, 64, 64) == binding.RN_QK_PAIRS
+    # one element a lane per half, and rotary 64 of 256: the four-heads grid
+    for D, r in ((64, 16), (256, 64)):
+        assert sel(1 << 20, D, r) == binding.RN_QK_PERSISTENT
+    assert sel(1 << 20, 256, 128) == binding.RN_QK_BULK
+    for T, D, r in ((-1, 128, 128), (100, 96, 96), (100, 128, 48), (100, 128, 16)):
+        assert lib.qk_norm_rope_select_schedule_ex(T, D, r) == binding.RN_ERR_SHAPE
+    with pytest.raises(binding.RowNormError):
+        sel(100, 128, 48)

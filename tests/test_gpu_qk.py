@@ -161,11 +161,31 @@ def test_schedules_agree_at_scale():
                        schedule=binding.RN_QK_FOUR_HEADS, device_inputs=True)
     b, _ = run_case(4096, 32, 8, 128, 64, positions="uniform", max_pos=131072,
                     schedule=binding.RN_QK_PERSISTENT, device_inputs=True)
-    c, _ = run_case(4096, 32, 8, 128, 64, positions="uniform", max_pos=131072,
-                    schedule=binding.RN_QK_PAIRS, device_inputs=True)
     assert_parity(a, want, "four heads")
     assert np.array_equal(a, b)  # same lane layout and arithmetic: bit-identical
-    assert np.array_equal(a, c)
+
+
+@pytest.mark.parametrize("D,r,style,bf16_table,twin", [
+    (128, 64, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
+    (128, 128, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
+    (64, 32, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
+    (128, 128, binding.RN_ROPE_GPTJ, False, binding.RN_QK_FOUR_HEADS),
+    (128, 64, binding.RN_ROPE_NEOX, True, binding.RN_QK_FOUR_HEADS),
+    (256, 128, binding.RN_ROPE_NEOX, False, binding.RN_QK_FOUR_HEADS),
+    (256, 64, binding.RN_ROPE_GPTJ, True, binding.RN_QK_FOUR_HEADS),
+])
+def test_pairs_bit_identical_to_their_twin(D, r, style, bf16_table, twin):
+    # The pairs take the ring's packed arithmetic for neox heads up to 128 wide
+    # with an fp32 table and the four-heads kernel's scalar arithmetic
+    # otherwise, in the same lane layout: bit-identical to that schedule.
+    Hq, Hkv = (32, 8) if D <= 128 else (16, 2)
+    a, want = run_case(3001, Hq, Hkv, D, r, positions="uniform", max_pos=131072,
+                       schedule=binding.RN_QK_PAIRS, device_inputs=True, seed=D + r,
+                       style=style, bf16_table=bf16_table)
+    b, _ = run_case(3001, Hq, Hkv, D, r, positions="uniform", max_pos=131072, schedule=twin,
+                    device_inputs=True, seed=D + r, style=style, bf16_table=bf16_table)
+    assert_parity(a, want, f"pairs D={D} r={r} style={style} bf16 table={bf16_table}")
+    assert np.array_equal(a, b)
 
 
 @pytest.mark.parametrize("T", [9, 3000])
