@@ -313,14 +313,13 @@ enum {
     RN_QK_BULK = 16,           /* persistent CTAs stream whole tokens'
                                   query/key regions and cos/sin rows
                                   through a bulk-copy shared-memory ring */
-    RN_QK_PAIRS = 32           /* 8 lanes per head, two heads of a token
-                                  per 8 lanes sharing one cos/sin slice,
-                                  grid of two whole waves.  Results
-                                  bit-identical to RN_QK_BULK for neox
-                                  heads up to 128 wide with an fp32 table,
-                                  to RN_QK_FOUR_HEADS otherwise.  Not for
-                                  D 64 with rotary_dim 16 (RN_ERR_SHAPE
-                                  when forced)                            */
+    RN_QK_PAIRS = 32           /* two heads of a token per lane group
+                                  sharing one cos/sin slice (4 lanes per
+                                  head at D 64, 8 at D 128, 16 at D 256),
+                                  grid of two whole waves.  At D 128 the
+                                  results are bit-identical to RN_QK_BULK
+                                  (neox, fp32 table) or RN_QK_FOUR_HEADS
+                                  (GPT-J or a bf16 table)                 */
 };
 
 /* qk_norm_rope_fwd with an explicit schedule (one of RN_QK_*).

@@ -464,33 +464,39 @@ __device__ __forceinline__ void qk_rotate(const uint32_t (&x1)[A2], const uint32
         qk_rotate_slice_gptj<A2, B2, TAIL>(x1, x2, x3, w1, w2, w3, c, sn, rstd, o1, o2, o3);
 }
 
-// The same operation as qk_norm_rope_kernel at 8 lanes per head, with two
-// heads per 8-lane group and round: heads j and j + 4 of the warp's eight.
+// The same operation as qk_norm_rope_kernel, with two heads per group of LPH
+// lanes and round: heads j and j + G of the warp's 2G (G = 32 / LPH groups).
 // The launch is bound by the bytes in flight, and two thirds of a lane's
 // in-flight registers in qk_norm_rope_kernel hold its cos/sin slice, which the
-// four heads of a warp load alike (they belong to one token).  Here the warp's
-// eight heads belong to one token whenever the normed heads per token are a
-// multiple of 8, so one cos/sin slice serves both heads of a group (a second
-// row is read only when the two tokens differ), and the heads stay packed
-// bf16 until they are reduced: twice the heads in flight a warp for a quarter
-// more registers.
+// heads of a warp load alike when they belong to one token.  Here both heads of
+// a group belong to one token whenever 2G divides the normed heads per token
+// (40 at D 128, LPH 8), so one cos/sin slice serves both (a second row is read
+// only when the two tokens differ), and the heads stay packed bf16 until they
+// are reduced: twice the heads in flight a warp for a quarter more registers.
 //
-// Arithmetic: neox heads up to 128 wide with an fp32 table take the token
-// ring's (fp32 pairs, two accumulators, qk_rotate), and their results are
-// bit-identical to RN_QK_BULK; it measured 1% (rotary 128) to 8% (rotary 64)
-// faster at 2048-4096 tokens than the scalar form.  GPT-J pairs, bf16 tables
-// and 256-wide heads keep qk_norm_rope_kernel's scalar form (bit-identical to
-// RN_QK_FOUR_HEADS), where the packed one measured 1-5% slower: more
-// registers, or spills under the three-CTA bound.
-template <int D, int R, int STYLE, bool TB>
-__global__ void __launch_bounds__(256, D >= 256 ? 2 : 3) qk_pair_kernel(const QkArgs a) {
-    constexpr int LPH = 8;
+// Lanes per head by layout (pair_lph): each lane's rotary pieces are 8
+// elements (16-byte loads) where the layout allows: 4 lanes at D 64, 8 at
+// D 128, 16 at D 256.  At 8 lanes for every D, a D 64 lane moved 8-byte
+// pieces and a D 256 lane held 32 cos/sin floats (two CTAs an SM): 0.70 and
+// 0.68 of the copy at 4096 tokens (D 64 rotary 64; D 256 rotary 256), against
+// 0.84 and 0.95 with 4 and 16 lanes.
+//
+// Arithmetic: neox heads with an fp32 table take the token ring's (fp32
+// pairs, two accumulators, qk_rotate); at D 128 (the ring's lane layout)
+// their results are bit-identical to RN_QK_BULK, and the packed form measured
+// 1% (rotary 128) to 8% (rotary 64) faster at 2048-4096 tokens than the
+// scalar one.  GPT-J pairs and bf16 tables keep qk_norm_rope_kernel's scalar
+// form (bit-identical to RN_QK_FOUR_HEADS at D 128), where the packed one
+// measured 1-5% slower.
+template <int D, int R, int LPH, int STYLE, bool TB>
+__global__ void __launch_bounds__(256, 3) qk_pair_kernel(const QkArgs a) {
+    constexpr int G = 32 / LPH;  // groups a warp
     constexpr int H2 = R / 2;
     constexpr int A = H2 / LPH;
     constexpr int B = (D - R) / LPH;
     constexpr int A2 = A / 2;
     constexpr int B2 = B > 0 ? B / 2 : 1;
-    constexpr bool PACKED = STYLE == 0 && D <= 128 && !TB;
+    constexpr bool PACKED = STYLE == 0 && !TB;
     static_assert(A * LPH == H2 && B * LPH == D - R && A % 2 == 0 && B % 2 == 0, "bad layout");
     pdl_trigger();
     pdl_wait();
@@ -508,13 +514,13 @@ __global__ void __launch_bounds__(256, D >= 256 ? 2 : 3) qk_pair_kernel(const Qk
     const uint64_t warp0 = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
 
-    for (uint64_t base = warp0 * 8; base < total; base += nwarps * 8) {
+    for (uint64_t base = warp0 * 2 * G; base < total; base += nwarps * 2 * G) {
         uint32_t th[2], hh[2];
         bool act[2];
         uint16_t *head[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const uint32_t g = static_cast<uint32_t>(base) + grp + 4 * j;
+            const uint32_t g = static_cast<uint32_t>(base) + grp + G * j;
             act[j] = g < total;
             th[j] = act[j] ? g / hpt : 0u;
             hh[j] = act[j] ? g - th[j] * hpt : 0u;
@@ -966,19 +972,24 @@ static int launch_qk(const QkArgs &a, bool persistent, cudaStream_t st, const De
                       dim3(kThreads), 0, st, a);
 }
 
-// Two heads per 8-lane group (qk_pair_kernel) on a grid of two whole waves:
+// Lanes per head of qk_pair_kernel: 16-byte rotary pieces a lane.
+template <int D>
+constexpr int pair_lph() { return D == 64 ? 4 : (D == 128 ? 8 : 16); }
+
+// Two heads per lane group (qk_pair_kernel) on a grid of two whole waves:
 // SMs x twice the CTAs an SM holds at once.  Grids that are not a whole
 // number of waves measured 3-10% slower at 2048-4096 tokens, and one wave
 // loses at 4096 tokens: with two, the second wave's CTAs take the place of
 // whichever finish first, which evens out the SMs' unequal rates.
 template <int D, int R, int STYLE, bool TB>
 static int launch_qk_pairs(const QkArgs &a, cudaStream_t st, const DeviceInfo &dev) {
+    constexpr int LPH = pair_lph<D>();
     static std::atomic<int> fit_cache[kMaxDevices];
     const int dev_idx = current_device_index();
     if (dev_idx < 0 || dev_idx >= kMaxDevices) return RN_ERR_DEVICE;
     int fit = fit_cache[dev_idx].load(std::memory_order_acquire);
     if (fit <= 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qk_pair_kernel<D, R, STYLE, TB>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qk_pair_kernel<D, R, LPH, STYLE, TB>,
                                                           256, 0) != cudaSuccess || fit <= 0) {
             cudaGetLastError();
             return RN_ERR_DEVICE;
@@ -986,10 +997,11 @@ static int launch_qk_pairs(const QkArgs &a, cudaStream_t st, const DeviceInfo &d
         fit_cache[dev_idx].store(fit, std::memory_order_release);
     }
     const uint64_t total = static_cast<uint64_t>(a.T) * static_cast<uint64_t>(a.Hq + a.Hkv);
-    uint64_t blocks = (total + 63) / 64;  // 8 warps x 8 heads a round
+    const uint64_t per_block = 8 * 2 * (32 / LPH);  // 8 warps x 2 heads a group a round
+    uint64_t blocks = (total + per_block - 1) / per_block;
     const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * 2 * static_cast<uint64_t>(fit);
     if (blocks > cap) blocks = cap;
-    return launch_pdl(qk_pair_kernel<D, R, STYLE, TB>, dim3(static_cast<unsigned>(blocks)),
+    return launch_pdl(qk_pair_kernel<D, R, LPH, STYLE, TB>, dim3(static_cast<unsigned>(blocks)),
                       dim3(256), 0, st, a);
 }
 
@@ -1058,27 +1070,30 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
 
 // Schedule by token count and layout (measured on GB300 in steady state,
 // back-to-back launches, positions uniform over 131072 rows): one head per
-// warp for 1-2 tokens, two heads per warp through 256 tokens, then four
-// heads per warp on a persistent grid until the token count reaches the
-// layout's `pairs_from`, two heads per 8-lane group (qk_pair_kernel) from
-// there, and the bulk-copy token ring above `ring_above` tokens, where its
-// deeper prefetch pays for its longer start-up.  At D 128 the pairs lead the
-// four-heads grid by 3-15% from 1024 to 4096 tokens at rotary 128 and 64
-// (except within 2% either way at 1536 tokens, rotary 64), and from 1792 at
-// rotary 32, where the four-heads grid leads by 4-7% up to 1024.  The ring
-// leads from 6144 tokens.  At D 64, and at
-// D 256 with full rotary, the ring stays behind the pairs at every count up to
-// 65536 (its tokens are small or its stages hold few of them); at D 256 with
-// rotary 64 the four-heads grid leads both everywhere.
+// warp for 1-2 tokens, two heads per warp through 256 tokens; beyond that the
+// bulk-copy token ring above `ring_above` tokens (its deeper prefetch pays
+// for its longer start-up), else the pairs (qk_pair_kernel) from `pairs_from`
+// through `pairs_upto` tokens, else four heads per warp on a persistent grid.
+//   D 128: the pairs lead the four-heads grid by 3-15% from 1024 tokens at
+//     rotary 128 and 64 (within 2% at 1536, rotary 64) and from 1792 at
+//     rotary 32; the ring leads from 6144.
+//   D 64: the pairs lead from 1024 tokens (3072 at rotary 16) at every count
+//     up to 65536 (0.82-0.91 of the copy from 4096 on, rotary 64); the ring
+//     stays behind them (tokens of 5 KB: 0.54-0.74).
+//   D 256: the pairs lead from the first persistent counts at rotary 256 and
+//     128 (rotary 256: 0.94 at 4096 tokens, 0.93 at 65536; the ring 0.57 and
+//     0.71), the ring from 6144 at rotary 128; at rotary 64 the pairs lead
+//     from 512 to 4096 and the four-heads grid beyond (0.86-0.97).
 struct QkRule {
     int D, r;
     int64_t pairs_from;  // 0: never
+    int64_t pairs_upto;  // 0: no limit
     int64_t ring_above;  // 0: never
 };
 static constexpr QkRule kQkRules[] = {
-    {64, 64, 1280, 0},      {64, 32, 1280, 0},      {64, 16, 0, 0},
-    {128, 128, 1024, 4096}, {128, 64, 1024, 4096}, {128, 32, 1792, 4096},
-    {256, 256, 1792, 0},    {256, 128, 1792, 4096}, {256, 64, 0, 0},
+    {64, 64, 1024, 0, 0},       {64, 32, 1024, 0, 0},       {64, 16, 3072, 0, 0},
+    {128, 128, 1024, 0, 4096},  {128, 64, 1024, 0, 4096},  {128, 32, 1792, 0, 4096},
+    {256, 256, 1, 0, 0},        {256, 128, 1, 0, 4096},    {256, 64, 512, 4096, 0},
 };
 
 // RN_ERR_SHAPE for a layout no schedule serves.
@@ -1090,7 +1105,9 @@ static int auto_qk_schedule(int64_t T, int D, int r) {
     if (T <= 2) return RN_QK_HEAD_PER_WARP;
     if (T <= 256) return RN_QK_TWO_HEADS;
     if (rule->ring_above > 0 && T > rule->ring_above) return RN_QK_BULK;
-    if (rule->pairs_from > 0 && T >= rule->pairs_from) return RN_QK_PAIRS;
+    if (rule->pairs_from > 0 && T >= rule->pairs_from &&
+        (rule->pairs_upto == 0 || T <= rule->pairs_upto))
+        return RN_QK_PAIRS;
     return RN_QK_PERSISTENT;
 }
 
@@ -1112,15 +1129,13 @@ static int qk_launch(const QkArgs &a, int D, int r, int schedule, bool automatic
         persistent = true;  // a token too wide for the ring: the warp grid serves it
     }
     if (schedule == RN_QK_PAIRS) {
-        // layouts with a whole number of words a lane in every part
 #define RN_QK_PAIRS_GO(D_, R_) \
     if (D == (D_) && r == (R_)) return launch_qk_pairs<D_, R_, STYLE, TB>(a, st, dev);
-        RN_QK_PAIRS_GO(64, 64) RN_QK_PAIRS_GO(64, 32)
+        RN_QK_PAIRS_GO(64, 64) RN_QK_PAIRS_GO(64, 32) RN_QK_PAIRS_GO(64, 16)
         RN_QK_PAIRS_GO(128, 128) RN_QK_PAIRS_GO(128, 64) RN_QK_PAIRS_GO(128, 32)
         RN_QK_PAIRS_GO(256, 256) RN_QK_PAIRS_GO(256, 128) RN_QK_PAIRS_GO(256, 64)
 #undef RN_QK_PAIRS_GO
-        // (64, 16) has one element a lane per half: the warp grid serves it
-        if (!automatic) return RN_ERR_SHAPE;
+        return RN_ERR_SHAPE;
     }
 #define RN_QK_GO(D_, R_)                                                               \
     if (D == (D_) && r == (R_)) return launch_qk_lph<D_, R_, STYLE, TB>(a, lph, persistent, st, dev);

@@ -271,13 +271,16 @@ def test_qk_schedule_selection_by_layout(lib):
     for r in (128, 64, 32):
         assert sel(1 << 20, 128, r) == binding.RN_QK_BULK
     # the ring never: 64-wide heads and 256-wide with full rotary take the pairs
-    for D, r in ((64, 64), (64, 32), (256, 256)):
+    for D, r in ((64, 64), (64, 32), (64, 16), (256, 256)):
         assert sel(1 << 20, D, r) == binding.RN_QK_PAIRS
-    assert sel(1279, 64, 64) == binding.RN_QK_PERSISTENT and sel(1280, 64, 64) == binding.RN_QK_PAIRS
-    # one element a lane per half, and rotary 64 of 256: the four-heads grid
-    for D, r in ((64, 16), (256, 64)):
-        assert sel(1 << 20, D, r) == binding.RN_QK_PERSISTENT
+    assert sel(1023, 64, 64) == binding.RN_QK_PERSISTENT and sel(1024, 64, 64) == binding.RN_QK_PAIRS
+    assert sel(3071, 64, 16) == binding.RN_QK_PERSISTENT and sel(3072, 64, 16) == binding.RN_QK_PAIRS
+    assert sel(257, 256, 256) == binding.RN_QK_PAIRS and sel(257, 256, 128) == binding.RN_QK_PAIRS
     assert sel(1 << 20, 256, 128) == binding.RN_QK_BULK
+    # rotary 64 of 256: the pairs from 512 through 4096 tokens, the four-heads grid around them
+    assert [sel(T, 256, 64) for T in (511, 512, 4096, 4097, 1 << 20)] == [
+        binding.RN_QK_PERSISTENT, binding.RN_QK_PAIRS, binding.RN_QK_PAIRS,
+        binding.RN_QK_PERSISTENT, binding.RN_QK_PERSISTENT]
     for T, D, r in ((-1, 128, 128), (100, 96, 96), (100, 128, 48), (100, 128, 16)):
         assert lib.qk_norm_rope_select_schedule_ex(T, D, r) == binding.RN_ERR_SHAPE
     with pytest.raises(binding.RowNormError):

@@ -25,8 +25,8 @@ pytestmark = pytest.mark.gpu
 QK_SCHEDULES = [binding.RN_QK_AUTO, binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_TWO_HEADS,
                 binding.RN_QK_FOUR_HEADS, binding.RN_QK_PERSISTENT, binding.RN_QK_BULK,
                 binding.RN_QK_PAIRS]
-# schedules that do not take D 64 with rotary 16 (one element a lane per half)
-NOT_64_16 = (binding.RN_QK_BULK, binding.RN_QK_PAIRS)
+# the ring does not take D 64 with rotary 16 (one element a lane per half)
+NOT_64_16 = (binding.RN_QK_BULK,)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -109,13 +109,14 @@ def test_bulk_ring_many_units_every_layout(D, r):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 2), (12, 4), (5, 2)])
-@pytest.mark.parametrize("D,r", [lr for lr in LAYOUTS if lr != (64, 16)])
+@pytest.mark.parametrize("D,r", LAYOUTS)
 def test_pairs_many_rounds_every_layout(D, r, Hq, Hkv):
-    # Two heads per 8-lane group.  With 40 or 16 normed heads a token (a
-    # multiple of 8) both heads of a group are always one token's; with 10 or
-    # 7 they straddle two tokens in some rounds, which reads a second cos/sin
-    # row.  About 200 000 heads: several rounds a warp on the two-wave grid,
-    # the last one ragged.
+    # Two heads per lane group (4, 8 or 16 lanes a head at D 64, 128, 256).
+    # A round covers 16, 8 or 4 consecutive heads: where that divides the
+    # normed heads a token, both heads of a group are always one token's;
+    # elsewhere (10 or 7 heads a token, 40 at D 64) they straddle two tokens
+    # in some rounds, which reads a second cos/sin row.  About 200 000 heads:
+    # several rounds a warp on the two-wave grid, the last one ragged.
     T = 200_000 // (Hq + Hkv) + 1
     got, want = run_case(T, Hq, Hkv, D, r, positions="uniform", max_pos=9000,
                          schedule=binding.RN_QK_PAIRS, seed=D * 5 + r + Hq, device_inputs=True)
@@ -168,17 +169,17 @@ def test_schedules_agree_at_scale():
 @pytest.mark.parametrize("D,r,style,bf16_table,twin", [
     (128, 64, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
     (128, 128, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
-    (64, 32, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
+    (128, 32, binding.RN_ROPE_NEOX, False, binding.RN_QK_BULK),
     (128, 128, binding.RN_ROPE_GPTJ, False, binding.RN_QK_FOUR_HEADS),
     (128, 64, binding.RN_ROPE_NEOX, True, binding.RN_QK_FOUR_HEADS),
-    (256, 128, binding.RN_ROPE_NEOX, False, binding.RN_QK_FOUR_HEADS),
-    (256, 64, binding.RN_ROPE_GPTJ, True, binding.RN_QK_FOUR_HEADS),
+    (128, 32, binding.RN_ROPE_GPTJ, True, binding.RN_QK_FOUR_HEADS),
 ])
 def test_pairs_bit_identical_to_their_twin(D, r, style, bf16_table, twin):
-    # The pairs take the ring's packed arithmetic for neox heads up to 128 wide
-    # with an fp32 table and the four-heads kernel's scalar arithmetic
-    # otherwise, in the same lane layout: bit-identical to that schedule.
-    Hq, Hkv = (32, 8) if D <= 128 else (16, 2)
+    # At D 128 the pairs share the 8-lane layout of the ring and of the
+    # four-heads kernel, and take the ring's packed arithmetic for neox with an
+    # fp32 table and the four-heads kernel's scalar arithmetic otherwise:
+    # bit-identical to that schedule.
+    Hq, Hkv = 32, 8
     a, want = run_case(3001, Hq, Hkv, D, r, positions="uniform", max_pos=131072,
                        schedule=binding.RN_QK_PAIRS, device_inputs=True, seed=D + r,
                        style=style, bf16_table=bf16_table)
@@ -296,7 +297,7 @@ def test_positions_view_at_8_byte_offset(schedule):
 @pytest.mark.parametrize("D,r", LAYOUTS)
 def test_gptj_layouts_every_schedule(D, r, schedule):
     if schedule in NOT_64_16 and (D, r) == (64, 16):
-        return  # the ring and the pairs do not take this layout (warp schedules do)
+        return  # the ring does not take this layout (the warp schedules do)
     got, want = run_case(5, 4, 2, D, r, positions="uniform", max_pos=97, schedule=schedule,
                          seed=D + r + 1, style=binding.RN_ROPE_GPTJ)
     assert_parity(got, want, f"gptj D={D} r={r} sched={schedule}")
@@ -345,7 +346,7 @@ def test_gptj_checked_positions():
 @pytest.mark.parametrize("D,r", LAYOUTS)
 def test_bf16_table_layouts_every_schedule(D, r, schedule, style):
     if schedule in NOT_64_16 and (D, r) == (64, 16):
-        return  # the ring and the pairs do not take this layout (warp schedules do)
+        return  # the ring does not take this layout (the warp schedules do)
     got, want = run_case(7, 4, 2, D, r, positions="uniform", max_pos=211, schedule=schedule,
                          seed=D + 3 * r + style, style=style, bf16_table=True)
     assert_parity(got, want, f"bf16 table D={D} r={r} sched={schedule} style={style}")
