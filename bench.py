@@ -740,6 +740,39 @@ def run_ours(args) -> int:
 E2E_CHUNK_BYTES = 64 << 20
 
 
+def link_copy_gbs(torch, device, nbytes: int = 512 << 20, reps: int = 5) -> float:
+    """What this host link carries with both directions busy: one pinned
+    host-to-device and one device-to-host copy of `nbytes` each, on two
+    streams at once, median of `reps` (GB/s, both directions added up).  The
+    e2e pipeline moves the same two directions, so its `link_gbs` is read
+    against this."""
+    hin = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    hout = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    din = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dout = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    times = []
+    for _ in range(reps + 1):
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        s1.wait_stream(torch.cuda.current_stream())
+        s2.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s1):
+            din.copy_(hin, non_blocking=True)
+        with torch.cuda.stream(s2):
+            hout.copy_(dout, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(s1)
+        torch.cuda.current_stream().wait_stream(s2)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times[1:])
+    del hin, hout, din, dout
+    return 2 * nbytes / (ms * 1e-3) / 1e9
+
+
 def run_e2e(torch, binding, rms, qk, args, dist, device):
     """The same step with host buffers, through the same C entry points.
 
@@ -773,6 +806,8 @@ def run_e2e(torch, binding, rms, qk, args, dist, device):
     h2d = sum(h[0].numel() * h[0].element_size() + (h[1].numel() * 8 if k == "qk" else 0)
               for k, _, _, h in chunks)
     d2h = sum((h[1] if k == "rms" else h[2]).numel() * 2 for k, _, _, h in chunks)
+
+    link_peak = link_copy_gbs(torch, device)
 
     n = len(chunks)
     done_comp = [None] * n  # kernel of the previous step on this chunk (WAR for the copy in)
@@ -836,6 +871,8 @@ def run_e2e(torch, binding, rms, qk, args, dist, device):
             "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": round(ms / E, 3),
             "host_wall_ms_per_step": round(wall_ms / E, 3),
             "link_gbs": round((h2d + d2h) / (ms / E * 1e-3) / 1e9, 1),
+            "link_peak_gbs": round(link_peak, 1),
+            "link_frac": round((h2d + d2h) / (ms / E * 1e-3) / 1e9 / link_peak, 4),
             "note": ("activations in from pinned host memory and results back every step, "
                      f"{n} chunks of <= 64 MB pipelined over copy-in / kernel / copy-out streams; "
                      "weights and the cos/sin table stay resident")}
