@@ -1076,13 +1076,14 @@ static int launch_qk_bulk(const QkArgs &a, cudaStream_t st, const DeviceInfo &de
 // through `pairs_upto` tokens, else four heads per warp on a persistent grid.
 //   D 128: the pairs lead the four-heads grid by 3-15% from 1024 tokens at
 //     rotary 128 and 64 (within 2% at 1536, rotary 64) and from 1792 at
-//     rotary 32; the ring leads from 6144.
+//     rotary 32, and the ring by 4-10% through 5120 tokens (4608 at rotary
+//     64); from 6144 they are even, and the ring leads from 8192-12288.
 //   D 64: the pairs lead from 1024 tokens (3072 at rotary 16) at every count
 //     up to 65536 (0.82-0.91 of the copy from 4096 on, rotary 64); the ring
 //     stays behind them (tokens of 5 KB: 0.54-0.74).
 //   D 256: the pairs lead from the first persistent counts at rotary 256 and
 //     128 (rotary 256: 0.94 at 4096 tokens, 0.93 at 65536; the ring 0.57 and
-//     0.71), the ring from 6144 at rotary 128; at rotary 64 the pairs lead
+//     0.71), the ring from 8192 at rotary 128; at rotary 64 the pairs lead
 //     from 512 to 4096 and the four-heads grid beyond (0.86-0.97).
 struct QkRule {
     int D, r;
@@ -1092,8 +1093,8 @@ struct QkRule {
 };
 static constexpr QkRule kQkRules[] = {
     {64, 64, 1024, 0, 0},       {64, 32, 1024, 0, 0},       {64, 16, 3072, 0, 0},
-    {128, 128, 1024, 0, 4096},  {128, 64, 1024, 0, 4096},  {128, 32, 1792, 0, 4096},
-    {256, 256, 1, 0, 0},        {256, 128, 1, 0, 4096},    {256, 64, 512, 4096, 0},
+    {128, 128, 1024, 0, 5120},  {128, 64, 1024, 0, 4096},  {128, 32, 1792, 0, 5120},
+    {256, 256, 1, 0, 0},        {256, 128, 1, 0, 6144},    {256, 64, 512, 4096, 0},
 };
 
 // RN_ERR_SHAPE for a layout no schedule serves.

@@ -261,10 +261,12 @@ def test_header_constants_are_the_bindings():
 def test_qk_schedule_selection_by_layout(lib):
     # host-only: the automatic pick by token count and layout, at its boundaries
     sel = binding.qk_norm_rope_select_schedule
-    assert [sel(T) for T in (1, 2, 3, 256, 257, 1023, 1024, 4096, 4097)] == [
+    assert [sel(T) for T in (1, 2, 3, 256, 257, 1023, 1024, 5120, 5121)] == [
         binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_HEAD_PER_WARP, binding.RN_QK_TWO_HEADS,
         binding.RN_QK_TWO_HEADS, binding.RN_QK_PERSISTENT, binding.RN_QK_PERSISTENT,
         binding.RN_QK_PAIRS, binding.RN_QK_PAIRS, binding.RN_QK_BULK]
+    assert sel(4096, 128, 64) == binding.RN_QK_PAIRS and sel(4097, 128, 64) == binding.RN_QK_BULK
+    assert sel(6144, 256, 128) == binding.RN_QK_PAIRS and sel(6145, 256, 128) == binding.RN_QK_BULK
     assert sel(1023, 128, 64) == binding.RN_QK_PERSISTENT and sel(1024, 128, 64) == binding.RN_QK_PAIRS
     assert sel(1791, 128, 32) == binding.RN_QK_PERSISTENT and sel(1792, 128, 32) == binding.RN_QK_PAIRS
     assert lib.qk_norm_rope_select_schedule(3000) == sel(3000, 128, 128)
