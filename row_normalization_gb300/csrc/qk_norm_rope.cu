@@ -474,9 +474,9 @@ __device__ __forceinline__ void qk_rotate(const uint32_t (&x1)[A2], const uint32
 // only when the two tokens differ), and the heads stay packed bf16 until they
 // are reduced: twice the heads in flight a warp for a quarter more registers.
 //
-// Lanes per head by layout (pair_lph): each lane's rotary pieces are 8
-// elements (16-byte loads) where the layout allows: 4 lanes at D 64, 8 at
-// D 128, 16 at D 256.  At 8 lanes for every D, a D 64 lane moved 8-byte
+// Lanes per head by layout (pair_lph): 4 lanes at D 64, 8 at D 128, 16 at
+// D 256, so that at full rotary each lane's two rotary pieces are 8 elements
+// (16-byte loads) at every D.  At 8 lanes for every D, a D 64 lane moved 8-byte
 // pieces and a D 256 lane held 32 cos/sin floats (two CTAs an SM): 0.70 and
 // 0.68 of the copy at 4096 tokens (D 64 rotary 64; D 256 rotary 256), against
 // 0.84 and 0.95 with 4 and 16 lanes.
