@@ -237,16 +237,45 @@ class ClockSampler:
 COUNTERS_FILE = os.path.join(ROOT, "profiles", "dram_counters.txt")
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of
+    whitespace made one space: what the compiler sees, so that editing a
+    comment does not change a kernel's digest.  String and character literals
+    (inline PTX) are kept as written."""
+    out = []
+    i, n = 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest(kernel: str) -> str:
-    """sha256[:16] of the sources a kernel is compiled from (its file and the
-    shared device helpers), which keys the recorded ncu counters."""
+    """sha256[:16] of the code a kernel is compiled from (its file and the
+    shared device helpers, comments and spacing aside), which keys the
+    recorded ncu counters."""
     csrc = os.path.join(ROOT, "row_normalization_gb300", "csrc")
     files = ["row_kernels.cuh" if kernel.startswith("rms") else "qk_norm_rope.cu",
              "rn_common.cuh"]
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
