@@ -1036,13 +1036,19 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
         case 1024: *g = {128, 1, 8, 2, 1, false}; break;
         case 2048: *g = {256, 1, 8, 2, 1, false}; break;
         case 4096:
-            // two CTAs per SM through 4096 rows, then one CTA with a third
-            // stage through 8192 rows, then two stages
+            // two CTAs per SM through 4096 rows, then one CTA with four stages
+            // through 8192 rows, then two stages.  Four stages measured even
+            // with three for a launch alone (0.843 against 0.847 of the copy
+            // at 8192 rows) and 7 us shorter inside a sequence of differently
+            // shaped launches, where the ring starts behind a wider one.
             *g = M <= 4096 ? BulkGeometry{256, 2, 4, 2, 2, false}
-                           : BulkGeometry{256, 2, 4, few_rows ? 3 : 2, 1, false};
+                           : BulkGeometry{256, 2, 4, few_rows ? 4 : 2, 1, false};
             break;
         case 8192: *g = {256, 4, 2, short_stages, 1, false}; break;
-        case 16384: *g = {512, 4, 1, short_stages, 1, false}; break;
+        // Three 32 KiB stages at every row count: with the dynamic unit order
+        // they measured 1% ahead of two from 8192 rows (32768 rows: 1.012 ->
+        // 1.024 of the copy).
+        case 16384: *g = {512, 4, 1, 3, 1, false}; break;
         case 32768: *g = {512, 8, 1, 2, 1, false}; break;
         default: return false;
     }
