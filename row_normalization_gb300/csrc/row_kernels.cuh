@@ -1037,12 +1037,14 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
         case 2048: *g = {256, 1, 8, 2, 1, false}; break;
         case 4096:
             // two CTAs per SM through 4096 rows, then one CTA with four stages
-            // through 8192 rows, then two stages.  Four stages measured even
-            // with three for a launch alone (0.843 against 0.847 of the copy
-            // at 8192 rows) and 7 us shorter inside a sequence of differently
-            // shaped launches, where the ring starts behind a wider one.
+            // (128 KiB in flight an SM).  Alone, four stages measured even with
+            // two or three (8192 rows: 0.843 against 0.847 of the copy; 32768
+            // rows: 0.979 against 0.983); inside a sequence of differently
+            // shaped launches, where the ring starts behind a wider one, 7 us
+            // shorter at 8192 rows, and 22 us for 16384 and 32768 rows together
+            // against two stages and one warp per row.
             *g = M <= 4096 ? BulkGeometry{256, 2, 4, 2, 2, false}
-                           : BulkGeometry{256, 2, 4, few_rows ? 4 : 2, 1, false};
+                           : BulkGeometry{256, 2, 4, 4, 1, false};
             break;
         case 8192: *g = {256, 4, 2, short_stages, 1, false}; break;
         // Three 32 KiB stages at every row count: with the dynamic unit order
@@ -1226,7 +1228,7 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     return RN_ERR_SHAPE;
 }
 
-static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &dev) {
+static int auto_schedule(int64_t M, int N, bool add, bool ln, bool l2, const DeviceInfo &dev) {
     BulkGeometry geo;
     // Up to 2048-wide rows one warp per row is ahead of the ring; wider rows
     // take the ring wherever it applies (3072-wide RMSNorm rows measured 0.85
@@ -1236,12 +1238,21 @@ static int auto_schedule(int64_t M, int N, bool add, bool ln, const DeviceInfo &
     // 4096-wide generic rows also stays on one CTA per row, which keeps twice
     // the loads in flight and measured ahead (0.94-0.97 against 0.89-0.94).
     if (N <= 2048 && M >= 4LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-    // RMSNorm / L2Norm rows up to 4096 wide over many rows (128 a SM and
-    // more): one warp per row, loads straight into registers, measured ahead
-    // of the ring (32768 x 4096: 0.94 -> 0.97, 32768 x 3584: 0.89 -> 0.97,
-    // 65536 x 4096: 0.97 -> 1.01 of the copy); with fewer rows the ring's
-    // deeper prefetch wins.
-    if (!add && !ln && N <= 4096 && M >= 128LL * dev.sm_count) return RN_SCHED_WARP_ROW;
+    // Rows up to 4096 wide over many rows: one warp per row, loads straight
+    // into registers.
+    //   L2Norm (no weights: more warps an SM) from 12 rows a SM, ahead of the
+    //     ring at every count measured from 2048 rows, 3072 or 4096 wide
+    //     (4096 x 4096: 0.80 -> 0.87, 12288 x 4096: 0.89 -> 0.94, 32768 x
+    //     4096: 0.98 -> 1.01 of the copy; even at 1024 rows).
+    //   RMSNorm at generic widths from 128 rows a SM (32768 x 3584: 0.89 ->
+    //     0.97).  RMSNorm 4096 wide stays on the ring, whose four stages there
+    //     are even with one warp per row alone (65536 rows: 1.01) or ahead
+    //     (24576 rows: 0.943 -> 0.958) and 11-12 us shorter a launch behind a
+    //     wider one (32768 rows).
+    if (!add && !ln && N <= 4096) {
+        if (l2 && M >= 12LL * dev.sm_count) return RN_SCHED_WARP_ROW;
+        if (!l2 && N != 4096 && M >= 128LL * dev.sm_count) return RN_SCHED_WARP_ROW;
+    }
     if (bulk_geometry(M, N, add, ln, &geo) && M >= 6LL * dev.sm_count &&
         !(add && geo.generic && N < 4096))
         return RN_SCHED_PERSIST_BULK;
@@ -1261,7 +1272,7 @@ static int rows_dispatch(const RowJob &j, int schedule, uint64_t timeout_ns, int
     const DeviceInfo *dev = current_device_info();
     if (!dev) return RN_ERR_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, LN, *dev);
+    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, LN, j.l2 != 0, *dev);
     switch (schedule) {
         case RN_SCHED_WARP_ROW: return launch_warp_rows<E, ADD, LN>(j, st, *dev);
         case RN_SCHED_CTA_ROW: return launch_cta_rows<E, ADD, LN>(j, st, *dev);
@@ -1307,7 +1318,7 @@ static int rows_select(int op, int64_t M, int64_t N) {
     if (check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
     const DeviceInfo *dev = current_device_info();
     if (!dev) return RN_ERR_DEVICE;
-    return auto_schedule(M, static_cast<int>(N), op == ROW_ADD_RMS, op == ROW_LN, *dev);
+    return auto_schedule(M, static_cast<int>(N), op == ROW_ADD_RMS, op == ROW_LN, op == ROW_L2, *dev);
 }
 
 // Reads (and optionally clears) this translation unit's status word; the

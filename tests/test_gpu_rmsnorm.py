@@ -164,13 +164,13 @@ def test_wait_timeout_reports_status_and_context_survives():
 # Full-size workloads, auto schedule (what the bench launches)
 # ---------------------------------------------------------------------------
 
-def _check_full_size(M, N, eps, outlier_frac, seed=0):
+def _check_full_size(M, N, eps, outlier_frac, seed=0, schedule=binding.RN_SCHED_AUTO):
     """The launch the bench times (with a workspace: the dynamic unit order),
     every element against the oracle; the fixed order gives the same bits."""
     x, w = rmsnorm_inputs(M, N, outlier_frac=outlier_frac, device="cuda", seed=seed)
     ws = binding.new_workspace()
-    y = binding.rmsnorm_fwd(x, w, eps, workspace=ws)
-    y_fixed = binding.rmsnorm_fwd(x, w, eps)
+    y = binding.rmsnorm_fwd(x, w, eps, workspace=ws, schedule=schedule)
+    y_fixed = binding.rmsnorm_fwd(x, w, eps, schedule=schedule)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y_fixed.view(torch.int16))
     assert int(ws.count_nonzero()) == 0
@@ -194,12 +194,23 @@ def test_sweep_full_size(M, N):
     _check_full_size(M, N, 1e-6, 0.01)
 
 
-@pytest.mark.parametrize("M,N", [(24576, 3072), (20480, 3584), (32768, 2560), (131072, 4096)])
+@pytest.mark.parametrize("M,N", [(24576, 3072), (20480, 3584), (32768, 2560)])
 def test_many_rows_up_to_4096_wide_take_one_warp_a_row(M, N):
-    # 128 rows an SM and more, 2049..4096 wide: one warp per row, 12 or 16
+    # 128 rows an SM and more, 2049..4095 wide: one warp per row, 12 or 16
     # chunks a lane (masked past the row end), chosen automatically
     assert binding.rmsnorm_select_schedule(M, N) == binding.RN_SCHED_WARP_ROW
     _check_full_size(M, N, 1e-6, 0.01)
+
+
+def test_many_rows_4096_wide_ring_and_one_warp_a_row():
+    # 4096 wide: RMSNorm takes the four-stage ring at every row count, L2Norm
+    # one warp per row from 12 rows an SM; the 16-chunk warp kernel is still
+    # checked at full size with its schedule forced
+    for M in (8192, 32768, 131072):
+        assert binding.rmsnorm_select_schedule(M, 4096) == binding.RN_SCHED_PERSIST_BULK
+    assert binding.row_norm_select_schedule(binding.RN_OP_L2NORM, 131072, 4096) == \
+        binding.RN_SCHED_WARP_ROW
+    _check_full_size(131072, 4096, 1e-6, 0.01, schedule=binding.RN_SCHED_WARP_ROW)
 
 
 @pytest.mark.parametrize("M", [1024, 4096, 8192])
