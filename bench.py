@@ -1034,6 +1034,13 @@ def run_reference(args) -> int:
 
 
 def main() -> int:
+    # The e2e pipeline copies in and out on their own streams.  The runtime
+    # multiplexes streams onto 8 hardware queues by default, and torch's
+    # stream pool can put the copy-in and copy-out streams on one queue, which
+    # serialises the two directions: 3 of 6 e2e runs at 140-200 GB/s against
+    # 328 with both directions busy.  With 32 queues, 6 of 6 ran at 328.  A
+    # setting of this process's runtime (read when CUDA starts), not of the GPU.
+    os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
