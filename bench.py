@@ -656,11 +656,10 @@ def run_ours(args) -> int:
     for k, c in enumerate(rms):
         op = ("add_rmsnorm" if "r" in c else "layernorm" if "b" in c else
               "l2norm" if "l2" in c else "rmsnorm")
-        select = {"add_rmsnorm": binding.add_rmsnorm_select_schedule,
-                  "layernorm": binding.layernorm_select_schedule,
-                  "l2norm": binding.rmsnorm_select_schedule,
-                  "rmsnorm": binding.rmsnorm_select_schedule}[op]
-        sched = FORCE["rms"] or select(c["M"], c["N"])
+        opcode = {"add_rmsnorm": binding.RN_OP_ADD_RMSNORM, "layernorm": binding.RN_OP_LAYERNORM,
+                  "l2norm": binding.RN_OP_L2NORM, "rmsnorm": binding.RN_OP_RMSNORM}[op]
+        sched = FORCE["rms"] or binding.row_norm_select_schedule(
+            opcode, c["M"], c["N"], workspace=WS["ws"] is not None)
         b = {"add_rmsnorm": add_bytes, "layernorm": ln_bytes, "l2norm": l2_bytes,
              "rmsnorm": rms_bytes}[op](c["M"], c["N"])
         per_shape.append({"op": op, "dtype": ROW_DTYPE, "M": c["M"], "N": c["N"],

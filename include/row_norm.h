@@ -260,6 +260,13 @@ int row_norm_fwd_ex(int op, int dtype, const void *x, const void *residual,
  * and (M, N) on the current device; the same for both formats. */
 int row_norm_select_schedule(int op, int64_t M, int64_t N);
 
+/* The same for the workspace forms (rmsnorm_fwd_ws, row_norm_fwd_ws under
+ * RN_SCHED_AUTO).  With a workspace the persistent ring can take its units in
+ * the dynamic order, and RMSNorm 4096 wide then stays on the ring at every
+ * row count, where the plain forms take one warp per row from 128 rows an SM.
+ * Host-only query: launches nothing. */
+int row_norm_select_schedule_ws(int op, int64_t M, int64_t N);
+
 /* ------------------------------------------------------------------------ */
 /* Fused Q/K RMSNorm + neox RoPE                                              */
 /* ------------------------------------------------------------------------ */

@@ -150,6 +150,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.row_norm_fwd_ex.restype = i32
         L.row_norm_select_schedule.argtypes = [i32, i64, i64]
         L.row_norm_select_schedule.restype = i32
+        L.row_norm_select_schedule_ws.argtypes = [i32, i64, i64]
+        L.row_norm_select_schedule_ws.restype = i32
         L.rn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.rn_device_status.restype = i32
         _lib = L
@@ -387,12 +389,14 @@ def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None, eps:
     return y
 
 
-def row_norm_select_schedule(op: int, M: int, N: int) -> int:
+def row_norm_select_schedule(op: int, M: int, N: int, *, workspace: bool = False) -> int:
     """The RN_SCHED_* schedule a row norm (RN_OP_*) picks for (M, N); the same
-    for both element formats."""
-    rc = int(load().row_norm_select_schedule(int(op), int(M), int(N)))
+    for both element formats.  workspace=True: the choice of the workspace
+    forms (the dynamic unit order is open to the ring)."""
+    name = "row_norm_select_schedule_ws" if workspace else "row_norm_select_schedule"
+    rc = int(getattr(load(), name)(int(op), int(M), int(N)))
     if rc < 0:
-        raise RowNormError("row_norm_select_schedule", rc)
+        raise RowNormError(name, rc)
     return rc
 
 
@@ -587,8 +591,11 @@ def rope_cos_sin_table(theta: float, max_pos: int, rotary_dim: int,
     return out
 
 
-def rmsnorm_select_schedule(M: int, N: int) -> int:
-    """The RN_SCHED_* schedule rmsnorm_fwd picks for (M, N) on the current device."""
+def rmsnorm_select_schedule(M: int, N: int, *, workspace: bool = False) -> int:
+    """The RN_SCHED_* schedule rmsnorm_fwd picks for (M, N) on the current
+    device; workspace=True: the schedule of rmsnorm_fwd with a workspace."""
+    if workspace:
+        return row_norm_select_schedule(RN_OP_RMSNORM, M, N, workspace=True)
     rc = int(load().rmsnorm_select_schedule(int(M), int(N)))
     if rc < 0:
         raise RowNormError("rmsnorm_select_schedule", rc)

@@ -84,7 +84,7 @@ int rows_run_bf16(const RowCall &c);
 int rows_run_f16(const RowCall &c);
 int rows_status_bf16(unsigned int *out, int clear);
 int rows_status_f16(unsigned int *out, int clear);
-int rows_select_schedule(int op, int64_t M, int64_t N);
+int rows_select_schedule(int op, int64_t M, int64_t N, bool ws = false);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -150,6 +150,11 @@ int row_norm_select_schedule(int op, int64_t M, int64_t N) {
     return rn::rows_select_schedule(op, M, N);
 }
 
+int row_norm_select_schedule_ws(int op, int64_t M, int64_t N) {
+    if (op < RN_OP_RMSNORM || op > RN_OP_LAYERNORM) return RN_ERR_ARG;
+    return rn::rows_select_schedule(op, M, N, true);
+}
+
 int rn_device_status(unsigned int *out, int clear) {
     if (!out) return RN_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) {

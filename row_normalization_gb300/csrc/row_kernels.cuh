@@ -991,7 +991,7 @@ static bool bulk_geometry_generic(int N, bool add, bool ln, BulkGeometry *g) {
     return true;
 }
 
-static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) {
+static bool bulk_geometry(int64_t M, int N, bool add, bool ln, bool dyn, BulkGeometry *g) {
     const bool few_rows = M <= 8192;
     if ((N & (N - 1)) != 0 || N < 1024) return bulk_geometry_generic(N, add, ln, g);
     if (ln) {
@@ -1036,21 +1036,25 @@ static bool bulk_geometry(int64_t M, int N, bool add, bool ln, BulkGeometry *g) 
         case 1024: *g = {128, 1, 8, 2, 1, false}; break;
         case 2048: *g = {256, 1, 8, 2, 1, false}; break;
         case 4096:
-            // two CTAs per SM through 4096 rows, then one CTA with four stages
-            // (128 KiB in flight an SM).  Alone, four stages measured even with
+            // Two CTAs per SM through 4096 rows, then one CTA.  In the dynamic
+            // unit order four stages (128 KiB in flight an SM): alone even with
             // two or three (8192 rows: 0.843 against 0.847 of the copy; 32768
-            // rows: 0.979 against 0.983); inside a sequence of differently
+            // rows: 0.979 against 0.983), and inside a sequence of differently
             // shaped launches, where the ring starts behind a wider one, 7 us
-            // shorter at 8192 rows, and 22 us for 16384 and 32768 rows together
-            // against two stages and one warp per row.
-            *g = M <= 4096 ? BulkGeometry{256, 2, 4, 2, 2, false}
-                           : BulkGeometry{256, 2, 4, 4, 1, false};
+            // shorter at 8192 rows and 22 us for 16384 and 32768 rows together
+            // (against two stages and one warp per row).  In the fixed order
+            // four stages measured 3-10% slower alone (32768 rows: 0.969 ->
+            // 0.876): three stages through 8192 rows, then two.
+            if (M <= 4096)
+                *g = BulkGeometry{256, 2, 4, 2, 2, false};
+            else
+                *g = BulkGeometry{256, 2, 4, dyn ? 4 : (few_rows ? 3 : 2), 1, false};
             break;
         case 8192: *g = {256, 4, 2, short_stages, 1, false}; break;
-        // Three 32 KiB stages at every row count: with the dynamic unit order
-        // they measured 1% ahead of two from 8192 rows (32768 rows: 1.012 ->
-        // 1.024 of the copy).
-        case 16384: *g = {512, 4, 1, 3, 1, false}; break;
+        // Three 32 KiB stages at every row count in the dynamic unit order,
+        // 1% ahead of two from 8192 rows (32768 rows: 1.012 -> 1.024 of the
+        // copy); in the fixed order two from 8192 rows (three: 0.992 -> 0.962).
+        case 16384: *g = {512, 4, 1, dyn ? 3 : short_stages, 1, false}; break;
         case 32768: *g = {512, 8, 1, 2, 1, false}; break;
         default: return false;
     }
@@ -1166,7 +1170,14 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     constexpr int NIN = ADD ? 2 : 1;
     BulkGeometry geo;
     const int N = j.N;
-    if (!bulk_geometry(j.M, N, ADD, LN, &geo)) return RN_ERR_SHAPE;
+    // The geometry for the dynamic unit order when the kernel will take it: a
+    // workspace, and six units a CTA or more (the kernel's own test).
+    bool dyn = !LN && j.ws != nullptr;
+    if (!bulk_geometry(j.M, N, ADD, LN, dyn, &geo)) return RN_ERR_SHAPE;
+    if (dyn && (j.M + geo.R - 1) / geo.R < 6LL * dev.sm_count * geo.ctas) {
+        dyn = false;
+        bulk_geometry(j.M, N, ADD, LN, dyn, &geo);
+    }
     const int smem_cap = dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448;
     if constexpr (LN) {
         if (geo.generic && (debug_flags & 0x1FF0) == 0) ln_multi_cta_layout<E>(N, smem_cap, &geo);
@@ -1228,7 +1239,8 @@ static int launch_persistent_bulk(const RowJob &j, cudaStream_t st, const Device
     return RN_ERR_SHAPE;
 }
 
-static int auto_schedule(int64_t M, int N, bool add, bool ln, bool l2, const DeviceInfo &dev) {
+static int auto_schedule(int64_t M, int N, bool add, bool ln, bool l2, bool ws,
+                         const DeviceInfo &dev) {
     BulkGeometry geo;
     // Up to 2048-wide rows one warp per row is ahead of the ring; wider rows
     // take the ring wherever it applies (3072-wide RMSNorm rows measured 0.85
@@ -1244,16 +1256,16 @@ static int auto_schedule(int64_t M, int N, bool add, bool ln, bool l2, const Dev
     //     ring at every count measured from 2048 rows, 3072 or 4096 wide
     //     (4096 x 4096: 0.80 -> 0.87, 12288 x 4096: 0.89 -> 0.94, 32768 x
     //     4096: 0.98 -> 1.01 of the copy; even at 1024 rows).
-    //   RMSNorm at generic widths from 128 rows a SM (32768 x 3584: 0.89 ->
-    //     0.97).  RMSNorm 4096 wide stays on the ring, whose four stages there
-    //     are even with one warp per row alone (65536 rows: 1.01) or ahead
-    //     (24576 rows: 0.943 -> 0.958) and 11-12 us shorter a launch behind a
-    //     wider one (32768 rows).
+    //   RMSNorm from 128 rows a SM (32768 x 3584: 0.89 -> 0.97), except 4096
+    //     wide with a workspace: there the ring's four stages in the dynamic
+    //     unit order are even with one warp per row alone (65536 rows: 1.01)
+    //     or ahead (24576 rows: 0.943 -> 0.958), and 11-12 us shorter a
+    //     launch behind a wider one (32768 rows).
     if (!add && !ln && N <= 4096) {
         if (l2 && M >= 12LL * dev.sm_count) return RN_SCHED_WARP_ROW;
-        if (!l2 && N != 4096 && M >= 128LL * dev.sm_count) return RN_SCHED_WARP_ROW;
+        if (!l2 && !(ws && N == 4096) && M >= 128LL * dev.sm_count) return RN_SCHED_WARP_ROW;
     }
-    if (bulk_geometry(M, N, add, ln, &geo) && M >= 6LL * dev.sm_count &&
+    if (bulk_geometry(M, N, add, ln, ws, &geo) && M >= 6LL * dev.sm_count &&
         !(add && geo.generic && N < 4096))
         return RN_SCHED_PERSIST_BULK;
     if (N <= 2048 && M < 64) return RN_SCHED_WARP_ROW;
@@ -1272,7 +1284,8 @@ static int rows_dispatch(const RowJob &j, int schedule, uint64_t timeout_ns, int
     const DeviceInfo *dev = current_device_info();
     if (!dev) return RN_ERR_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (schedule == RN_SCHED_AUTO) schedule = auto_schedule(j.M, j.N, ADD, LN, j.l2 != 0, *dev);
+    if (schedule == RN_SCHED_AUTO)
+        schedule = auto_schedule(j.M, j.N, ADD, LN, j.l2 != 0, j.ws != nullptr, *dev);
     switch (schedule) {
         case RN_SCHED_WARP_ROW: return launch_warp_rows<E, ADD, LN>(j, st, *dev);
         case RN_SCHED_CTA_ROW: return launch_cta_rows<E, ADD, LN>(j, st, *dev);
@@ -1314,11 +1327,12 @@ static int rows_run(const RowCall &c) {
 
 // The schedule rows_run picks in RN_SCHED_AUTO (the same for both formats:
 // only the element size enters the geometry).
-static int rows_select(int op, int64_t M, int64_t N) {
+static int rows_select(int op, int64_t M, int64_t N, bool ws) {
     if (check_rows(M, N) != RN_OK) return RN_ERR_SHAPE;
     const DeviceInfo *dev = current_device_info();
     if (!dev) return RN_ERR_DEVICE;
-    return auto_schedule(M, static_cast<int>(N), op == ROW_ADD_RMS, op == ROW_LN, op == ROW_L2, *dev);
+    return auto_schedule(M, static_cast<int>(N), op == ROW_ADD_RMS, op == ROW_LN, op == ROW_L2, ws,
+                         *dev);
 }
 
 // Reads (and optionally clears) this translation unit's status word; the

@@ -11,7 +11,7 @@ int rows_run_bf16(const RowCall &c) { return rows_run<Bf16>(c); }
 
 int rows_status_bf16(unsigned int *out, int clear) { return rows_status_word(out, clear); }
 
-int rows_select_schedule(int op, int64_t M, int64_t N) { return rows_select(op, M, N); }
+int rows_select_schedule(int op, int64_t M, int64_t N, bool ws) { return rows_select(op, M, N, ws); }
 
 // ---- scratch for rmsnorm_fwd_noalloc ----------------------------------------
 // The dynamic unit order of the row ring keeps two counters in device memory

@@ -166,19 +166,28 @@ def test_wait_timeout_reports_status_and_context_survives():
 
 def _check_full_size(M, N, eps, outlier_frac, seed=0, schedule=binding.RN_SCHED_AUTO):
     """The launch the bench times (with a workspace: the dynamic unit order),
-    every element against the oracle; the fixed order gives the same bits."""
+    every element against the oracle.  The plain form gives the same bits
+    when it takes the same schedule (the unit order and the stage count do
+    not change a row's arithmetic); where it takes another (RMSNorm 4096 wide
+    over many rows: one warp per row), its output is compared in full too."""
     x, w = rmsnorm_inputs(M, N, outlier_frac=outlier_frac, device="cuda", seed=seed)
     ws = binding.new_workspace()
     y = binding.rmsnorm_fwd(x, w, eps, workspace=ws, schedule=schedule)
-    y_fixed = binding.rmsnorm_fwd(x, w, eps, schedule=schedule)
+    y_plain = binding.rmsnorm_fwd(x, w, eps, schedule=schedule)
     torch.cuda.synchronize()
-    assert torch.equal(y.view(torch.int16), y_fixed.view(torch.int16))
     assert int(ws.count_nonzero()) == 0
-    del y_fixed
-    xb, wb, got = bf16_bits(x), bf16_bits(w), bf16_bits(y)
-    del x, y
-    assert_full_parity(got, lambda a, b: (None, oracle.rmsnorm(xb[a:b], wb, eps)),
-                       f"full size M={M} N={N}")
+    same = schedule != binding.RN_SCHED_AUTO or \
+        binding.rmsnorm_select_schedule(M, N, workspace=True) == binding.rmsnorm_select_schedule(M, N)
+    if same:
+        assert torch.equal(y.view(torch.int16), y_plain.view(torch.int16))
+        outs = [("", bf16_bits(y))]
+    else:
+        outs = [(" workspace", bf16_bits(y)), (" plain", bf16_bits(y_plain))]
+    xb, wb = bf16_bits(x), bf16_bits(w)
+    del x, y, y_plain
+    for tag, got in outs:
+        assert_full_parity(got, lambda a, b: (None, oracle.rmsnorm(xb[a:b], wb, eps)),
+                           f"full size M={M} N={N}{tag}")
 
 
 def test_latency_config_full():
@@ -203,14 +212,19 @@ def test_many_rows_up_to_4096_wide_take_one_warp_a_row(M, N):
 
 
 def test_many_rows_4096_wide_ring_and_one_warp_a_row():
-    # 4096 wide: RMSNorm takes the four-stage ring at every row count, L2Norm
-    # one warp per row from 12 rows an SM; the 16-chunk warp kernel is still
-    # checked at full size with its schedule forced
+    # 4096 wide: RMSNorm with a workspace takes the four-stage ring at every
+    # row count, without one one warp per row from 128 rows an SM; L2Norm one
+    # warp per row from 12 rows an SM either way
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for M in (8192, 32768, 131072):
-        assert binding.rmsnorm_select_schedule(M, 4096) == binding.RN_SCHED_PERSIST_BULK
-    assert binding.row_norm_select_schedule(binding.RN_OP_L2NORM, 131072, 4096) == \
-        binding.RN_SCHED_WARP_ROW
-    _check_full_size(131072, 4096, 1e-6, 0.01, schedule=binding.RN_SCHED_WARP_ROW)
+        assert binding.rmsnorm_select_schedule(M, 4096, workspace=True) == \
+            binding.RN_SCHED_PERSIST_BULK
+    assert binding.rmsnorm_select_schedule(128 * sms - 8, 4096) == binding.RN_SCHED_PERSIST_BULK
+    assert binding.rmsnorm_select_schedule(128 * sms, 4096) == binding.RN_SCHED_WARP_ROW
+    for ws in (False, True):
+        assert binding.row_norm_select_schedule(binding.RN_OP_L2NORM, 12 * sms, 4096,
+                                                workspace=ws) == binding.RN_SCHED_WARP_ROW
+    _check_full_size(131072, 4096, 1e-6, 0.01)
 
 
 @pytest.mark.parametrize("M", [1024, 4096, 8192])
