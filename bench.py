@@ -584,6 +584,11 @@ def run_ours(args) -> int:
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
     torch.cuda.set_device(local)
+    # The e2e pipeline's three streams are the first this process creates.  A
+    # stream taken from torch's pool late in the run can share a hardware
+    # queue with another, which serialises the two copy directions (one of
+    # three e2e runs at 134 GB/s, against 328 with streams taken first).
+    e2e_streams = tuple(torch.cuda.Stream() for _ in range(3))
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
@@ -707,7 +712,8 @@ def run_ours(args) -> int:
     plain = not ADD_SHAPES and not LN_SHAPES and not L2_SHAPES and ROW_DTYPE == "bf16"
     configs = config_points(torch, binding, inputs, hbm_peak) \
         if plain and WORKLOAD.startswith("rmsnorm sweep") and args.steady_reps > 0 else None
-    e2e = run_e2e(torch, binding, rms, qk, args, dist, device) if args.e2e_steps > 0 and plain \
+    e2e = run_e2e(torch, binding, rms, qk, args, dist, device, e2e_streams) \
+        if args.e2e_steps > 0 and plain \
         else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and plain:
@@ -768,7 +774,7 @@ def run_ours(args) -> int:
 E2E_CHUNK_BYTES = 64 << 20
 
 
-def link_copy_gbs(torch, device, nbytes: int = 512 << 20, reps: int = 5) -> float:
+def link_copy_gbs(torch, device, nbytes: int = 512 << 20, reps: int = 5, streams=None) -> float:
     """What this host link carries with both directions busy: one pinned
     host-to-device and one device-to-host copy of `nbytes` each, on two
     streams at once, median of `reps` (GB/s, both directions added up).  The
@@ -778,7 +784,7 @@ def link_copy_gbs(torch, device, nbytes: int = 512 << 20, reps: int = 5) -> floa
     hout = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     din = torch.empty(nbytes, dtype=torch.uint8, device=device)
     dout = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    s1, s2 = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    s1, s2 = streams or (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
     times = []
     for _ in range(reps + 1):
         torch.cuda.synchronize()
@@ -801,7 +807,7 @@ def link_copy_gbs(torch, device, nbytes: int = 512 << 20, reps: int = 5) -> floa
     return 2 * nbytes / (ms * 1e-3) / 1e9
 
 
-def run_e2e(torch, binding, rms, qk, args, dist, device):
+def run_e2e(torch, binding, rms, qk, args, dist, device, streams=None):
     """The same step with host buffers, through the same C entry points.
 
     Every step copies each activation (x, qkv, positions) in from pinned host
@@ -811,7 +817,7 @@ def run_e2e(torch, binding, rms, qk, args, dist, device):
     two copy directions and the kernels overlap.  Weights and the cos/sin
     table stay resident."""
     world = dist.get_world_size() if dist else 1
-    s_in, s_comp, s_out = (torch.cuda.Stream(device=device) for _ in range(3))
+    s_in, s_comp, s_out = streams or tuple(torch.cuda.Stream(device=device) for _ in range(3))
 
     # one entry per chunk: (kind, device views, pinned host views, launch args)
     chunks = []
@@ -835,7 +841,7 @@ def run_e2e(torch, binding, rms, qk, args, dist, device):
               for k, _, _, h in chunks)
     d2h = sum((h[1] if k == "rms" else h[2]).numel() * 2 for k, _, _, h in chunks)
 
-    link_peak = link_copy_gbs(torch, device)
+    link_peak = link_copy_gbs(torch, device, streams=(s_in, s_out))
 
     n = len(chunks)
     done_comp = [None] * n  # kernel of the previous step on this chunk (WAR for the copy in)
@@ -1034,11 +1040,12 @@ def run_reference(args) -> int:
 
 def main() -> int:
     # The e2e pipeline copies in and out on their own streams.  The runtime
-    # multiplexes streams onto 8 hardware queues by default, and torch's
-    # stream pool can put the copy-in and copy-out streams on one queue, which
-    # serialises the two directions: 3 of 6 e2e runs at 140-200 GB/s against
-    # 328 with both directions busy.  With 32 queues, 6 of 6 ran at 328.  A
-    # setting of this process's runtime (read when CUDA starts), not of the GPU.
+    # multiplexes streams onto 8 hardware queues by default, and the copy-in
+    # and copy-out streams can land on one queue, which serialises the two
+    # directions: 3 of 6 e2e runs at 140-200 GB/s against 328 with both
+    # directions busy.  32 queues, and the e2e streams created first (run_ours),
+    # keep them apart.  A setting of this process's runtime (read when CUDA
+    # starts), not of the GPU.
     os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
