@@ -584,11 +584,6 @@ def run_ours(args) -> int:
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
     torch.cuda.set_device(local)
-    # The e2e pipeline's three streams are the first this process creates.  A
-    # stream taken from torch's pool late in the run can share a hardware
-    # queue with another, which serialises the two copy directions (one of
-    # three e2e runs at 134 GB/s, against 328 with streams taken first).
-    e2e_streams = tuple(torch.cuda.Stream() for _ in range(3))
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
@@ -712,8 +707,7 @@ def run_ours(args) -> int:
     plain = not ADD_SHAPES and not LN_SHAPES and not L2_SHAPES and ROW_DTYPE == "bf16"
     configs = config_points(torch, binding, inputs, hbm_peak) \
         if plain and WORKLOAD.startswith("rmsnorm sweep") and args.steady_reps > 0 else None
-    e2e = run_e2e(torch, binding, rms, qk, args, dist, device, e2e_streams) \
-        if args.e2e_steps > 0 and plain \
+    e2e = run_e2e(torch, binding, rms, qk, args, dist, device) if args.e2e_steps > 0 and plain \
         else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and plain:
@@ -1039,14 +1033,6 @@ def run_reference(args) -> int:
 
 
 def main() -> int:
-    # The e2e pipeline copies in and out on their own streams.  The runtime
-    # multiplexes streams onto 8 hardware queues by default, and the copy-in
-    # and copy-out streams can land on one queue, which serialises the two
-    # directions: 3 of 6 e2e runs at 140-200 GB/s against 328 with both
-    # directions busy.  32 queues, and the e2e streams created first (run_ours),
-    # keep them apart.  A setting of this process's runtime (read when CUDA
-    # starts), not of the GPU.
-    os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
