@@ -7,6 +7,7 @@ only rank 0 runs.  No GPU is involved here.
 """
 from __future__ import annotations
 
+import json
 import os
 import socket
 import subprocess
@@ -70,3 +71,24 @@ def test_reference_arm_runs_on_rank_zero_only():
                          text=True, timeout=300, cwd=ROOT)
     assert res.returncode == 0
     assert res.stdout.strip() == ""
+
+
+def test_reference_arm_prints_the_contract_line():
+    # rank 0 of the reference arm: one JSON line with the contract's keys, the
+    # oracle timed on the host cores, and an e2e that copies nothing
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "1"], env=env, capture_output=True,
+                         text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["value"] > 0 and d["unit"] == "GB/s" and d["steps"] == 2 and d["warmup"] == 1
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
